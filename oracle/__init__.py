@@ -1,0 +1,139 @@
+"""TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle of the KDA token step.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+leg of ``bench.py`` may import this package.  The CUDA library never calls it
+and shares no code with it.
+
+``build()`` compiles ``kda_oracle.c`` with gcc into ``oracle/_build``;
+``run()`` wraps the C entry point for numpy float64 arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libkda_oracle.so")
+_libs: dict = {}
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (plain C, IEEE double, no fast-math) and return the .so path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    hdr = os.path.join(_HERE, "kda_oracle.h")
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(hdr))
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-fPIC", "-shared",
+             "-fno-fast-math", "-ffp-contract=off",
+             "-o", tmp, _SRC, "-lm", "-lpthread"],
+            check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def build_variant(src_text: str, tag: str) -> str:
+    """Compile another version of the oracle source (used by the mutation tests
+    that check the pins catch planted mistakes).  Returns the .so path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    src = os.path.join(_BUILD, f"variant_{tag}.c")
+    with open(src, "w") as f:
+        f.write(src_text)
+    out = os.path.join(_BUILD, f"libkda_oracle_{tag}.so")
+    subprocess.run(
+        ["gcc", "-O1", "-std=c11", "-D_GNU_SOURCE", "-fPIC", "-shared",
+         "-fno-fast-math", "-ffp-contract=off", f"-I{_HERE}",
+         "-o", out, src, "-lm", "-lpthread"], check=True)
+    return out
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def _load(lib_path: str | None = None):
+    path = lib_path or build()
+    if path not in _libs:
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        lib.kda_oracle_run.restype = ctypes.c_int
+        lib.kda_oracle_run.argtypes = (
+            [ctypes.c_int] * 4 + [dp] * 10 + [ctypes.c_double] * 2 + [dp] * 9 + [ctypes.c_int])
+        lib.kda_oracle_cpu_count.restype = ctypes.c_int
+        lib.kda_oracle_cpu_count.argtypes = []
+        _libs[path] = lib
+    return _libs[path]
+
+
+def cpu_count() -> int:
+    return int(_load().kda_oracle_cpu_count())
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.dtype == np.float64 and a.flags["C_CONTIGUOUS"], "oracle wants C-contiguous float64"
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+@dataclass
+class OracleOut:
+    o: np.ndarray
+    o_pre: np.ndarray
+    S: np.ndarray
+    conv_state: np.ndarray
+    qhat: np.ndarray | None = None
+    khat: np.ndarray | None = None
+    vconv: np.ndarray | None = None
+    gk: np.ndarray | None = None
+    beta: np.ndarray | None = None
+
+
+def _f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def run(q, k, v, z, beta_logit, gate_logit, conv_w, dt_bias, A_log, gamma,
+        conv_state, S, *, l2_eps=1e-6, rms_eps=1e-6, intermediates=False,
+        nthreads=1, lib_path: str | None = None) -> OracleOut:
+    """Run T tokens of the KDA step for every (sequence, head).
+
+    q, k, v, z, gate_logit: [B, T, H, d]; beta_logit: [B, T, H];
+    conv_w: [3, H*d, 4]; dt_bias, A_log, gamma: [H, d];
+    conv_state: [B, 3, 3*H*d]; S: [B, H, d, d].  Inputs are copied to
+    float64 (exact for fp32 and bf16 values); S and conv_state are returned
+    updated, the caller's arrays are left untouched.
+    """
+    q, k, v, z, gate_logit = (_f64(a) for a in (q, k, v, z, gate_logit))
+    beta_logit, conv_w, dt_bias, A_log, gamma = (
+        _f64(a) for a in (beta_logit, conv_w, dt_bias, A_log, gamma))
+    B, T, H, d = q.shape
+    for a in (k, v, z, gate_logit):
+        assert a.shape == (B, T, H, d)
+    assert beta_logit.shape == (B, T, H)
+    assert conv_w.shape == (3, H * d, 4)
+    for a in (dt_bias, A_log, gamma):
+        assert a.shape == (H, d)
+    cs = _f64(conv_state).copy()
+    St = _f64(S).copy()
+    assert cs.shape == (B, 3, 3 * H * d) and St.shape == (B, H, d, d)
+    o = np.zeros((B, T, H, d))
+    o_pre = np.zeros((B, T, H, d))
+    extra = [np.zeros((B, T, H, d)) for _ in range(4)] + [np.zeros((B, T, H))] \
+        if intermediates else [None] * 5
+    rc = _load(lib_path).kda_oracle_run(
+        B, T, H, d, _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta_logit),
+        _ptr(gate_logit), _ptr(conv_w), _ptr(dt_bias), _ptr(A_log), _ptr(gamma),
+        float(l2_eps), float(rms_eps), _ptr(cs), _ptr(St), _ptr(o), _ptr(o_pre),
+        *[_ptr(e) for e in extra], int(nthreads))
+    if rc != 0:
+        raise ValueError(f"kda_oracle_run rejected its arguments (rc={rc})")
+    return OracleOut(o, o_pre, St, cs, *extra)

@@ -1,0 +1,57 @@
+/*
+ * kda_oracle.h -- TEST INFRASTRUCTURE ONLY.
+ *
+ * Plain, sequential, double-precision CPU definition of the Kimi Delta
+ * Attention (KDA) token step.  Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library; the product path never
+ * does.  It shares no code, header or constant with the CUDA library.
+ *
+ * Sources (page title, then section/table/row):
+ *   "Kimi K3 Metal Gap Analysis", section 2 "KDA Attention (kda_forward)",
+ *     rows "Conv4 + SiLU", "L2 normalize q/k", "Decay compute",
+ *     "Recurrence", "O projection".
+ *   "Metal (Apple GPU) backend for Kimi K3", table "What runs where (per
+ *     layer)" (low-rank fa/fb/bp feed the decay and beta) and section
+ *     "Correctness" (token-0 zero-state identity, which fixes beta and the
+ *     read-out-after-update order).
+ *
+ * All arrays are dense, row-major, double, host memory, owned by the caller.
+ * Shapes (B sequences, T tokens, H heads, d = head dimension):
+ *   q, k, v, z, gate_logit : [B][T][H][d]      (pre-conv q/k/v)
+ *   beta_logit             : [B][T][H]
+ *   conv_w                 : [3][H*d][4]       (q, k, v; tap 3 = current token)
+ *   dt_bias, A_log, gamma  : [H][d]
+ *   conv_state             : [B][3][3*H*d]     (oldest tap first; in/out)
+ *   S                      : [B][H][d][d]      (row = key channel, col = value channel; in/out)
+ *   o, o_pre               : [B][T][H][d]      (o_pre may be NULL)
+ *   qhat, khat, vconv, gk  : [B][T][H][d]      (optional intermediates, may be NULL)
+ *   beta                   : [B][T][H]         (optional, may be NULL)
+ */
+#ifndef KDA_ORACLE_H
+#define KDA_ORACLE_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Returns 0 on success, -1 on a bad argument. */
+int kda_oracle_run(int B, int T, int H, int d,
+                   const double *q, const double *k, const double *v,
+                   const double *z, const double *beta_logit,
+                   const double *gate_logit,
+                   const double *conv_w, const double *dt_bias,
+                   const double *A_log, const double *gamma,
+                   double l2_eps, double rms_eps,
+                   double *conv_state, double *S,
+                   double *o, double *o_pre,
+                   double *qhat, double *khat, double *vconv,
+                   double *gk, double *beta,
+                   int nthreads);
+
+/* Number of hardware threads this process may run on (sched affinity). */
+int kda_oracle_cpu_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

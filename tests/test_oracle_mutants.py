@@ -1,0 +1,51 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check that
+the pins catch every one of them."""
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+# (name, text in the oracle source, replacement)
+MUTANTS = [
+    ("no_decay", "S[(size_t)i * d + j] *= a[i];", "S[(size_t)i * d + j] *= 1.0;"),
+    ("decay_on_columns", "S[(size_t)i * d + j] *= a[i];", "S[(size_t)i * d + j] *= a[j];"),
+    ("decay_sign", "gkv[c] = -exp(", "gkv[c] = exp("),
+    ("no_beta_on_erase", "-beta * kv[i] * u[j]", "-kv[i] * u[j]"),
+    ("no_erase", "-beta * kv[i] * u[j]", "0.0"),
+    ("readout_transposed", "s += S[(size_t)i * d + j] * qv[i];", "s += S[(size_t)j * d + i] * qv[i];"),
+    ("taps_reversed", "w[0] * x_m3 + w[1] * x_m2 + w[2] * x_m1 + w[3] * x_t[c]",
+     "w[3] * x_m3 + w[2] * x_m2 + w[1] * x_m1 + w[0] * x_t[c]"),
+    ("no_silu", "y[c] = silu(pre);", "y[c] = pre;"),
+    ("k_not_normalised", "l2_normalize(kv, d, J->l2_eps);", ""),
+    ("window_not_shifted", "win[2 * HD3 + ch] = x_t[c];", "win[2 * HD3 + ch] = x_m1;"),
+    ("rms_sum_not_mean", "ms /= d;", ""),
+    ("no_gate", "* inv_rms *\n                            sigmoid(J->gate_logit[row + j]);", "* inv_rms;"),
+    ("erase_uses_q", "s += kv[i] * S[(size_t)i * d + j];", "s += qv[i] * S[(size_t)i * d + j];"),
+    ("write_uses_q", "beta * kv[i] * vv[j]", "beta * qv[i] * vv[j]"),
+    ("no_softplus", "softplus(J->z[row + c] + J->dt_bias[(size_t)h * d + c])",
+     "(J->z[row + c] + J->dt_bias[(size_t)h * d + c])"),
+    ("no_dt_bias", " + J->dt_bias[(size_t)h * d + c]", ""),
+    ("no_gamma", "J->gamma[(size_t)h * d + j] * op[j]", "op[j]"),
+    ("beta_not_squashed", "sigmoid(J->beta_logit[bth])", "(J->beta_logit[bth])"),
+    ("l2_eps_dropped", "1.0 / sqrt(ss + eps)", "1.0 / sqrt(ss)"),
+    ("rms_eps_dropped", "sqrt(ms + J->rms_eps)", "sqrt(ms)"),
+    ("exp_alog_dropped", "-exp(J->A_log[(size_t)h * d + c])", "-(J->A_log[(size_t)h * d + c])"),
+]
+
+
+def _fails(lib):
+    failed = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+    return failed
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new):
+    src = oracle.source()
+    assert src.count(old) == 1, f"mutation site for {name} not unique/found"
+    lib = oracle.build_variant(src.replace(old, new), name)
+    assert _fails(lib), f"no pin catches the planted mistake {name}"
