@@ -1,0 +1,522 @@
+#!/usr/bin/env python
+"""Benchmark of the KDA token step on GB300 (one JSON line on stdout).
+
+Headline: batched decode, 64 sequences x 32 heads x d=128, one token per call
+(fp32 state, 128 MiB), metric = state GB/s (2 * d * d * 4 bytes per sequence,
+head and token, over the device time of one call).  L2 is flushed between
+timed calls (a 256 MiB write, then a 256 MiB read).  The line also carries
+the batched prefill (8 x 64 heads x 8192 tokens, chunk 64, bf16 q/k/v) as
+tokens/s, each with its roofline, an end-to-end figure through the C ABI with
+host buffers, and the fp64 CPU oracle timed on this host's cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (torchrun), each rank runs an independent replica of the workload
+on its own GPU (the (sequence, head) units never interact); value is the
+units of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA decode state GB/s (% of HBM peak); prefill tokens/s (% tensor peak)"
+DECODE_WL = "decode_b64_h32_x256"
+PREFILL_WL = "prefill_b8_h64_t8192"
+D = 128
+STATE_BYTES = 2 * D * D * 4          # read + write of one 128x128 fp32 state
+FLUSH_BYTES = 256 << 20
+PREFILL_FLOP_PER_TOKEN_HEAD = 140.6e3  # algorithmic, triangles counted once
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "src": "fallback"}
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "kda_delta_rule_token_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(md_name, sha):
+    """DRAM bytes per launch recorded by an ncu capture in profiles/<md_name>,
+    or None when missing or taken on another version of the kernel source."""
+    p = os.path.join(ROOT, "profiles", md_name)
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m_sha = re.search(r"kernel source sha256\[:16\]:\s*([0-9a-f]{16})", text)
+    m_tr = re.search(r"dram bytes per launch \(full workload\):\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != sha:
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of the SM clock and throttle reasons."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Ours:
+    def __init__(self, args, world, rank, local):
+        import torch
+        import kda_delta_rule_token_gb300 as kda
+        from kda_delta_rule_token_gb300 import synth
+        self.torch, self.kda, self.synth = torch, kda, synth
+        self.args, self.world, self.rank = args, world, rank
+        torch.cuda.set_device(local)
+        self.dev = torch.device("cuda", local)
+        self.local = local
+        kda.load()
+        self.stream = torch.cuda.current_stream()
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl", device_id=self.dev)
+            self.dist = dist
+        else:
+            self.dist = None
+        self.flush_w = torch.empty(FLUSH_BYTES // 4, device=self.dev)
+        self.flush_r = torch.ones(FLUSH_BYTES // 4, device=self.dev)
+        self.sink = torch.empty((), device=self.dev)
+
+    def barrier_sync(self):
+        self.torch.cuda.synchronize()
+        if self.dist is not None:
+            self.dist.barrier()
+        self.torch.cuda.synchronize()
+
+    def max_over_ranks(self, x):
+        if self.dist is None:
+            return x
+        t = self.torch.tensor([x], device=self.dev, dtype=self.torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def flush_l2(self):
+        self.flush_w.fill_(1.0)
+        self.torch.sum(self.flush_r, out=self.sink)
+
+    # ---------------------------------------------------------------- decode
+    def decode(self):
+        torch, kda, synth = self.torch, self.kda, self.synth
+        wl = synth.WORKLOADS[DECODE_WL]
+        p = synth.make_params(wl, self.dev)
+        tk = synth.make_tokens(wl, self.dev)
+        st = synth.make_state(wl, self.dev)
+        S, cs = st["S"], st["conv_state"]
+        B, H = wl.B, wl.H
+        o = torch.empty((B, H, D), device=self.dev)
+        ctx = kda.kda_create(H, p["conv_w"], p["dt_bias"], p["A_log"], p["gamma"])
+        K, W = self.args.steps, self.args.warmup
+
+        def step(i, out=o):
+            t = i % wl.T
+            kda.kda_decode_step(ctx, B, tk["q"][t], tk["k"][t], tk["v"][t], tk["z"][t],
+                                tk["beta_logit"][t], tk["gate_logit"][t], cs, S, out,
+                                None, self.stream)
+
+        for i in range(W):
+            self.flush_l2()
+            step(i)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        self.barrier_sync()
+        l0 = kda.kda_launch_count()
+        t_wall = time.perf_counter()
+        for i in range(K):
+            self.flush_l2()
+            ev[i][0].record(self.stream)
+            step(W + i)
+            ev[i][1].record(self.stream)
+        self.barrier_sync()
+        t_wall = time.perf_counter() - t_wall
+        launches = kda.kda_launch_count() - l0
+        times = [a.elapsed_time(b) for a, b in ev]
+        ms = self.max_over_ranks(statistics.fmean(times))
+        assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
+
+        # End to end through the C ABI with pinned host buffers: copy this
+        # call's inputs in, run, copy o out, all inside the timed region.
+        nh = min(8, wl.T)
+        host = [{n: tk[n][t].to("cpu").pin_memory() for n in
+                 ("q", "k", "v", "z", "beta_logit", "gate_logit")} for t in range(nh)]
+        dbuf = {n: torch.empty_like(tk[n][0]) for n in host[0]}
+        o_host = torch.empty((B, H, D), pin_memory=True)
+        h2d = sum(x.numel() * x.element_size() for x in host[0].values())
+        d2h = o_host.numel() * 4
+        Ke = max(3, min(K, 200))
+        eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(Ke)]
+        for i in range(W + Ke):
+            self.flush_l2()
+            if i >= W:
+                eve[i - W][0].record(self.stream)
+            hb = host[i % nh]
+            for n in hb:
+                dbuf[n].copy_(hb[n], non_blocking=True)
+            kda.kda_decode_step(ctx, B, dbuf["q"], dbuf["k"], dbuf["v"], dbuf["z"],
+                                dbuf["beta_logit"], dbuf["gate_logit"], cs, S, o, None,
+                                self.stream)
+            o_host.copy_(o, non_blocking=True)
+            if i >= W:
+                eve[i - W][1].record(self.stream)
+        self.barrier_sync()
+        ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
+        kda.kda_destroy(ctx)
+
+        units = B * H                                   # (sequence, head) pairs per call
+        alg_bytes = units * (STATE_BYTES + 5 * D * 4 + 4 + D * 4 + 2 * 9 * D * 4) + H * 7680
+        res = {
+            "wl": wl, "ms": ms, "times": times, "launches": launches, "wall": t_wall,
+            "state_gbs": self.world * units * STATE_BYTES / (ms * 1e-3) / 1e9,
+            "alg_gbs": alg_bytes / (ms * 1e-3) / 1e9, "alg_bytes": alg_bytes,
+            "e2e_gbs": self.world * units * STATE_BYTES / (ms_e2e * 1e-3) / 1e9,
+            "ms_e2e": ms_e2e, "h2d": h2d, "d2h": d2h,
+        }
+        del tk, S, cs
+        torch.cuda.empty_cache()
+        return res
+
+    # ---------------------------------------------------------------- prefill
+    def prefill(self):
+        torch, kda, synth = self.torch, self.kda, self.synth
+        wl = synth.WORKLOADS[PREFILL_WL]
+        p = synth.make_params(wl, self.dev)
+        tk = synth.make_tokens(wl, self.dev)
+        st = synth.make_state(wl, self.dev)
+        S, cs = st["S"], st["conv_state"]
+        B, T, H = wl.B, wl.T, wl.H
+        o = torch.empty((B, T, H, D), device=self.dev)
+        q, k, v = (tk[n].view(torch.int16) for n in ("q", "k", "v"))
+        ctx = kda.kda_create(H, p["conv_w"], p["dt_bias"], p["A_log"], p["gamma"])
+        nws = kda.kda_prefill_workspace_bytes(ctx, B, T)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=self.dev)
+        W = max(3, self.args.warmup)
+        K = max(3, min(self.args.steps, self.args.prefill_steps))
+
+        def call(qq, kk, vv, zz, bb, gg, out):
+            S.zero_()
+            cs.zero_()
+            kda.kda_prefill(ctx, B, T, qq, kk, vv, zz, bb, gg, cs, S, out, ws, nws, self.stream)
+
+        for _ in range(W):
+            call(q, k, v, tk["z"], tk["beta_logit"], tk["gate_logit"], o)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        self.barrier_sync()
+        l0 = kda.kda_launch_count()
+        for i in range(K):
+            S.zero_()
+            cs.zero_()
+            ev[i][0].record(self.stream)
+            kda.kda_prefill(ctx, B, T, q, k, v, tk["z"], tk["beta_logit"], tk["gate_logit"],
+                            cs, S, o, ws, nws, self.stream)
+            ev[i][1].record(self.stream)
+        self.barrier_sync()
+        launches = kda.kda_launch_count() - l0
+        times = [a.elapsed_time(b) for a, b in ev]
+        ms = self.max_over_ranks(statistics.fmean(times))
+        assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
+
+        # End to end with pinned host buffers (inputs in, o out, per call).
+        names = ("q", "k", "v", "z", "beta_logit", "gate_logit")
+        host = {n: tk[n].to("cpu").pin_memory() for n in names}
+        o_host = torch.empty((B, T, H, D), pin_memory=True)
+        h2d = sum(x.numel() * x.element_size() for x in host.values())
+        d2h = o_host.numel() * 4
+        dbuf = tk                                       # reuse the device input buffers
+        Ke = 3
+        eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(Ke)]
+        for i in range(1 + Ke):
+            S.zero_()
+            cs.zero_()
+            if i >= 1:
+                eve[i - 1][0].record(self.stream)
+            for n in names:
+                dbuf[n].copy_(host[n], non_blocking=True)
+            kda.kda_prefill(ctx, B, T, dbuf["q"].view(torch.int16), dbuf["k"].view(torch.int16),
+                            dbuf["v"].view(torch.int16), dbuf["z"], dbuf["beta_logit"],
+                            dbuf["gate_logit"], cs, S, o, ws, nws, self.stream)
+            o_host.copy_(o, non_blocking=True)
+            if i >= 1:
+                eve[i - 1][1].record(self.stream)
+        self.barrier_sync()
+        ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
+        kda.kda_destroy(ctx)
+        th = B * T * H
+        io_bytes = th * (3 * D * 2 + 3 * D * 4 + 4) + B * H * (STATE_BYTES + 2 * 9 * D * 4) \
+            + H * 7680
+        res = {"wl": wl, "ms": ms, "launches": launches,
+               "tokens_s": self.world * B * T / (ms * 1e-3),
+               "e2e_tokens_s": self.world * B * T / (ms_e2e * 1e-3), "ms_e2e": ms_e2e,
+               "h2d": h2d, "d2h": d2h, "alg_bytes": io_bytes,
+               "alg_gbs": io_bytes / (ms * 1e-3) / 1e9,
+               "alg_tflops": th * PREFILL_FLOP_PER_TOKEN_HEAD / (ms * 1e-3) / 1e12}
+        del tk, S, cs, o, host, o_host
+        torch.cuda.empty_cache()
+        return res
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def oracle_decode(budget_s, calls_cap, threads=None):
+    """Time the fp64 oracle on whole decode calls of the headline workload."""
+    import numpy as np
+    import torch
+    from kda_delta_rule_token_gb300 import synth
+    import oracle
+    wl = synth.WORKLOADS[DECODE_WL]
+    nthreads = threads or oracle.cpu_count()
+    p = {k: v.numpy().astype(np.float64) for k, v in synth.make_params(wl, "cpu").items()}
+    st = {k: v.numpy().astype(np.float64) for k, v in synth.make_state(wl, "cpu").items()}
+    ncalls = max(1, min(wl.T, calls_cap))
+    tk = synth.make_tokens(wl, "cpu", T=ncalls)
+    S, cs = st["S"], st["conv_state"]
+    done, elapsed = 0, 0.0
+    per_call = []
+    while done < calls_cap and elapsed < budget_s:
+        t = done % ncalls
+        one = {n: tk[n][t:t + 1].transpose(0, 1).contiguous().numpy().astype(np.float64)
+               for n in ("q", "k", "v", "z", "gate_logit", "beta_logit")}
+        t0 = time.perf_counter()
+        out = oracle.run(**one, conv_w=p["conv_w"], dt_bias=p["dt_bias"], A_log=p["A_log"],
+                         gamma=p["gamma"], conv_state=cs, S=S, nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        S, cs = out.S, out.conv_state
+        per_call.append(dt)
+        elapsed += dt
+        done += 1
+    units = wl.B * wl.H
+    return {"gbs": done * units * STATE_BYTES / elapsed / 1e9, "calls": done,
+            "per_call": per_call, "threads": nthreads,
+            "sample": f"{done} whole decode calls of {wl.B}x{wl.H} heads (all units; the "
+                      f"first {ncalls} calls' inputs, cycled), fp64, {nthreads} threads"}
+
+
+def oracle_prefill(budget_tokens, heads):
+    import numpy as np
+    from kda_delta_rule_token_gb300 import synth
+    import oracle
+    wl = synth.WORKLOADS[PREFILL_WL]
+    nthreads = oracle.cpu_count()
+    small = synth.shrink(wl, B=1, H=heads, T=budget_tokens)
+    p = {k: v.numpy().astype(np.float64) for k, v in synth.make_params(small, "cpu").items()}
+    tk = {k: v.float().numpy().astype(np.float64) for k, v in
+          synth.make_tokens(small, "cpu").items()}
+    st = {k: v.numpy().astype(np.float64) for k, v in synth.make_state(small, "cpu").items()}
+    t0 = time.perf_counter()
+    oracle.run(**tk, conv_w=p["conv_w"], dt_bias=p["dt_bias"], A_log=p["A_log"],
+               gamma=p["gamma"], conv_state=st["conv_state"], S=st["S"], nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    token_heads = heads * budget_tokens
+    return {"tokens_s": token_heads / wl.H / dt, "threads": min(nthreads, heads),
+            "sample": f"1 sequence x {heads} heads x {budget_tokens} tokens of the "
+                      f"{wl.B}x{wl.H}x{wl.T} prefill shape (fp64 sequential, tokens/s "
+                      f"scaled by {heads}/{wl.H} heads)"}
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the fp64 oracle as it stands, on this host's cores."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    W, K = args.warmup, args.steps
+    calls = W + K
+    from kda_delta_rule_token_gb300 import synth
+    wl = synth.WORKLOADS[DECODE_WL]
+    r = oracle_decode(budget_s=float("inf"), calls_cap=calls)
+    timed = r["per_call"][W:]
+    ms = statistics.fmean(timed) * 1e3
+    units = wl.B * wl.H
+    value = units * STATE_BYTES / (ms * 1e-3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": DECODE_WL, "B": wl.B, "H": wl.H, "d": D,
+                   "calls": wl.T, "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": r["threads"],
+                         "kind": "oracle", "sample": r["sample"]},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--prefill-steps", type=int, default=10)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    ours = Ours(args, world, rank, local)
+    peaks = load_peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    dec = ours.decode()
+    pre = None if args.no_prefill else ours.prefill()
+    clk = clocks.stop()
+
+    if rank != 0:
+        return
+    cpu_dec = None if args.no_cpu_baseline else oracle_decode(budget_s=10.0, calls_cap=100000)
+    cpu_pre = None if (args.no_cpu_baseline or pre is None) else oracle_prefill(256, 4)
+
+    wl = dec["wl"]
+    dsha = source_sha("decode.cu")
+    frac = dec["alg_gbs"] / peaks["hbm_gbs"]
+    line = {
+        "metric": METRIC,
+        "value": round(dec["state_gbs"], 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dec["ms"], 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": DECODE_WL, "B": wl.B, "H": wl.H, "d": D,
+                   "calls_cycled": wl.T, "state_MiB": wl.B * wl.H * D * D * 4 / 2**20,
+                   "l2": "flushed between timed calls (256 MiB write + 256 MiB read)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "state_pct_of_hbm_peak": round(100 * dec["state_gbs"] / world / peaks["hbm_gbs"], 2),
+        "roofline": {"bound": "hbm", "achieved": round(dec["alg_gbs"], 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(frac, 4),
+                     "traffic": profile_traffic("decode_b64_h32_kda_decode_kernel.md", dsha),
+                     "kernel": "kda_decode_kernel", "peak_src": peaks["src"] + " hbm_gbs",
+                     "alg_bytes_per_launch": dec["alg_bytes"]},
+        "e2e": {"value": round(dec["e2e_gbs"], 2), "unit": "GB/s",
+                "ms_per_step": round(dec["ms_e2e"], 5),
+                "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"]},
+        "gpu_launches": dec["launches"],
+        "clocks": clk,
+    }
+    if cpu_dec is not None:
+        line["cpu_baseline"] = {"value": round(cpu_dec["gbs"], 4), "unit": "GB/s",
+                                "cores": cpu_dec["threads"], "kind": "oracle",
+                                "sample": cpu_dec["sample"]}
+    if pre is not None:
+        pw = pre["wl"]
+        tf32_peak = peaks["bf16_tflops"] * 0.5
+        psha = source_sha("prefill.cu")
+        line["prefill"] = {
+            "workload": PREFILL_WL, "B": pw.B, "H": pw.H, "T": pw.T, "chunk": pw.chunk,
+            "value": round(pre["tokens_s"], 1), "unit": "tokens/s",
+            "ms_per_step": round(pre["ms"], 4), "steps": max(3, min(args.steps, args.prefill_steps)),
+            "dtype": "bf16 in, f32 compute/state/out", "l2": "inputs 9.7 GB > L2",
+            "gpu_launches": pre["launches"],
+            "roofline": {"bound": "hbm", "achieved": round(pre["alg_gbs"], 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(pre["alg_gbs"] / peaks["hbm_gbs"], 4),
+                         "traffic": profile_traffic("prefill_b8_h64_kernel.md", psha),
+                         "alg_bytes_per_launch": pre["alg_bytes"]},
+            "tensor": {"achieved_tflops": round(pre["alg_tflops"], 2),
+                       "pct_of_bf16_peak": round(100 * pre["alg_tflops"] / peaks["bf16_tflops"], 2),
+                       "pct_of_tf32_peak": round(100 * pre["alg_tflops"] / tf32_peak, 2),
+                       "flop_per_token_head": PREFILL_FLOP_PER_TOKEN_HEAD},
+            "e2e": {"value": round(pre["e2e_tokens_s"], 1), "unit": "tokens/s",
+                    "ms_per_step": round(pre["ms_e2e"], 3),
+                    "h2d_bytes_per_step": pre["h2d"], "d2h_bytes_per_step": pre["d2h"]},
+        }
+        if cpu_pre is not None:
+            line["prefill"]["cpu_baseline"] = {
+                "value": round(cpu_pre["tokens_s"], 3), "unit": "tokens/s",
+                "cores": cpu_pre["threads"], "kind": "oracle", "sample": cpu_pre["sample"]}
+    print(json.dumps(line), flush=True)
+    if ours.dist is not None:
+        ours.dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention (KDA) token step.
+ *
+ * What the library computes, per sequence b, head h and token t (d_k = d_v =
+ * d = 128), following "Kimi K3 Metal Gap Analysis", section 2 "KDA Attention
+ * (kda_forward)":
+ *
+ *   row "Conv4 + SiLU":      y = SiLU(w0*x[t-3] + w1*x[t-2] + w2*x[t-1] + w3*x[t])
+ *                            per channel, for q, k and v (causal, depthwise,
+ *                            width 4, no bias; the window keeps the last three
+ *                            pre-conv inputs, oldest first)
+ *   row "L2 normalize q/k":  q^ = q / sqrt(|q|^2 + l2_eps), same for k
+ *   row "Decay compute":     gk = -exp(A_log) * softplus(z + dt_bias) per channel
+ *                            (the printed formula is garbled; this is its
+ *                            sign-safe form), beta = sigmoid(beta_logit)
+ *   row "Recurrence":        S <- (I - beta k^ k^T) Diag(e^gk) S + beta k^ v^T
+ *                            (S is d_k x d_v fp32, rows = key channels)
+ *   row "O projection":      o = gamma * RMSNorm_head(S^T q^) * sigmoid(gate_logit)
+ *                            (the W_o / W_g matmuls stay outside the library;
+ *                            the gate logits come in)
+ *
+ * The read-out uses the updated state and beta scales both the erase and the
+ * write term; "Metal (Apple GPU) backend for Kimi K3", section "Correctness"
+ * (token-0 zero-state check o / (v * beta) = q^ . k^) fixes both.
+ *
+ * Conventions shared by every call:
+ *  - Pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA tensors), dense
+ *    and row-major, 16-byte aligned; a misaligned pointer gives
+ *    KDA_ERR_ALIGNMENT and nothing is launched.
+ *  - Parameters given to kda_create are BORROWED: they must stay valid and
+ *    unchanged until kda_destroy.  State (S) and conv windows are owned by the
+ *    caller and updated in place.
+ *  - Work is enqueued on the caller's stream (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream) and is asynchronous: the library does
+ *    not synchronise and allocates no device memory after kda_create.
+ *  - Errors come back as a kda_status; there is no CPU fallback.  Argument
+ *    errors are detected on the host before any launch.
+ *  - One kda_ctx may be used from one host thread at a time.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kda_ctx kda_ctx;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, bad config */
+    KDA_ERR_ALIGNMENT = 2,    /* a pointer is not 16-byte aligned */
+    KDA_ERR_UNSUPPORTED = 3,  /* head_dim != 128, chunk_size != 64, no sm_103a device */
+    KDA_ERR_CUDA = 4,         /* a CUDA runtime call failed; see kda_last_error_detail() */
+    KDA_ERR_TIMEOUT = 5       /* a bounded wait inside a kernel gave up (kda_sync_status) */
+} kda_status;
+
+typedef struct {
+    int num_heads;   /* H >= 1 */
+    int head_dim;    /* d_k = d_v; must be 128 */
+    int chunk_size;  /* prefill chunk length; must be 64 */
+    float l2_eps;    /* added to |x|^2 in the q/k L2 normalisation (e.g. 1e-6) */
+    float rms_eps;   /* added to mean(o^2) in the head RMSNorm (e.g. 1e-6) */
+} kda_config;
+
+/*
+ * Create a context bound to one layer's parameters (the wrap-once,
+ * model-lifetime buffers of "Metal (Apple GPU) backend for Kimi K3", section
+ * "Design notes worth a reviewer's eye").  All parameter pointers are device
+ * pointers, fp32, borrowed:
+ *   conv_w    [3][H*d][4]  depthwise taps for q, k, v; tap 3 multiplies the current token
+ *   dt_bias   [H][d]
+ *   A_log     [H][d]
+ *   rms_gamma [H][d]
+ * Allocates a few bytes of device memory for the kernel error word on the
+ * current device; the context is tied to that device.
+ * Returns KDA_OK and *out, or an error with *out left NULL.
+ */
+KDA_API kda_status kda_create(const kda_config *cfg, const float *conv_w, const float *dt_bias,
+                      const float *A_log, const float *rms_gamma, kda_ctx **out);
+
+/* Release the context (NULL is ignored).  Does not touch borrowed buffers. */
+KDA_API void kda_destroy(kda_ctx *ctx);
+
+/* Static, human-readable name of a status. */
+KDA_API const char *kda_strerror(kda_status status);
+
+/* Text of the last CUDA error seen by this thread's calls into the library
+ * (empty string if none).  Static thread-local storage; do not free. */
+KDA_API const char *kda_last_error_detail(void);
+
+/*
+ * One decode token for B sequences ("Fused KDA token": conv + SiLU, L2 norm,
+ * decay, recurrence, read-out, RMSNorm and gate in ONE kernel launch).
+ *   q, k, v      [B][H][d] fp32  pre-conv inputs of this token (in)
+ *   z            [B][H][d] fp32  low-rank decay input (in)
+ *   beta_logit   [B][H]    fp32  (in)
+ *   gate_logit   [B][H][d] fp32  (in)
+ *   conv_state   [B][3][3*H*d] fp32  previous three pre-conv inputs of q, k,
+ *                            v (channel = tensor*H*d + h*d + c), oldest
+ *                            first (in/out)
+ *   S            [B][H][d][d] fp32  state, row = key channel (in/out)
+ *   o            [B][H][d] fp32  gated, normalised output (out)
+ *   o_pre        [B][H][d] fp32  S^T q^ before RMSNorm (out), or NULL
+ * B == 0 is a no-op returning KDA_OK.  Outputs must not alias inputs.
+ */
+KDA_API kda_status kda_decode_step(kda_ctx *ctx, int B,
+                           const float *q, const float *k, const float *v,
+                           const float *z, const float *beta_logit,
+                           const float *gate_logit,
+                           float *conv_state, float *S,
+                           float *o, float *o_pre, void *stream);
+
+/*
+ * Bytes of device workspace kda_prefill needs for B sequences of T tokens
+ * (0 when none is needed).
+ */
+KDA_API size_t kda_prefill_workspace_bytes(const kda_ctx *ctx, int B, int T);
+
+/*
+ * Prefill: T tokens for each of B sequences at once, chunked (chunk_size
+ * tokens per chunk, the WY/UT form of the recurrence above), with the same
+ * result as T calls of kda_decode_step up to rounding.
+ *   q, k, v      [B][T][H][d] bf16 (raw bit patterns)  pre-conv inputs (in)
+ *   z            [B][T][H][d] fp32 (in)
+ *   beta_logit   [B][T][H]    fp32 (in)
+ *   gate_logit   [B][T][H][d] fp32 (in)
+ *   conv_state   [B][3][3*H*d] fp32 (in/out), as for kda_decode_step
+ *   S            [B][H][d][d] fp32 (in/out)
+ *   o            [B][T][H][d] fp32 (out)
+ *   workspace    device buffer of at least kda_prefill_workspace_bytes(ctx,B,T)
+ *                bytes (may be NULL when that is 0); workspace_bytes is its size
+ * B == 0 or T == 0 is a no-op returning KDA_OK.
+ */
+KDA_API kda_status kda_prefill(kda_ctx *ctx, int B, int T,
+                       const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const float *z, const float *beta_logit, const float *gate_logit,
+                       float *conv_state, float *S, float *o,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Synchronise `stream` and report whether any kernel launched with this
+ * context since the last call gave up on a bounded wait (KDA_ERR_TIMEOUT) or
+ * raised a CUDA error (KDA_ERR_CUDA).  Clears the error word.
+ */
+KDA_API kda_status kda_sync_status(kda_ctx *ctx, void *stream);
+
+/* Number of kernels this library has launched in this process (all contexts). */
+KDA_API uint64_t kda_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

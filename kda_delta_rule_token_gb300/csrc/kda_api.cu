@@ -1,0 +1,185 @@
+// Host side of the C ABI declared in include/kda.h: argument validation,
+// device checks, launch and error reporting.  No allocation happens on the
+// per-call path; kda_create allocates the 16-byte kernel error word.
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "kda_internal.cuh"
+
+struct kda_ctx {
+    kda::LayerParams params;
+    int chunk;
+    kda::DeviceInfo dev;
+    int* err_word;  // device int: nonzero after a kernel gave up on a bounded wait
+};
+
+namespace kda {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_detail[256] = "";
+
+void set_detail(const char* what, cudaError_t e) {
+    std::snprintf(g_detail, sizeof(g_detail), "%s: %s (%s)", what, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+}  // namespace kda
+
+using kda::aligned16;
+
+extern "C" {
+
+const char* kda_strerror(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: null pointer, negative size or bad config";
+        case KDA_ERR_ALIGNMENT: return "KDA_ERR_ALIGNMENT: a pointer is not 16-byte aligned";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: head_dim must be 128, chunk_size 64, device sm_103";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call failed (see kda_last_error_detail)";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded wait inside a kernel gave up";
+    }
+    return "unknown kda_status";
+}
+
+const char* kda_last_error_detail(void) { return kda::g_detail; }
+
+uint64_t kda_launch_count(void) { return kda::g_launches.load(std::memory_order_relaxed); }
+
+kda_status kda_create(const kda_config* cfg, const float* conv_w, const float* dt_bias,
+                      const float* A_log, const float* rms_gamma, kda_ctx** out) {
+    if (!out) return KDA_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!cfg || !conv_w || !dt_bias || !A_log || !rms_gamma) return KDA_ERR_INVALID_ARG;
+    if (cfg->num_heads < 1 || !(cfg->l2_eps >= 0.0f) || !(cfg->rms_eps >= 0.0f) ||
+        !std::isfinite(cfg->l2_eps) || !std::isfinite(cfg->rms_eps))
+        return KDA_ERR_INVALID_ARG;
+    if (cfg->head_dim != kda::kHeadDim || cfg->chunk_size != kda::kChunk) return KDA_ERR_UNSUPPORTED;
+    if (!aligned16(conv_w) || !aligned16(dt_bias) || !aligned16(A_log) || !aligned16(rms_gamma))
+        return KDA_ERR_ALIGNMENT;
+
+    kda::DeviceInfo dev{};
+    cudaError_t e = cudaGetDevice(&dev.device);
+    if (e != cudaSuccess) { kda::set_detail("cudaGetDevice", e); return KDA_ERR_CUDA; }
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev.device)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev.device)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&dev.sm_count, cudaDevAttrMultiProcessorCount, dev.device)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&dev.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                    dev.device)) != cudaSuccess) {
+        kda::set_detail("cudaDeviceGetAttribute", e);
+        return KDA_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail),
+                      "device %d is sm_%d%d; this library is built for sm_103a only", dev.device,
+                      major, minor);
+        return KDA_ERR_UNSUPPORTED;
+    }
+    kda_ctx* c = new (std::nothrow) kda_ctx{};
+    if (!c) return KDA_ERR_INVALID_ARG;
+    c->params = kda::LayerParams{cfg->num_heads, cfg->l2_eps, cfg->rms_eps,
+                                 conv_w, dt_bias, A_log, rms_gamma};
+    c->chunk = cfg->chunk_size;
+    c->dev = dev;
+    if ((e = cudaMalloc(&c->err_word, 16)) != cudaSuccess) {
+        kda::set_detail("cudaMalloc(error word)", e);
+        delete c;
+        return KDA_ERR_CUDA;
+    }
+    if ((e = cudaMemset(c->err_word, 0, 16)) != cudaSuccess) {
+        kda::set_detail("cudaMemset(error word)", e);
+        cudaFree(c->err_word);
+        delete c;
+        return KDA_ERR_CUDA;
+    }
+    *out = c;
+    return KDA_OK;
+}
+
+void kda_destroy(kda_ctx* ctx) {
+    if (!ctx) return;
+    if (ctx->err_word) cudaFree(ctx->err_word);
+    delete ctx;
+}
+
+kda_status kda_decode_step(kda_ctx* ctx, int B, const float* q, const float* k, const float* v,
+                           const float* z, const float* beta_logit, const float* gate_logit,
+                           float* conv_state, float* S, float* o, float* o_pre, void* stream) {
+    if (!ctx || B < 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !z || !beta_logit || !gate_logit || !conv_state || !S || !o)
+        return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, z, beta_logit, gate_logit, conv_state, S, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (o_pre && !aligned16(o_pre)) return KDA_ERR_ALIGNMENT;
+    if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    kda::DecodeIO io{B, q, k, v, z, beta_logit, gate_logit, conv_state, S, o, o_pre};
+    cudaError_t e = kda::launch_decode(ctx->params, io, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { kda::set_detail("decode launch", e); return KDA_ERR_CUDA; }
+    return KDA_OK;
+}
+
+size_t kda_prefill_workspace_bytes(const kda_ctx* ctx, int B, int T) {
+    if (!ctx || B <= 0 || T <= 0) return 0;
+    return kda::prefill_workspace_bytes(ctx->params.H, B, T);
+}
+
+kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint16_t* k,
+                       const uint16_t* v, const float* z, const float* beta_logit,
+                       const float* gate_logit, float* conv_state, float* S, float* o,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    if (!ctx || B < 0 || T < 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0 || T == 0) return KDA_OK;
+    if (!q || !k || !v || !z || !beta_logit || !gate_logit || !conv_state || !S || !o)
+        return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, z, beta_logit, gate_logit, conv_state, S, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    const size_t need = kda::prefill_workspace_bytes(ctx->params.H, B, T);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(workspace)) return KDA_ERR_ALIGNMENT;
+    }
+    kda::PrefillIO io{B, T, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
+                      workspace, workspace_bytes};
+    cudaError_t e = kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word,
+                                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { kda::set_detail("prefill launch", e); return KDA_ERR_CUDA; }
+    return KDA_OK;
+}
+
+kda_status kda_sync_status(kda_ctx* ctx, void* stream) {
+    if (!ctx) return KDA_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { kda::set_detail("cudaStreamSynchronize", e); return KDA_ERR_CUDA; }
+    int word = 0;
+    if ((e = cudaMemcpy(&word, ctx->err_word, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) {
+        kda::set_detail("cudaMemcpy(error word)", e);
+        return KDA_ERR_CUDA;
+    }
+    if (word != 0) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail),
+                      "kernel error word 0x%x (bounded wait gave up)", word);
+        if ((e = cudaMemset(ctx->err_word, 0, sizeof(int))) != cudaSuccess) {
+            kda::set_detail("cudaMemset(error word)", e);
+            return KDA_ERR_CUDA;
+        }
+        return KDA_ERR_TIMEOUT;
+    }
+    return KDA_OK;
+}
+
+}  // extern "C"

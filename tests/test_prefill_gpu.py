@@ -1,0 +1,176 @@
+"""Prefill vs the fp64 oracle (GPU).
+
+Tolerance: relative L2 error 2e-3 over all of o and, separately, over the
+final state S (bf16 q/k/v inputs, fp32 everything else).  The conv window
+after the prefill holds raw inputs and must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_delta_rule_token_gb300 as kda
+from kda_delta_rule_token_gb300 import synth
+from harness import max_rel_err, np64, oracle_pairs, pair_window, rel_l2
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from kda_delta_rule_token_gb300 import build
+    build.build()
+    kda.load()
+
+
+def bits(x: torch.Tensor) -> torch.Tensor:
+    assert x.dtype == torch.bfloat16
+    return x.view(torch.int16)
+
+
+def gpu_prefill(wl, params, tokens, S, conv, T=None, t0=0, stream=None):
+    """Prefill tokens [t0, t0+T) of ``tokens`` ([B, T, H, d]) in place on S / conv."""
+    B, Tall, H, d = tokens["q"].shape
+    T = Tall - t0 if T is None else T
+    sl = lambda x: x[:, t0:t0 + T].contiguous()
+    q, k, v = (bits(sl(tokens[n])) for n in ("q", "k", "v"))
+    z, g = sl(tokens["z"]), sl(tokens["gate_logit"])
+    bl = tokens["beta_logit"][:, t0:t0 + T].contiguous()
+    o = torch.empty((B, T, H, d), device=DEV)
+    ctx = kda.kda_create(H, params["conv_w"], params["dt_bias"], params["A_log"], params["gamma"])
+    try:
+        nws = kda.kda_prefill_workspace_bytes(ctx, B, T)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=DEV) if nws else None
+        kda.kda_prefill(ctx, B, T, q, k, v, z, bl, g, conv, S, o, ws, nws, stream=stream)
+        assert kda.kda_sync_status(ctx, stream) == kda.KDA_OK
+    finally:
+        kda.kda_destroy(ctx)
+    return o
+
+
+def check(ref, o, S, conv, pairs, tol=TOL):
+    o_g = np.stack([np64(o[b, :, h]) for b, h in pairs])
+    o_r = np.stack([ref[p].o[0, :, 0] for p in pairs])
+    S_g = np.stack([np64(S[b, h]) for b, h in pairs])
+    S_r = np.stack([ref[p].S[0, 0] for p in pairs])
+    eo, es = rel_l2(o_g, o_r), rel_l2(S_g, S_r)
+    assert eo <= tol, f"o rel-L2 {eo:.3e}"
+    assert es <= tol, f"S rel-L2 {es:.3e}"
+    for b, h in pairs:
+        assert max_rel_err(pair_window(conv, b, h), ref[(b, h)].conv_state) == 0.0
+    return eo, es
+
+
+def _setup(wl, T=None):
+    return (synth.make_params(wl, DEV), synth.make_tokens(wl, DEV, T=T),
+            *synth.make_state(wl, DEV).values())
+
+
+SMALL = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], B=2, H=3, T=130,
+                     s0_std=0.05, win_std=1.0)
+
+
+@pytest.mark.parametrize("T", [1, 2, 16, 63, 64, 65, 100, 130])
+def test_small_prefill_every_output(T):
+    wl = synth.shrink(SMALL, T=T)
+    params, tokens, S, conv = _setup(wl)
+    S0, c0 = S.clone(), conv.clone()
+    o = gpu_prefill(wl, params, tokens, S, conv)
+    pairs = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    ref = oracle_pairs(params, tokens, S0, c0, pairs, call_major=False)
+    check(ref, o, S, conv, pairs)
+
+
+def test_prefill_equals_decode_calls():
+    """Prefill of T tokens = T decode calls on the same (bf16-valued) inputs."""
+    wl = synth.shrink(SMALL, T=70)
+    params, tokens, S, conv = _setup(wl)
+    Sd, cd = S.clone(), conv.clone()
+    o_p = gpu_prefill(wl, params, tokens, S, conv)
+    ctx = kda.kda_create(wl.H, params["conv_w"], params["dt_bias"], params["A_log"],
+                         params["gamma"])
+    try:
+        od = torch.empty_like(o_p)
+        f32 = {n: tokens[n].float().transpose(0, 1).contiguous()
+               for n in ("q", "k", "v", "z", "gate_logit")}
+        bl = tokens["beta_logit"].transpose(0, 1).contiguous()
+        ot = torch.empty((wl.T, wl.B, wl.H, 128), device=DEV)
+        for t in range(wl.T):
+            kda.kda_decode_step(ctx, wl.B, f32["q"][t], f32["k"][t], f32["v"][t], f32["z"][t],
+                                bl[t], f32["gate_logit"][t], cd, Sd, ot[t])
+        od.copy_(ot.transpose(0, 1))
+        torch.cuda.synchronize()
+    finally:
+        kda.kda_destroy(ctx)
+    assert rel_l2(np64(o_p), np64(od)) <= TOL
+    assert rel_l2(np64(S), np64(Sd)) <= TOL
+    assert torch.equal(conv, cd)
+
+
+def test_resume_split_equals_whole():
+    """prefill(T1) then prefill(T2) continues exactly like prefill(T1 + T2)."""
+    wl = synth.shrink(SMALL, T=150)
+    params, tokens, S, conv = _setup(wl)
+    S2, c2 = S.clone(), conv.clone()
+    o_all = gpu_prefill(wl, params, tokens, S, conv)
+    o_a = gpu_prefill(wl, params, tokens, S2, c2, T=77, t0=0)
+    o_b = gpu_prefill(wl, params, tokens, S2, c2, T=73, t0=77)
+    assert rel_l2(np64(torch.cat([o_a, o_b], 1)), np64(o_all)) <= TOL
+    assert rel_l2(np64(S2), np64(S)) <= TOL
+    assert torch.equal(c2, conv)
+
+
+def test_strong_and_extreme_decay():
+    """Channels with gk near -30 per token, beta saturated, huge values."""
+    wl = synth.shrink(SMALL, T=100)
+    params, tokens, S, conv = _setup(wl)
+    params["A_log"][0, :32].fill_(0.0)
+    tokens["z"][:, :, 0, :32] = 30.0
+    tokens["z"][:, 40:60, 1] = 80.0
+    tokens["beta_logit"][:, 10:20] = 50.0
+    tokens["beta_logit"][:, 20:30] = -50.0
+    S0, c0 = S.clone(), conv.clone()
+    o = gpu_prefill(wl, params, tokens, S, conv)
+    pairs = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    ref = oracle_pairs(params, tokens, S0, c0, pairs, call_major=False)
+    check(ref, o, S, conv, pairs)
+
+
+def test_zero_sizes_are_noops():
+    wl = synth.shrink(SMALL, T=4)
+    params, tokens, S, conv = _setup(wl)
+    S1, c1 = S.clone(), conv.clone()
+    ctx = kda.kda_create(wl.H, params["conv_w"], params["dt_bias"], params["A_log"],
+                         params["gamma"])
+    try:
+        o = torch.empty((wl.B, 4, wl.H, 128), device=DEV)
+        for B, T in ((0, 4), (wl.B, 0)):
+            kda.kda_prefill(ctx, B, T, bits(tokens["q"]), bits(tokens["k"]), bits(tokens["v"]),
+                            tokens["z"], tokens["beta_logit"], tokens["gate_logit"], conv, S, o)
+        torch.cuda.synchronize()
+        assert torch.equal(S, S1) and torch.equal(conv, c1)
+    finally:
+        kda.kda_destroy(ctx)
+
+
+def test_prefill_b1_h32_t4096_sampled():
+    """Single-sequence prefill workload at full size."""
+    wl = synth.WORKLOADS["prefill_b1_h32_t4096"]
+    params, tokens, S, conv = _setup(wl)
+    S0, c0 = S.clone(), conv.clone()
+    o = gpu_prefill(wl, params, tokens, S, conv)
+    pairs = synth.sample_heads(wl, 6)
+    ref = oracle_pairs(params, tokens, S0, c0, pairs, call_major=False)
+    check(ref, o, S, conv, pairs)
+
+
+def test_prefill_b8_h64_t8192_sampled():
+    """Batched prefill workload at full size (long-memory channels)."""
+    wl = synth.WORKLOADS["prefill_b8_h64_t8192"]
+    params, tokens, S, conv = _setup(wl)
+    S0, c0 = S.clone(), conv.clone()
+    o = gpu_prefill(wl, params, tokens, S, conv)
+    pairs = synth.sample_heads(wl, 6)
+    ref = oracle_pairs(params, tokens, S0, c0, pairs, call_major=False)
+    check(ref, o, S, conv, pairs)
