@@ -25,8 +25,8 @@
  *
  * Conventions shared by every call:
  *  - Pointers are DEVICE pointers (cudaMalloc / PyTorch CUDA tensors), dense
- *    and row-major, 16-byte aligned; a misaligned pointer gives
- *    KDA_ERR_ALIGNMENT and nothing is launched.
+ *    and row-major, 16-byte aligned (beta_logit: 4-byte aligned); a
+ *    misaligned pointer gives KDA_ERR_ALIGNMENT and nothing is launched.
  *  - Parameters given to kda_create are BORROWED: they must stay valid and
  *    unchanged until kda_destroy.  State (S) and conv windows are owned by the
  *    caller and updated in place.
@@ -58,7 +58,7 @@ typedef struct kda_ctx kda_ctx;
 typedef enum {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1,  /* NULL pointer, negative size, bad config */
-    KDA_ERR_ALIGNMENT = 2,    /* a pointer is not 16-byte aligned */
+    KDA_ERR_ALIGNMENT = 2,    /* a pointer is not 16-byte (beta_logit: 4-byte) aligned */
     KDA_ERR_UNSUPPORTED = 3,  /* head_dim != 128, chunk_size != 64, no sm_103a device */
     KDA_ERR_CUDA = 4,         /* a CUDA runtime call failed; see kda_last_error_detail() */
     KDA_ERR_TIMEOUT = 5       /* a bounded wait inside a kernel gave up (kda_sync_status) */

@@ -29,6 +29,7 @@ void set_detail(const char* what, cudaError_t e) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 }  // namespace
 
@@ -37,6 +38,7 @@ void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_rela
 }  // namespace kda
 
 using kda::aligned16;
+using kda::aligned4;
 
 extern "C" {
 
@@ -44,7 +46,7 @@ const char* kda_strerror(kda_status s) {
     switch (s) {
         case KDA_OK: return "KDA_OK";
         case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: null pointer, negative size or bad config";
-        case KDA_ERR_ALIGNMENT: return "KDA_ERR_ALIGNMENT: a pointer is not 16-byte aligned";
+        case KDA_ERR_ALIGNMENT: return "KDA_ERR_ALIGNMENT: a pointer is not 16-byte (beta_logit: 4-byte) aligned";
         case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: head_dim must be 128, chunk_size 64, device sm_103";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call failed (see kda_last_error_detail)";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded wait inside a kernel gave up";
@@ -120,9 +122,10 @@ kda_status kda_decode_step(kda_ctx* ctx, int B, const float* q, const float* k, 
     if (B == 0) return KDA_OK;
     if (!q || !k || !v || !z || !beta_logit || !gate_logit || !conv_state || !S || !o)
         return KDA_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, z, beta_logit, gate_logit, conv_state, S, o};
+    const void* ptrs[] = {q, k, v, z, gate_logit, conv_state, S, o};
     for (const void* p : ptrs)
         if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (!aligned4(beta_logit)) return KDA_ERR_ALIGNMENT;
     if (o_pre && !aligned16(o_pre)) return KDA_ERR_ALIGNMENT;
     if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     kda::DecodeIO io{B, q, k, v, z, beta_logit, gate_logit, conv_state, S, o, o_pre};
@@ -144,9 +147,10 @@ kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint
     if (B == 0 || T == 0) return KDA_OK;
     if (!q || !k || !v || !z || !beta_logit || !gate_logit || !conv_state || !S || !o)
         return KDA_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, z, beta_logit, gate_logit, conv_state, S, o};
+    const void* ptrs[] = {q, k, v, z, gate_logit, conv_state, S, o};
     for (const void* p : ptrs)
         if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (!aligned4(beta_logit)) return KDA_ERR_ALIGNMENT;
     if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     const size_t need = kda::prefill_workspace_bytes(ctx->params.H, B, T);
     if (need > 0) {
