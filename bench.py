@@ -173,7 +173,7 @@ class Ours:
 
     def flush_l2(self):
         self.flush_w.fill_(1.0)
-        self.torch.sum(self.flush_r, out=self.sink)
+        self.torch.sum(self.flush_r, 0, out=self.sink)
 
     # ---------------------------------------------------------------- decode
     def decode(self):
