@@ -4,28 +4,33 @@
 // "Conv4 + SiLU", "L2 normalize q/k", "Decay compute", "Recurrence" and "O
 // projection" (read-out, head RMSNorm and sigmoid gate), fused the way the
 // "Fused KDA token" note of "Metal (Apple GPU) backend for Kimi K3" fuses
-// them (one submission per token), but laid out for GB300's HBM3e:
+// them (one submission per token), laid out for GB300's HBM3e:
 //
-//  * one CTA of 256 threads per (sequence, head); the 64 KiB fp32 state is
-//    read once and written once with 128-bit streaming accesses (evict-first,
-//    it is touched exactly twice per token);
-//  * warp w owns state rows [16w, 16w+16), lane l owns columns [4l, 4l+4):
-//    every warp load is one contiguous 512-byte row;
-//  * all 64 KiB of loads are issued before any other work, so the conv, the
-//    norms and the decay run while the state is in flight;
-//  * u = S'^T k and the read-out p = S'^T q come out of the same pass over
-//    registers (S' = Diag(e^gk) S); the column sums need only in-thread adds
-//    plus one 8-way shared-memory reduction, since lanes own distinct columns;
-//  * o_pre = S_new^T q = p + (q^.k^) delta with delta = beta (v - u), so the
-//    read-out needs no second pass over the state.
+//  * one CTA of 256 threads per (sequence, head), three CTAs resident per SM;
+//  * the 64 KiB fp32 state moves as ONE bulk TMA copy each way
+//    (cp.async.bulk global -> shared on an mbarrier, shared -> global as a
+//    bulk group), so a whole state is in flight per CTA with one instruction
+//    and the load overlaps the conv / norm / decay prologue;
+//  * the update runs from shared memory in two passes, keeping registers low
+//    enough for three CTAs per SM: warp w owns rows [16w, 16w+16), lane l
+//    owns columns [4l, 4l+4) (one 512-byte row per warp access, no bank
+//    conflicts);
+//  * u = S'^T k and the read-out p = S'^T q come from the same first pass
+//    (S' = Diag(e^gk) S); lanes own distinct columns, so column sums need only
+//    in-thread adds plus one 8-way shared-memory reduction;
+//  * o_pre = S_new^T q = p + (q^.k^) delta with delta = beta (v - u): the
+//    read-out needs no extra pass over the state.
 #include "kda_internal.cuh"
+#include "ptx.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowsPerWarp = kHeadDim / kWarps;  // 16
+constexpr int kRowsPerWarp = kHeadDim / kWarps;           // 16
+constexpr int kStateBytes = kHeadDim * kHeadDim * 4;      // 65536
+constexpr int kDynSmem = kStateBytes;
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -40,62 +45,68 @@ __device__ __forceinline__ float softplusf_(float x) {
     return x > 0.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
-kda_decode_kernel(const LayerParams p, const DecodeIO io) {
+__global__ void __launch_bounds__(kThreads, 3)
+kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     constexpr int D = kHeadDim;
-    const int bh = blockIdx.x;
-    const int b = bh / p.H;
-    const int h = bh - b * p.H;
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-
+    extern __shared__ __align__(128) float sS[];          // the 128 x 128 state
     __shared__ float s_q[D], s_k[D], s_v[D], s_a[D];
     __shared__ __align__(16) float s_red_u[kWarps][D];
     __shared__ __align__(16) float s_red_p[kWarps][D];
     __shared__ __align__(16) float s_delta[D];
     __shared__ float s_scal[4];
     __shared__ float s_ms[4];
+    __shared__ __align__(8) uint64_t s_bar;
 
-    // 1. Put the whole state tile in flight first.
+    const int bh = blockIdx.x;
+    const int b = bh / p.H;
+    const int h = bh - b * p.H;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     float* Sg = io.S + (size_t)bh * D * D;
-    const int row0 = warp * kRowsPerWarp;
-    float4 s[kRowsPerWarp];
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r)
-        s[r] = __ldcs(reinterpret_cast<const float4*>(Sg + (size_t)(row0 + r) * D) + lane);
 
-    // 2. Conv4 + SiLU on the 3*d channels of q, k, v; shift the window.
+    // 1. One bulk copy brings the whole state in.
+    if (tid == 0) {
+        ptx::mbar_init(&s_bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        ptx::mbar_arrive_expect_tx(&s_bar, kStateBytes);
+        ptx::bulk_g2s(sS, Sg, kStateBytes, &s_bar);
+    }
+
+    // 2. While it is in flight: conv4 + SiLU on the 3*d channels of q, k, v
+    //    (shifting the window) and the per-channel decay a = exp(gk),
+    //    gk = -exp(A_log) softplus(z + dt_bias).
     const size_t HD = (size_t)p.H * D;
     const size_t HD3 = 3 * HD;
     float* win = io.conv_state + (size_t)b * 3 * HD3;
-    for (int ch = tid; ch < 3 * D; ch += kThreads) {
-        const int tensor = ch >> 7;
-        const int c = ch & (D - 1);
-        const size_t gc = (size_t)tensor * HD + (size_t)h * D + c;
-        const float* x = tensor == 0 ? io.q : (tensor == 1 ? io.k : io.v);
-        const float xt = x[(size_t)bh * D + c];
-        const float4 w = *reinterpret_cast<const float4*>(p.conv_w + gc * 4);
-        const float m3 = win[gc];
-        const float m2 = win[HD3 + gc];
-        const float m1 = win[2 * HD3 + gc];
-        const float pre = fmaf(w.w, xt, fmaf(w.z, m1, fmaf(w.y, m2, w.x * m3)));
-        const float y = pre / (1.0f + expf(-pre));
-        win[gc] = m2;
-        win[HD3 + gc] = m1;
-        win[2 * HD3 + gc] = xt;
-        (tensor == 0 ? s_q : (tensor == 1 ? s_k : s_v))[c] = y;
-    }
-    // 3. Per-channel decay a = exp(gk), gk = -exp(A_log) softplus(z + dt_bias).
-    if (tid >= kThreads - D) {
-        const int c = tid - (kThreads - D);
-        const float x = io.z[(size_t)bh * D + c] + p.dt_bias[h * D + c];
-        const float gk = -expf(p.A_log[h * D + c]) * softplusf_(x);
-        s_a[c] = expf(gk);
+    for (int ch = tid; ch < 4 * D; ch += kThreads) {
+        if (ch < 3 * D) {
+            const int tensor = ch >> 7;
+            const int c = ch & (D - 1);
+            const size_t gc = (size_t)tensor * HD + (size_t)h * D + c;
+            const float* x = tensor == 0 ? io.q : (tensor == 1 ? io.k : io.v);
+            const float xt = x[(size_t)bh * D + c];
+            const float4 w = *reinterpret_cast<const float4*>(p.conv_w + gc * 4);
+            const float m3 = win[gc];
+            const float m2 = win[HD3 + gc];
+            const float m1 = win[2 * HD3 + gc];
+            const float pre = fmaf(w.w, xt, fmaf(w.z, m1, fmaf(w.y, m2, w.x * m3)));
+            win[gc] = m2;
+            win[HD3 + gc] = m1;
+            win[2 * HD3 + gc] = xt;
+            (tensor == 0 ? s_q : (tensor == 1 ? s_k : s_v))[c] = pre / (1.0f + expf(-pre));
+        } else {
+            const int c = ch - 3 * D;
+            const float x = io.z[(size_t)bh * D + c] + p.dt_bias[h * D + c];
+            s_a[c] = expf(-expf(p.A_log[h * D + c]) * softplusf_(x));
+        }
     }
     __syncthreads();
 
-    // 4. |q|^2, |k|^2, q.k (warps 0..2) and beta (warp 3).
+    // 3. |q|^2, |k|^2, q.k (warps 0..2) and beta (warp 3).
     if (warp < 3) {
         const float* xa = warp == 1 ? s_k : s_q;
         const float* xb = warp == 0 ? s_q : s_k;
@@ -113,25 +124,28 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io) {
     const float qk = s_scal[2] * rq * rk;
     const float beta = s_scal[3];
 
-    // 5. S' = Diag(a) S in registers; partial u = S'^T k, p = S'^T q over
-    //    this warp's 16 rows (norm scales folded in afterwards).
+    const bool ok = ptx::mbar_wait(&s_bar, 0, err, ptx::kErrDecodeLoadWait);
+
+    // 4. Pass 1: partial u = S'^T k and p = S'^T q over this warp's rows
+    //    (the 1/|k| and 1/|q| scales are applied to the column totals).
+    const int row0 = warp * kRowsPerWarp;
     float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 pr = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
         const int i = row0 + r;
-        const float ai = s_a[i], ki = s_k[i], qi = s_q[i];
-        s[r].x *= ai; s[r].y *= ai; s[r].z *= ai; s[r].w *= ai;
-        u.x = fmaf(ki, s[r].x, u.x); u.y = fmaf(ki, s[r].y, u.y);
-        u.z = fmaf(ki, s[r].z, u.z); u.w = fmaf(ki, s[r].w, u.w);
-        pr.x = fmaf(qi, s[r].x, pr.x); pr.y = fmaf(qi, s[r].y, pr.y);
-        pr.z = fmaf(qi, s[r].z, pr.z); pr.w = fmaf(qi, s[r].w, pr.w);
+        const float ai = s_a[i], ki = s_k[i] * ai, qi = s_q[i] * ai;
+        const float4 x = reinterpret_cast<const float4*>(sS + i * D)[lane];
+        u.x = fmaf(ki, x.x, u.x); u.y = fmaf(ki, x.y, u.y);
+        u.z = fmaf(ki, x.z, u.z); u.w = fmaf(ki, x.w, u.w);
+        pr.x = fmaf(qi, x.x, pr.x); pr.y = fmaf(qi, x.y, pr.y);
+        pr.z = fmaf(qi, x.z, pr.z); pr.w = fmaf(qi, x.w, pr.w);
     }
     reinterpret_cast<float4*>(s_red_u[warp])[lane] = u;
     reinterpret_cast<float4*>(s_red_p[warp])[lane] = pr;
     __syncthreads();
 
-    // 6. Column totals, delta = beta (v - u), o_pre = p + (q^.k^) delta.
+    // 5. Column totals, delta = beta (v - u), o_pre = p + (q^.k^) delta.
     float opre = 0.0f;
     if (tid < D) {
         const int j = tid;
@@ -149,18 +163,26 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io) {
     }
     __syncthreads();
 
-    // 7. S_new = S' + k^ delta^T, streamed back.
+    // 6. Pass 2: S_new = Diag(a) S + k^ delta^T in shared memory, then one
+    //    bulk store back.
     const float4 dl = reinterpret_cast<const float4*>(s_delta)[lane];
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
-        const float ki = s_k[row0 + r];
-        float4 t = s[r];
-        t.x = fmaf(ki, dl.x, t.x); t.y = fmaf(ki, dl.y, t.y);
-        t.z = fmaf(ki, dl.z, t.z); t.w = fmaf(ki, dl.w, t.w);
-        __stcs(reinterpret_cast<float4*>(Sg + (size_t)(row0 + r) * D) + lane, t);
+        const int i = row0 + r;
+        const float ai = s_a[i], ki = s_k[i];
+        float4 t = reinterpret_cast<const float4*>(sS + i * D)[lane];
+        t.x = fmaf(ki, dl.x, t.x * ai); t.y = fmaf(ki, dl.y, t.y * ai);
+        t.z = fmaf(ki, dl.z, t.z * ai); t.w = fmaf(ki, dl.w, t.w * ai);
+        reinterpret_cast<float4*>(sS + i * D)[lane] = t;
+    }
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0 && ok) {
+        ptx::bulk_s2g(Sg, sS, kStateBytes);
+        ptx::bulk_commit();
     }
 
-    // 8. Head RMSNorm, gamma and the sigmoid gate.
+    // 7. Head RMSNorm, gamma and the sigmoid gate.
     if (tid < D) {
         const int j = tid;
         const float ms = (s_ms[0] + s_ms[1] + s_ms[2] + s_ms[3]) * (1.0f / D);
@@ -168,14 +190,28 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io) {
         const float g = sigmoidf_(io.gate_logit[(size_t)bh * D + j]);
         io.o[(size_t)bh * D + j] = p.gamma[h * D + j] * opre * inv * g;
     }
+    // The CTA's shared memory must outlive the bulk store's reads of it.
+    if (tid == 0 && ok) ptx::bulk_wait_read_all();
 }
+
+bool g_attr_done[64] = {};
 
 }  // namespace
 
-cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, cudaStream_t stream) {
+cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const DeviceInfo& dev,
+                          int* err_word, cudaStream_t stream) {
     const long long grid = (long long)io.B * p.H;
     if (grid <= 0) return cudaSuccess;
-    kda_decode_kernel<<<(unsigned)grid, kThreads, 0, stream>>>(p, io);
+    if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device]) {
+        cudaError_t e = cudaFuncSetAttribute(kda_decode_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kda_decode_kernel,
+                                 cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device] = true;
+    }
+    kda_decode_kernel<<<(unsigned)grid, kThreads, kDynSmem, stream>>>(p, io, err_word);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -129,7 +129,8 @@ kda_status kda_decode_step(kda_ctx* ctx, int B, const float* q, const float* k, 
     if (o_pre && !aligned16(o_pre)) return KDA_ERR_ALIGNMENT;
     if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     kda::DecodeIO io{B, q, k, v, z, beta_logit, gate_logit, conv_state, S, o, o_pre};
-    cudaError_t e = kda::launch_decode(ctx->params, io, static_cast<cudaStream_t>(stream));
+    cudaError_t e = kda::launch_decode(ctx->params, io, ctx->dev, ctx->err_word,
+                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) { kda::set_detail("decode launch", e); return KDA_ERR_CUDA; }
     return KDA_OK;
 }

@@ -63,7 +63,8 @@ struct DeviceInfo {
 
 // Launchers (kernels live in decode.cu / prefill.cu).  They return the
 // cudaError_t of the launch.
-cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, cudaStream_t stream);
+cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const DeviceInfo& dev,
+                          int* err_word, cudaStream_t stream);
 size_t prefill_workspace_bytes(int H, int B, int T);
 cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const DeviceInfo& dev,
                            int* err_word, cudaStream_t stream);
