@@ -259,7 +259,7 @@ class Ours:
     # ---------------------------------------------------------------- prefill
     def prefill(self):
         torch, kda, synth = self.torch, self.kda, self.synth
-        wl = synth.WORKLOADS[PREFILL_WL]
+        wl = synth.WORKLOADS[self.args.prefill_workload]
         p = synth.make_params(wl, self.dev)
         tk = synth.make_tokens(wl, self.dev)
         st = synth.make_state(wl, self.dev)
@@ -436,6 +436,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode headline (profiling only)")
+    ap.add_argument("--prefill-workload", default=PREFILL_WL,
+                    help="prefill workload of the secondary line (default: the 8x64x8192 one)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -448,11 +451,15 @@ def main():
     peaks = load_peaks()
     clocks = ClockSampler(local)
     clocks.start()
-    dec = ours.decode()
+    dec = None if args.no_decode else ours.decode()
     pre = None if args.no_prefill else ours.prefill()
     clk = clocks.stop()
 
     if rank != 0:
+        return
+    if dec is None:   # profiling run: report the prefill alone
+        print(json.dumps({"profiling_only": True, "prefill_ms": pre and round(pre["ms"], 4),
+                          "prefill_workload": args.prefill_workload}), flush=True)
         return
     cpu_dec = None if args.no_cpu_baseline else oracle_decode(budget_s=10.0, calls_cap=100000)
     cpu_pre = None if (args.no_cpu_baseline or pre is None) else oracle_prefill(256, 4)
@@ -491,7 +498,7 @@ def main():
         tf32_peak = peaks["bf16_tflops"] * 0.5
         psha = source_sha("prefill.cu")
         line["prefill"] = {
-            "workload": PREFILL_WL, "B": pw.B, "H": pw.H, "T": pw.T, "chunk": pw.chunk,
+            "workload": pw.name, "B": pw.B, "H": pw.H, "T": pw.T, "chunk": pw.chunk,
             "value": round(pre["tokens_s"], 1), "unit": "tokens/s",
             "ms_per_step": round(pre["ms"], 4), "steps": max(3, min(args.steps, args.prefill_steps)),
             "dtype": "bf16 in, f32 compute/state/out", "l2": "inputs 9.7 GB > L2",

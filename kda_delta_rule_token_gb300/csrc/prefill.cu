@@ -34,6 +34,9 @@
 //   MMA3  M  += R^T U               A from TMEM       (N = 128, K = 64)
 //         on the TMEM master M = Diag(e^rho) S0; then S_new = e^{G_last-rho} M.
 // The unit-lower inverse is a forward substitution on CUDA cores.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kda_internal.cuh"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -47,15 +50,19 @@ constexpr int kThreads = 256;
 constexpr float kMaxSpan = 160.0f;
 
 // Dynamic shared memory map (bytes).
-constexpr uint32_t OFF_ST = 0;                // (Diag(e^rho) S0)^T operand, N=128 x K=128 tf32
+constexpr uint32_t OFF_ST = 0;                // (Diag(e^rho) S0)^T operand, N=128 x K=128 tf32;
+                                              // between MMA1 and the state pass it stages the
+                                              // next chunk's q, k (bf16) and z (fp32) tiles
 constexpr uint32_t OFF_L = OFF_ST + 65536;    // L operand 128 x 128; staging of y_k / y_q
 constexpr uint32_t OFF_R = OFF_L + 65536;     // R operand 64 x 128; staging of G; then
                                               // Diag(beta) A' (fp32 64x64); then the
                                               // Diag(beta) X / U operand N=128 x K=64
 constexpr uint32_t OFF_V = OFF_R + 32768;     // v conv output, fp32 64 x 128 (SW128 layout)
-constexpr uint32_t OFF_MT = OFF_V + 32768;    // Minv^T operand N=64 x K=64
+constexpr uint32_t OFF_MT = OFF_V + 32768;    // Minv^T operand N=64 x K=64; stages the v tile
 constexpr uint32_t OFF_SMALL = OFF_MT + 16384;
 constexpr uint32_t kSmemBytes = OFF_SMALL + 4096;
+constexpr uint32_t STG_Q = OFF_ST, STG_K = OFF_ST + 16384, STG_Z = OFF_ST + 32768, STG_V = OFF_MT;
+constexpr uint32_t kStageBytes = 3 * C * D * 2 + C * D * 4;   // 80 KiB per chunk
 
 // TMEM column map (512 columns allocated).
 constexpr int TM_S = 0;     // state master, lane = key channel, column = value channel
@@ -65,10 +72,11 @@ constexpr int TM_DT = 320;  // [Minv; P Minv] (A operand of MMA2)
 constexpr int TM_RT = 384;  // R^T (A operand of MMA3), lane = channel, column = token
 
 __device__ __forceinline__ float bf16f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
-__device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
+// Fast-intrinsic forms (relative error ~1e-6, far inside the tf32 operand rounding).
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float siluf_(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 __device__ __forceinline__ float softplusf_(float x) {
-    return x > 0.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
+    return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x)));
 }
 
 template <typename T>
@@ -112,8 +120,12 @@ __device__ __forceinline__ void publish() {
     sync_tc();
 }
 
+struct Maps {
+    CUtensorMap q, k, v, z;   // 4-D (d, H, T, B) boxes of (128, 1, 64, 1)
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
-kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err) {
+kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __grid_constant__ Maps maps) {
     extern __shared__ __align__(1024) uint8_t sm[];
     float* s_beta = reinterpret_cast<float*>(sm + OFF_SMALL);   // [64]
     float* s_rq = s_beta + 64;                                    // [64]
@@ -123,7 +135,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err) {
     float* s_esc = s_rhoR + 128;                                  // [128] e^{G_last - rho_R}
     float* s_part = s_esc + 128;                                  // [2][64] RMS partial sums
     uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_part + 128);
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 1);
+    uint64_t* s_tbar = s_bar + 1;                                 // input tiles landed
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 2);
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -133,14 +146,32 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err) {
     const size_t HD = (size_t)H * D, HD3 = 3 * HD;
 
     if (warp == 0) tc::alloc(s_tmem, 512);
+    const int nchunks = (T + C - 1) / C;
+    // Thread 0 stages chunk ci's q, k, v, z tiles with four TMA box loads and
+    // asks L2 for its gate rows; rows past T come back as zeros.
+    auto stage = [&](int ci) {
+        if (tid == 0) {
+            ptx::mbar_arrive_expect_tx(s_tbar, kStageBytes);
+            ptx::tma_load_4d(sm + STG_Q, &maps.q, 0, h, ci * C, b, s_tbar);
+            ptx::tma_load_4d(sm + STG_K, &maps.k, 0, h, ci * C, b, s_tbar);
+            ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, ci * C, b, s_tbar);
+            ptx::tma_load_4d(sm + STG_Z, &maps.z, 0, h, ci * C, b, s_tbar);
+        }
+        const int r = tid >> 2;
+        if (ci * C + r < T)
+            ptx::prefetch_l2(io.gate_logit + (((size_t)(b * T + ci * C + r)) * H + h) * D + (tid & 3) * 32);
+    };
     if (tid == 0) {
         ptx::mbar_init(s_bar, 1);
+        ptx::mbar_init(s_tbar, 1);
         ptx::fence_mbar_init();
         *s_dead = 0;
     }
     sync_tc();
     const uint32_t tm = *s_tmem;
     Waiter wt{s_bar, s_dead, err, 0u};
+    Waiter wtma{s_tbar, s_dead, err, 0u};
+    stage(0);
 
     // Per-thread roles: c = channel for the thread-per-channel passes; the
     // TMEM quadrant of this warp is (warp & 3), its column half is warp >> 2.
@@ -186,55 +217,63 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err) {
         }
     }
 
-    const int nchunks = (T + C - 1) / C;
     for (int ci = 0; ci < nchunks; ++ci) {
         const int t0 = ci * C;
         const int n = min(C, T - t0);
         const size_t row0 = ((size_t)(b * T + t0) * H + h) * D;   // token t0, channel 0
         const size_t tstride = HD;                                   // elements between tokens
 
-        // ---- A1: conv + SiLU per channel over the chunk; decay and its cumulative sum.
+        // ---- A1: conv + SiLU per channel over the chunk (from the staged
+        //      tiles); decay and its cumulative sum.
+        wtma.wait();
         bool big = false;
         if (half == 0) {
+            const uint16_t* tq = reinterpret_cast<const uint16_t*>(sm + STG_Q);
+            const uint16_t* tkk = reinterpret_cast<const uint16_t*>(sm + STG_K);
             float xq[C], xk[C];
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                xq[r] = r < n ? bf16f(io.q[row0 + r * tstride + c]) : 0.f;
-                xk[r] = r < n ? bf16f(io.k[row0 + r * tstride + c]) : 0.f;
+                xq[r] = bf16f(tq[r * D + c]);
+                xk[r] = bf16f(tkk[r * D + c]);
             }
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                float yq = 0.f, yk = 0.f;
-                if (r < n) {
-                    const float pq = fmaf(w_a.w, xq[r], fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
-                    const float pk = fmaf(w_b.w, xk[r], fmaf(w_b.z, wb[2], fmaf(w_b.y, wb[1], w_b.x * wb[0])));
-                    yq = siluf_(pq);
-                    yk = siluf_(pk);
-                    wa[0] = wa[1]; wa[1] = wa[2]; wa[2] = xq[r];
-                    wb[0] = wb[1]; wb[1] = wb[2]; wb[2] = xk[r];
-                }
-                at<float>(sm, OFF_L + tc::sw128(r, c, 128)) = yk;
-                at<float>(sm, OFF_L + tc::sw128(C + r, c, 128)) = yq;
+                const bool ok = r < n;
+                const float pq = fmaf(w_a.w, xq[r], fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
+                const float pk = fmaf(w_b.w, xk[r], fmaf(w_b.z, wb[2], fmaf(w_b.y, wb[1], w_b.x * wb[0])));
+                wa[0] = ok ? wa[1] : wa[0]; wa[1] = ok ? wa[2] : wa[1]; wa[2] = ok ? xq[r] : wa[2];
+                wb[0] = ok ? wb[1] : wb[0]; wb[1] = ok ? wb[2] : wb[1]; wb[2] = ok ? xk[r] : wb[2];
+                xq[r] = ok ? siluf_(pq) : 0.f;       // the registers now hold y
+                xk[r] = ok ? siluf_(pk) : 0.f;
+            }
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                at<float>(sm, OFF_L + tc::sw128(r, c, 128)) = xk[r];
+                at<float>(sm, OFF_L + tc::sw128(C + r, c, 128)) = xq[r];
             }
         } else {
+            const uint16_t* tv = reinterpret_cast<const uint16_t*>(sm + STG_V);
+            const float* tz = reinterpret_cast<const float*>(sm + STG_Z);
             float xv[C], xz[C];
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                xv[r] = r < n ? bf16f(io.v[row0 + r * tstride + c]) : 0.f;
-                xz[r] = r < n ? io.z[row0 + r * tstride + c] : 0.f;
+                xv[r] = bf16f(tv[r * D + c]);
+                xz[r] = tz[r * D + c];
             }
             float G = 0.f;
 #pragma unroll
             for (int r = 0; r < C; ++r) {
-                float yv = 0.f;
-                if (r < n) {
-                    const float pv = fmaf(w_a.w, xv[r], fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
-                    yv = siluf_(pv);
-                    wa[0] = wa[1]; wa[1] = wa[2]; wa[2] = xv[r];
-                    G += -expA * softplusf_(xz[r] + dtb);
-                }
-                at<float>(sm, OFF_V + tc::sw128(r, c, C)) = yv;
-                at<float>(sm, OFF_R + tc::sw128(r, c, C)) = G;
+                const bool ok = r < n;
+                const float pv = fmaf(w_a.w, xv[r], fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
+                wa[0] = ok ? wa[1] : wa[0]; wa[1] = ok ? wa[2] : wa[1]; wa[2] = ok ? xv[r] : wa[2];
+                xv[r] = ok ? siluf_(pv) : 0.f;
+                G -= ok ? expA * softplusf_(xz[r] + dtb) : 0.f;
+                xz[r] = G;
+            }
+#pragma unroll
+            for (int r = 0; r < C; ++r) {
+                at<float>(sm, OFF_V + tc::sw128(r, c, C)) = xv[r];
+                at<float>(sm, OFF_R + tc::sw128(r, c, C)) = xz[r];
             }
             big = -G > kMaxSpan;
             s_esc[c] = G;   // G_last for now
@@ -299,23 +338,29 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err) {
         // ---- A3: L, R (shared memory, in place over the staging) and R^T (TMEM).
         {
             const float rl = s_rhoL[c], rr = s_rhoR[c];
-            uint32_t rt[32];
+            float g[32], yk[32], yq[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int r = half * 32 + i;
-                const uint32_t oK = OFF_L + tc::sw128(r, c, 128);
-                const uint32_t oQ = OFF_L + tc::sw128(C + r, c, 128);
-                const uint32_t oR = OFF_R + tc::sw128(r, c, C);
-                const float G = at<float>(sm, oR);
-                const float kh = at<float>(sm, oK) * s_rk[r];
-                const float qh = at<float>(sm, oQ) * s_rq[r];
-                const float eL = expf(G - rl);
-                const float eR = expf(rr - G);
-                at<uint32_t>(sm, oK) = tc::f2tf32(kh * eL);
-                at<uint32_t>(sm, oQ) = tc::f2tf32(qh * eL);
-                const uint32_t rv = tc::f2tf32(kh * eR);
-                at<uint32_t>(sm, oR) = rv;
-                rt[i] = rv;
+                g[i] = at<float>(sm, OFF_R + tc::sw128(r, c, C));
+                yk[i] = at<float>(sm, OFF_L + tc::sw128(r, c, 128)) * s_rk[r];
+                yq[i] = at<float>(sm, OFF_L + tc::sw128(C + r, c, 128)) * s_rq[r];
+            }
+            uint32_t rt[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float eL = __expf(g[i] - rl);
+                const float eR = __expf(rr - g[i]);
+                rt[i] = tc::f2tf32(yk[i] * eR);
+                yk[i] = __uint_as_float(tc::f2tf32(yk[i] * eL));
+                yq[i] = __uint_as_float(tc::f2tf32(yq[i] * eL));
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int r = half * 32 + i;
+                at<float>(sm, OFF_L + tc::sw128(r, c, 128)) = yk[i];
+                at<float>(sm, OFF_L + tc::sw128(C + r, c, 128)) = yq[i];
+                at<uint32_t>(sm, OFF_R + tc::sw128(r, c, C)) = rt[i];
             }
             tc::st32(tc::taddr(tm, warp, TM_RT + half * 32), rt);
         }
@@ -338,60 +383,98 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err) {
             wt.wait();
         }
 
-        // ---- C1: Diag(beta) A' to shared memory, D0 -> [I; P] in TMEM.
-        if (warp < 4) {
+        // ---- C1: Diag(beta) A' to shared memory, D0 -> [I; P] in TMEM
+        //      (warp quadrant = 32 rows, warp >> 2 = 32-column half).
+        {
             float* sM = reinterpret_cast<float*>(sm + OFF_R);   // [64][64], R is no longer needed
-            if (warp < 2) {
-                const int r = qrow;   // 0..63
+            const int i0 = half * 32;
+            uint32_t v[32];
+            tc::ld32(tc::taddr(tm, warp, TM_D0 + i0), v);
+            tc::wait_ld();
+            if (qrow < C) {
+                const int r = qrow;
                 const float br = s_beta[r];
 #pragma unroll
-                for (int i0 = 0; i0 < C; i0 += 32) {
-                    uint32_t v[32];
-                    tc::ld32(tc::taddr(tm, warp, TM_D0 + i0), v);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int col = i0 + i;
-                        sM[r * C + col] = col < r ? br * __uint_as_float(v[i]) : 0.f;
-                        v[i] = col == r ? tc::f2tf32(1.0f) : 0u;
-                    }
-                    tc::st32(tc::taddr(tm, warp, TM_D0 + i0), v);
+                for (int i = 0; i < 32; i += 4) {
+                    float4 m;
+                    m.x = (i0 + i) < r ? br * __uint_as_float(v[i]) : 0.f;
+                    m.y = (i0 + i + 1) < r ? br * __uint_as_float(v[i + 1]) : 0.f;
+                    m.z = (i0 + i + 2) < r ? br * __uint_as_float(v[i + 2]) : 0.f;
+                    m.w = (i0 + i + 3) < r ? br * __uint_as_float(v[i + 3]) : 0.f;
+                    *reinterpret_cast<float4*>(sM + r * C + i0 + i) = m;
                 }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = (i0 + i) == r ? tc::f2tf32(1.0f) : 0u;
             } else {
                 const int r = qrow - C;   // P row
 #pragma unroll
-                for (int i0 = 0; i0 < C; i0 += 32) {
-                    uint32_t v[32];
-                    tc::ld32(tc::taddr(tm, warp, TM_D0 + i0), v);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = (i0 + i) <= r ? tc::f2tf32(__uint_as_float(v[i])) : 0u;
-                    tc::st32(tc::taddr(tm, warp, TM_D0 + i0), v);
-                }
+                for (int i = 0; i < 32; ++i)
+                    v[i] = (i0 + i) <= r ? tc::f2tf32(__uint_as_float(v[i])) : 0u;
             }
+            tc::st32(tc::taddr(tm, warp, TM_D0 + i0), v);
         }
         tc::wait_st();
         sync_tc();
 
-        // ---- C2: Minv = (I + Diag(beta) A')^{-1}, one column per thread
-        //      (forward substitution), written as the N=64 x K=64 operand Minv^T.
-        if (tid < C) {
-            const float* sM = reinterpret_cast<const float*>(sm + OFF_R);
-            const int j = tid;
-            float x[C];
+        // ---- C2: Minv = (I + N)^{-1}, N = Diag(beta) A' (strictly lower), by
+        //      16 x 16 blocks: diagonal blocks by forward substitution, then
+        //      Minv[I][J] = -Minv[I][I] sum_{J<=K<I} N[I][K] Minv[K][J] level by
+        //      level (I - J = 1, 2, 3).  fp32 in shared memory, then the
+        //      N=64 x K=64 tf32 operand Minv^T.
+        {
+            const float* sN = reinterpret_cast<const float*>(sm + OFF_R);    // [64][64]
+            float* sMi = reinterpret_cast<float*>(sm + OFF_R + 16384);       // [64][64]
+            float* sTmp = reinterpret_cast<float*>(sm + OFF_MT);             // [3][16][16]
+            if (tid < C) {
+                const int I = tid >> 4, jj = tid & 15, j = I * 16 + jj;
+                float x[16];
 #pragma unroll
-            for (int r = 0; r < C; ++r) {
-                float s = r == j ? 1.0f : 0.0f;
+                for (int rr = 0; rr < 16; ++rr) {
+                    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-                for (int i = 0; i < r; ++i) s = fmaf(-sM[r * C + i], x[i], s);
-                x[r] = s;
+                    for (int i = 0; i < rr; ++i) {
+                        if (i & 1) a1 = fmaf(sN[(I * 16 + rr) * C + I * 16 + i], x[i], a1);
+                        else a0 = fmaf(sN[(I * 16 + rr) * C + I * 16 + i], x[i], a0);
+                    }
+                    x[rr] = (rr == jj ? 1.0f : 0.0f) - (a0 + a1);
+                }
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) sMi[(I * 16 + rr) * C + j] = x[rr];
             }
+            __syncthreads();
 #pragma unroll
-            for (int i = 0; i < C; i += 4) {
+            for (int lev = 1; lev < 4; ++lev) {
+                const int nblk = 4 - lev;
+                // tmp[blk] = sum_{K=J}^{I-1} N[I][K] Minv[K][J], I = J + lev
+                for (int e = tid; e < nblk * 256; e += kThreads) {
+                    const int J = e >> 8, row = (e >> 4) & 15, col = e & 15, I = J + lev;
+                    float acc = 0.f;
+                    for (int K = J; K < I; ++K) {
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            acc = fmaf(sN[(I * 16 + row) * C + K * 16 + m], sMi[(K * 16 + m) * C + J * 16 + col], acc);
+                    }
+                    sTmp[e] = acc;
+                }
+                __syncthreads();
+                for (int e = tid; e < nblk * 256; e += kThreads) {
+                    const int J = e >> 8, row = (e >> 4) & 15, col = e & 15, I = J + lev;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        acc = fmaf(sMi[(I * 16 + row) * C + I * 16 + m], sTmp[(J << 8) + m * 16 + col], acc);
+                    sMi[(I * 16 + row) * C + J * 16 + col] = -acc;
+                }
+                __syncthreads();
+            }
+            // Minv^T operand: row j holds Minv[.][j]; zero above the diagonal.
+            for (int e = tid; e < C * C / 4; e += kThreads) {
+                const int j = e >> 4, i = (e & 15) * 4;
                 uint4 u;
-                u.x = tc::f2tf32(x[i]); u.y = tc::f2tf32(x[i + 1]);
-                u.z = tc::f2tf32(x[i + 2]); u.w = tc::f2tf32(x[i + 3]);
+                u.x = (i + 0) >= j ? tc::f2tf32(sMi[(i + 0) * C + j]) : 0u;
+                u.y = (i + 1) >= j ? tc::f2tf32(sMi[(i + 1) * C + j]) : 0u;
+                u.z = (i + 2) >= j ? tc::f2tf32(sMi[(i + 2) * C + j]) : 0u;
+                u.w = (i + 3) >= j ? tc::f2tf32(sMi[(i + 3) * C + j]) : 0u;
                 at<uint4>(sm, OFF_MT + tc::sw128(j, i, C)) = u;
             }
         }
@@ -452,6 +535,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err) {
             tc::commit(s_bar);
         }
         wt.wait();
+        if (ci + 1 < nchunks) stage(ci + 1);   // S^T and Minv^T regions are free now
 
         // ---- E: X = V - K_g S0 -> Diag(beta) X operand (N=128 x K=64); clear D1 top.
         if ((warp & 3) < 2) {
@@ -462,18 +546,18 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err) {
                 uint32_t v[32];
                 tc::ld32(tc::taddr(tm, warp, TM_D1 + half * 64 + j0), v);
                 tc::wait_ld();
+                float4 vv[8];
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 4) {
-                    const int j = half * 64 + j0 + jj;
-                    const float4 vv = at<float4>(sm, OFF_V + tc::sw128(r, j, C));
-                    at<uint32_t>(sm, OFF_R + tc::sw128(j, r, 128)) =
-                        tc::f2tf32(br * (vv.x - __uint_as_float(v[jj])));
-                    at<uint32_t>(sm, OFF_R + tc::sw128(j + 1, r, 128)) =
-                        tc::f2tf32(br * (vv.y - __uint_as_float(v[jj + 1])));
-                    at<uint32_t>(sm, OFF_R + tc::sw128(j + 2, r, 128)) =
-                        tc::f2tf32(br * (vv.z - __uint_as_float(v[jj + 2])));
-                    at<uint32_t>(sm, OFF_R + tc::sw128(j + 3, r, 128)) =
-                        tc::f2tf32(br * (vv.w - __uint_as_float(v[jj + 3])));
+                for (int q4 = 0; q4 < 8; ++q4)
+                    vv[q4] = at<float4>(sm, OFF_V + tc::sw128(r, half * 64 + j0 + q4 * 4, C));
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const int j = half * 64 + j0 + q4 * 4;
+                    const float xs[4] = {vv[q4].x, vv[q4].y, vv[q4].z, vv[q4].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        at<uint32_t>(sm, OFF_R + tc::sw128(j + e, r, 128)) =
+                            tc::f2tf32(br * (xs[e] - __uint_as_float(v[q4 * 4 + e])));
                 }
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) v[jj] = 0u;
@@ -606,6 +690,34 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err) {
 
 bool g_attr_done[64] = {};
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// [B][T][H][d] tensor seen as 4-D (d, H, T, B); boxes of one head x 64 tokens.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int H, int T,
+              int B) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * esize, (cuuint64_t)H * D * esize,
+                                   (cuuint64_t)T * H * D * esize};
+    const cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)C, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 size_t prefill_workspace_bytes(int, int, int) { return 0; }
@@ -620,7 +732,13 @@ cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const Devi
         if (e != cudaSuccess) return e;
         if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device] = true;
     }
-    kda_prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p, io, err_word);
+    Maps maps;
+    if (!make_map(&maps.q, io.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, io.B) ||
+        !make_map(&maps.k, io.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, io.B) ||
+        !make_map(&maps.v, io.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, io.B) ||
+        !make_map(&maps.z, io.z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, io.B))
+        return cudaErrorInvalidValue;
+    kda_prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p, io, err_word, maps);
     count_launches(1);
     return cudaGetLastError();
 }

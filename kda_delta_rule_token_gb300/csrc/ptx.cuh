@@ -85,6 +85,22 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 // Wait until every committed bulk store has fully completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Tiled TMA load of a 4-D box (coordinates innermost first) into shared
+// memory, completing its bytes on mbarrier m.  tmap is the address of a
+// CUtensorMap kernel parameter (__grid_constant__).
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2, int c3,
+                                            uint64_t* m) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        ::"r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(m))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
