@@ -89,15 +89,11 @@ struct Waiter {
     int* dead;  // shared: a bounded wait already gave up in this CTA
     int* err;
     uint32_t phase;
-    // Wait for the next MMA commit; bounded, and immediate once the CTA is dead.
+    // Wait for the next phase of the barrier; gives up after kWaitLimitNs of
+    // wall time (then marks the CTA dead so later waits return at once).
     __device__ __forceinline__ void wait() {
-        if (!*dead) {
-            bool ok = false;
-            for (int i = 0; i < (1 << 20); ++i) {
-                if (ptx::mbar_try_wait(bar, phase)) { ok = true; break; }
-                if ((i & 1023) == 1023 && *(volatile int*)dead) break;
-            }
-            if (!ok) {
+        if (!*(volatile int*)dead) {
+            if (!ptx::mbar_wait_timed(bar, phase, dead)) {
                 *(volatile int*)dead = 1;
                 atomicOr(err, ptx::kErrPrefillWait);
             }
@@ -217,6 +213,13 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
     }
 
+    // Swizzled addressing for the thread-per-channel passes: channel c is the
+    // K index of the L / R / V layouts (fixed per thread), rows vary.
+    const uint32_t cL = (uint32_t)((c >> 5) * 128 * 128 + (c & 3) * 4);   // 128-row operands
+    const uint32_t cR = (uint32_t)((c >> 5) * 64 * 128 + (c & 3) * 4);    // 64-row operands
+    const int cch = (c >> 2) & 7;
+    auto rowoff = [&](int r) -> uint32_t { return (uint32_t)(r * 128 + ((cch ^ (r & 7)) << 4)); };
+
     for (int ci = 0; ci < nchunks; ++ci) {
         const int t0 = ci * C;
         const int n = min(C, T - t0);
@@ -228,52 +231,36 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         wtma.wait();
         bool big = false;
         if (half == 0) {
-            const uint16_t* tq = reinterpret_cast<const uint16_t*>(sm + STG_Q);
-            const uint16_t* tkk = reinterpret_cast<const uint16_t*>(sm + STG_K);
-            float xq[C], xk[C];
-#pragma unroll
+            const uint16_t* tq = reinterpret_cast<const uint16_t*>(sm + STG_Q) + c;
+            const uint16_t* tkk = reinterpret_cast<const uint16_t*>(sm + STG_K) + c;
+#pragma unroll 4
             for (int r = 0; r < C; ++r) {
-                xq[r] = bf16f(tq[r * D + c]);
-                xk[r] = bf16f(tkk[r * D + c]);
-            }
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
+                const float xq = bf16f(tq[r * D]);
+                const float xk = bf16f(tkk[r * D]);
                 const bool ok = r < n;
-                const float pq = fmaf(w_a.w, xq[r], fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
-                const float pk = fmaf(w_b.w, xk[r], fmaf(w_b.z, wb[2], fmaf(w_b.y, wb[1], w_b.x * wb[0])));
-                wa[0] = ok ? wa[1] : wa[0]; wa[1] = ok ? wa[2] : wa[1]; wa[2] = ok ? xq[r] : wa[2];
-                wb[0] = ok ? wb[1] : wb[0]; wb[1] = ok ? wb[2] : wb[1]; wb[2] = ok ? xk[r] : wb[2];
-                xq[r] = ok ? siluf_(pq) : 0.f;       // the registers now hold y
-                xk[r] = ok ? siluf_(pk) : 0.f;
-            }
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                at<float>(sm, OFF_L + tc::sw128(r, c, 128)) = xk[r];
-                at<float>(sm, OFF_L + tc::sw128(C + r, c, 128)) = xq[r];
+                const float pq = fmaf(w_a.w, xq, fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
+                const float pk = fmaf(w_b.w, xk, fmaf(w_b.z, wb[2], fmaf(w_b.y, wb[1], w_b.x * wb[0])));
+                wa[0] = ok ? wa[1] : wa[0]; wa[1] = ok ? wa[2] : wa[1]; wa[2] = ok ? xq : wa[2];
+                wb[0] = ok ? wb[1] : wb[0]; wb[1] = ok ? wb[2] : wb[1]; wb[2] = ok ? xk : wb[2];
+                const uint32_t ro = rowoff(r);
+                at<float>(sm, OFF_L + cL + ro) = ok ? siluf_(pk) : 0.f;
+                at<float>(sm, OFF_L + cL + C * 128 + ro) = ok ? siluf_(pq) : 0.f;
             }
         } else {
-            const uint16_t* tv = reinterpret_cast<const uint16_t*>(sm + STG_V);
-            const float* tz = reinterpret_cast<const float*>(sm + STG_Z);
-            float xv[C], xz[C];
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                xv[r] = bf16f(tv[r * D + c]);
-                xz[r] = tz[r * D + c];
-            }
+            const uint16_t* tv = reinterpret_cast<const uint16_t*>(sm + STG_V) + c;
+            const float* tz = reinterpret_cast<const float*>(sm + STG_Z) + c;
             float G = 0.f;
-#pragma unroll
+#pragma unroll 4
             for (int r = 0; r < C; ++r) {
+                const float xv = bf16f(tv[r * D]);
+                const float xz = tz[r * D];
                 const bool ok = r < n;
-                const float pv = fmaf(w_a.w, xv[r], fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
-                wa[0] = ok ? wa[1] : wa[0]; wa[1] = ok ? wa[2] : wa[1]; wa[2] = ok ? xv[r] : wa[2];
-                xv[r] = ok ? siluf_(pv) : 0.f;
-                G -= ok ? expA * softplusf_(xz[r] + dtb) : 0.f;
-                xz[r] = G;
-            }
-#pragma unroll
-            for (int r = 0; r < C; ++r) {
-                at<float>(sm, OFF_V + tc::sw128(r, c, C)) = xv[r];
-                at<float>(sm, OFF_R + tc::sw128(r, c, C)) = xz[r];
+                const float pv = fmaf(w_a.w, xv, fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
+                wa[0] = ok ? wa[1] : wa[0]; wa[1] = ok ? wa[2] : wa[1]; wa[2] = ok ? xv : wa[2];
+                G -= ok ? expA * softplusf_(xz + dtb) : 0.f;
+                const uint32_t ro = rowoff(r);
+                at<float>(sm, OFF_V + cR + ro) = ok ? siluf_(pv) : 0.f;
+                at<float>(sm, OFF_R + cR + ro) = G;
             }
             big = -G > kMaxSpan;
             s_esc[c] = G;   // G_last for now
@@ -285,7 +272,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const float rr = fb ? G : 0.5f * G;
             s_rhoL[c] = rl;
             s_rhoR[c] = rr;
-            s_esc[c] = expf(G - rr);
+            s_esc[c] = __expf(G - rr);
         }
 
         // ---- A2: per-token norms of the conv outputs and beta.
@@ -293,12 +280,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const int r = tid & (C - 1);
             const int rowL = tid < C ? r : C + r;   // y_k rows first, then y_q
             float ss = 0.f;
-#pragma unroll
+#pragma unroll 8
             for (int k4 = 0; k4 < D; k4 += 4) {
                 const float4 v = at<float4>(sm, OFF_L + tc::sw128(rowL, k4, 128));
                 ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
             }
-            (tid < C ? s_rk : s_rq)[r] = 1.0f / sqrtf(ss + p.l2_eps);
+            (tid < C ? s_rk : s_rq)[r] = rsqrtf(ss + p.l2_eps);
         } else if (tid < 3 * C) {
             const int r = tid - 2 * C;
             s_beta[r] = r < n ? sigmoidf_(io.beta_logit[((size_t)(b * T + t0 + r)) * H + h]) : 0.f;
@@ -311,58 +298,54 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const int r = R & (C - 1);
             const bool isP = R >= C;
             const float rn = isP ? s_rq[r] : s_rk[r];
-            float acc[32];
+#pragma unroll 1
+            for (int g8 = 0; g8 < 4; ++g8) {
+                uint32_t out[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-            for (int ch = 0; ch < D; ++ch) {
-                const float a = at<float>(sm, OFF_L + tc::sw128(R, ch, 128));
-                const float gr = at<float>(sm, OFF_R + tc::sw128(r, ch, C));
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = half * 32 + i;
+                for (int i = 0; i < 8; ++i) {
+                    const int col = half * 32 + g8 * 8 + i;
+                    float acc = 0.f;
                     if (isP ? col <= r : col < r) {
-                        const float kk = at<float>(sm, OFF_L + tc::sw128(col, ch, 128));
-                        const float gi = at<float>(sm, OFF_R + tc::sw128(col, ch, C));
-                        acc[i] = fmaf(a * kk, expf(gr - gi), acc[i]);
+#pragma unroll 4
+                        for (int ch = 0; ch < D; ++ch) {
+                            const float a = at<float>(sm, OFF_L + tc::sw128(R, ch, 128));
+                            const float gr = at<float>(sm, OFF_R + tc::sw128(r, ch, C));
+                            const float kk = at<float>(sm, OFF_L + tc::sw128(col, ch, 128));
+                            const float gi = at<float>(sm, OFF_R + tc::sw128(col, ch, C));
+                            acc = fmaf(a * kk, expf(gr - gi), acc);
+                        }
                     }
+                    out[i] = __float_as_uint(acc * rn * s_rk[col]);
                 }
+                tc::st8(tc::taddr(tm, warp, TM_D0 + half * 32 + g8 * 8), out);
             }
-            uint32_t out[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) out[i] = __float_as_uint(acc[i] * rn * s_rk[half * 32 + i]);
-            tc::st32(tc::taddr(tm, warp, TM_D0 + half * 32), out);
             tc::wait_st();
             __syncthreads();
         }
 
-        // ---- A3: L, R (shared memory, in place over the staging) and R^T (TMEM).
+        // ---- A3: L, R (shared memory, in place over the staging) and R^T
+        //      (TMEM), 8 tokens at a time.
         {
             const float rl = s_rhoL[c], rr = s_rhoR[c];
-            float g[32], yk[32], yq[32];
+#pragma unroll 1
+            for (int g8 = 0; g8 < 4; ++g8) {
+                uint32_t rt[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int r = half * 32 + i;
-                g[i] = at<float>(sm, OFF_R + tc::sw128(r, c, C));
-                yk[i] = at<float>(sm, OFF_L + tc::sw128(r, c, 128)) * s_rk[r];
-                yq[i] = at<float>(sm, OFF_L + tc::sw128(C + r, c, 128)) * s_rq[r];
+                for (int i = 0; i < 8; ++i) {
+                    const int r = half * 32 + g8 * 8 + i;
+                    const uint32_t ro = rowoff(r);
+                    const float g = at<float>(sm, OFF_R + cR + ro);
+                    const float yk = at<float>(sm, OFF_L + cL + ro) * s_rk[r];
+                    const float yq = at<float>(sm, OFF_L + cL + C * 128 + ro) * s_rq[r];
+                    const float eL = __expf(g - rl);
+                    const float eR = __expf(rr - g);
+                    rt[i] = tc::f2tf32(yk * eR);
+                    at<uint32_t>(sm, OFF_L + cL + ro) = tc::f2tf32(yk * eL);
+                    at<uint32_t>(sm, OFF_L + cL + C * 128 + ro) = tc::f2tf32(yq * eL);
+                    at<uint32_t>(sm, OFF_R + cR + ro) = rt[i];
+                }
+                tc::st8(tc::taddr(tm, warp, TM_RT + half * 32 + g8 * 8), rt);
             }
-            uint32_t rt[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float eL = __expf(g[i] - rl);
-                const float eR = __expf(rr - g[i]);
-                rt[i] = tc::f2tf32(yk[i] * eR);
-                yk[i] = __uint_as_float(tc::f2tf32(yk[i] * eL));
-                yq[i] = __uint_as_float(tc::f2tf32(yq[i] * eL));
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int r = half * 32 + i;
-                at<float>(sm, OFF_L + tc::sw128(r, c, 128)) = yk[i];
-                at<float>(sm, OFF_L + tc::sw128(C + r, c, 128)) = yq[i];
-                at<uint32_t>(sm, OFF_R + tc::sw128(r, c, C)) = rt[i];
-            }
-            tc::st32(tc::taddr(tm, warp, TM_RT + half * 32), rt);
         }
         publish();
 
@@ -370,7 +353,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         if (!fb) {
             if (tid == 0) {
                 constexpr uint32_t id = tc::idesc_tf32(128, 64);
-#pragma unroll
+#pragma unroll 1
                 for (int ks = 0; ks < D / 8; ++ks) {
                     const int kb = ks >> 2, kin = ks & 3;
                     tc::mma_ss(tm + TM_D0,
@@ -387,31 +370,31 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         //      (warp quadrant = 32 rows, warp >> 2 = 32-column half).
         {
             float* sM = reinterpret_cast<float*>(sm + OFF_R);   // [64][64], R is no longer needed
-            const int i0 = half * 32;
-            uint32_t v[32];
-            tc::ld32(tc::taddr(tm, warp, TM_D0 + i0), v);
-            tc::wait_ld();
-            if (qrow < C) {
-                const int r = qrow;
-                const float br = s_beta[r];
+            const bool isA = qrow < C;
+            const int r = isA ? qrow : qrow - C;
+            const float br = s_beta[r];
+#pragma unroll 1
+            for (int g8 = 0; g8 < 4; ++g8) {
+                const int i0 = half * 32 + g8 * 8;
+                uint32_t v[8];
+                tc::ld8(tc::taddr(tm, warp, TM_D0 + i0), v);
+                tc::wait_ld();
+                if (isA) {
+                    float m[8];
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    float4 m;
-                    m.x = (i0 + i) < r ? br * __uint_as_float(v[i]) : 0.f;
-                    m.y = (i0 + i + 1) < r ? br * __uint_as_float(v[i + 1]) : 0.f;
-                    m.z = (i0 + i + 2) < r ? br * __uint_as_float(v[i + 2]) : 0.f;
-                    m.w = (i0 + i + 3) < r ? br * __uint_as_float(v[i + 3]) : 0.f;
-                    *reinterpret_cast<float4*>(sM + r * C + i0 + i) = m;
+                    for (int i = 0; i < 8; ++i) {
+                        m[i] = (i0 + i) < r ? br * __uint_as_float(v[i]) : 0.f;
+                        v[i] = (i0 + i) == r ? tc::f2tf32(1.0f) : 0u;
+                    }
+                    *reinterpret_cast<float4*>(sM + r * C + i0) = make_float4(m[0], m[1], m[2], m[3]);
+                    *reinterpret_cast<float4*>(sM + r * C + i0 + 4) = make_float4(m[4], m[5], m[6], m[7]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        v[i] = (i0 + i) <= r ? tc::f2tf32(__uint_as_float(v[i])) : 0u;
                 }
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = (i0 + i) == r ? tc::f2tf32(1.0f) : 0u;
-            } else {
-                const int r = qrow - C;   // P row
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    v[i] = (i0 + i) <= r ? tc::f2tf32(__uint_as_float(v[i])) : 0u;
+                tc::st8(tc::taddr(tm, warp, TM_D0 + i0), v);
             }
-            tc::st32(tc::taddr(tm, warp, TM_D0 + i0), v);
         }
         tc::wait_st();
         sync_tc();
@@ -427,14 +410,15 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             float* sTmp = reinterpret_cast<float*>(sm + OFF_MT);             // [3][16][16]
             if (tid < C) {
                 const int I = tid >> 4, jj = tid & 15, j = I * 16 + jj;
+                const float* nb = sN + I * 16 * C + I * 16;
                 float x[16];
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
                     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                     for (int i = 0; i < rr; ++i) {
-                        if (i & 1) a1 = fmaf(sN[(I * 16 + rr) * C + I * 16 + i], x[i], a1);
-                        else a0 = fmaf(sN[(I * 16 + rr) * C + I * 16 + i], x[i], a0);
+                        if (i & 1) a1 = fmaf(nb[rr * C + i], x[i], a1);
+                        else a0 = fmaf(nb[rr * C + i], x[i], a0);
                     }
                     x[rr] = (rr == jj ? 1.0f : 0.0f) - (a0 + a1);
                 }
@@ -442,32 +426,35 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 for (int rr = 0; rr < 16; ++rr) sMi[(I * 16 + rr) * C + j] = x[rr];
             }
             __syncthreads();
-#pragma unroll
+#pragma unroll 1
             for (int lev = 1; lev < 4; ++lev) {
                 const int nblk = 4 - lev;
                 // tmp[blk] = sum_{K=J}^{I-1} N[I][K] Minv[K][J], I = J + lev
                 for (int e = tid; e < nblk * 256; e += kThreads) {
                     const int J = e >> 8, row = (e >> 4) & 15, col = e & 15, I = J + lev;
+                    const float* nrow = sN + (I * 16 + row) * C;
                     float acc = 0.f;
+#pragma unroll 1
                     for (int K = J; K < I; ++K) {
 #pragma unroll
                         for (int m = 0; m < 16; ++m)
-                            acc = fmaf(sN[(I * 16 + row) * C + K * 16 + m], sMi[(K * 16 + m) * C + J * 16 + col], acc);
+                            acc = fmaf(nrow[K * 16 + m], sMi[(K * 16 + m) * C + J * 16 + col], acc);
                     }
                     sTmp[e] = acc;
                 }
                 __syncthreads();
                 for (int e = tid; e < nblk * 256; e += kThreads) {
                     const int J = e >> 8, row = (e >> 4) & 15, col = e & 15, I = J + lev;
+                    const float* mrow = sMi + (I * 16 + row) * C + I * 16;
                     float acc = 0.f;
 #pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        acc = fmaf(sMi[(I * 16 + row) * C + I * 16 + m], sTmp[(J << 8) + m * 16 + col], acc);
+                    for (int m = 0; m < 16; ++m) acc = fmaf(mrow[m], sTmp[(J << 8) + m * 16 + col], acc);
                     sMi[(I * 16 + row) * C + J * 16 + col] = -acc;
                 }
                 __syncthreads();
             }
             // Minv^T operand: row j holds Minv[.][j]; zero above the diagonal.
+#pragma unroll 1
             for (int e = tid; e < C * C / 4; e += kThreads) {
                 const int j = e >> 4, i = (e & 15) * 4;
                 uint4 u;
@@ -483,7 +470,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- MMA_T: [Minv; P Minv] = [I; P] Minv.
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
-#pragma unroll
+#pragma unroll 1
             for (int ks = 0; ks < C / 8; ++ks) {
                 const int kb = ks >> 2, kin = ks & 3;
                 tc::mma_ts(tm + TM_DT, tm + TM_D0 + ks * 8,
@@ -496,28 +483,36 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- C4 + D: round DT to tf32 in place; state pass: S^T operand
         //      scaled by e^{rho_L}, master scaled by e^{rho_R}.
         {
-            uint32_t v[32];
-            tc::ld32(tc::taddr(tm, warp, TM_DT + half * 32), v);
-            tc::wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = tc::f2tf32(__uint_as_float(v[i]));
-            tc::st32(tc::taddr(tm, warp, TM_DT + half * 32), v);
-
-            const float eL = expf(s_rhoL[qrow]);
-            const float eR = expf(s_rhoR[qrow]);
-#pragma unroll
-            for (int j0 = 0; j0 < 64; j0 += 32) {
-                uint32_t s[32];
-                tc::ld32(tc::taddr(tm, warp, TM_S + half * 64 + j0), s);
+#pragma unroll 1
+            for (int g8 = 0; g8 < 4; ++g8) {
+                uint32_t v[8];
+                const uint32_t ta = tc::taddr(tm, warp, TM_DT + half * 32 + g8 * 8);
+                tc::ld8(ta, v);
                 tc::wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = half * 64 + j0 + jj;
-                    const float sv = __uint_as_float(s[jj]);
-                    at<uint32_t>(sm, OFF_ST + tc::sw128(j, qrow, 128)) = tc::f2tf32(sv * eL);
-                    s[jj] = __float_as_uint(sv * eR);
+                for (int i = 0; i < 8; ++i) v[i] = tc::f2tf32(__uint_as_float(v[i]));
+                tc::st8(ta, v);
+            }
+            const float eL = __expf(s_rhoL[qrow]);
+            const float eR = __expf(s_rhoR[qrow]);
+            // S^T operand element (row j, K = qrow): K block and chunk are fixed per thread.
+            const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
+            const int kch = (qrow >> 2) & 7;
+#pragma unroll 1
+            for (int g8 = 0; g8 < 8; ++g8) {
+                uint32_t v[8];
+                const int j0 = half * 64 + g8 * 8;
+                const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
+                tc::ld8(ta, v);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int j = j0 + i;
+                    const float sv = __uint_as_float(v[i]);
+                    at<uint32_t>(sm, OFF_ST + kq + j * 128 + ((kch ^ (j & 7)) << 4)) = tc::f2tf32(sv * eL);
+                    v[i] = __float_as_uint(sv * eR);
                 }
-                tc::st32(tc::taddr(tm, warp, TM_S + half * 64 + j0), s);
+                tc::st8(ta, v);
             }
         }
         publish();
@@ -525,7 +520,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- MMA1: D1 = L (Diag(e^rho_L) S0) = [K_g S0; Q_g S0].
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
-#pragma unroll
+#pragma unroll 1
             for (int ks = 0; ks < D / 8; ++ks) {
                 const int kb = ks >> 2, kin = ks & 3;
                 tc::mma_ss(tm + TM_D1,
@@ -538,30 +533,33 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         if (ci + 1 < nchunks) stage(ci + 1);   // S^T and Minv^T regions are free now
 
         // ---- E: X = V - K_g S0 -> Diag(beta) X operand (N=128 x K=64); clear D1 top.
+        //      The operand element (row j, K = token r) has a fixed K block and
+        //      chunk per thread.
         if ((warp & 3) < 2) {
             const int r = qrow;   // token
             const float br = s_beta[r];
-#pragma unroll
-            for (int j0 = 0; j0 < 64; j0 += 32) {
-                uint32_t v[32];
-                tc::ld32(tc::taddr(tm, warp, TM_D1 + half * 64 + j0), v);
+            const uint32_t kr = (uint32_t)((r >> 5) * 128 * 128 + (r & 3) * 4);
+            const int rch = (r >> 2) & 7;
+            const uint32_t vrow = OFF_V + r * 128;   // + K block of j, swizzled chunk
+#pragma unroll 1
+            for (int g8 = 0; g8 < 8; ++g8) {
+                const int j0 = half * 64 + g8 * 8;
+                uint32_t v[8];
+                const uint32_t ta = tc::taddr(tm, warp, TM_D1 + j0);
+                tc::ld8(ta, v);
+                const uint32_t vb = vrow + (j0 >> 5) * 64 * 128;
+                const float4 v0 = at<float4>(sm, vb + (((((j0 & 31) >> 2)) ^ (r & 7)) << 4));
+                const float4 v1 = at<float4>(sm, vb + (((((j0 & 31) >> 2) + 1) ^ (r & 7)) << 4));
                 tc::wait_ld();
-                float4 vv[8];
+                const float xs[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4)
-                    vv[q4] = at<float4>(sm, OFF_V + tc::sw128(r, half * 64 + j0 + q4 * 4, C));
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const int j = half * 64 + j0 + q4 * 4;
-                    const float xs[4] = {vv[q4].x, vv[q4].y, vv[q4].z, vv[q4].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        at<uint32_t>(sm, OFF_R + tc::sw128(j + e, r, 128)) =
-                            tc::f2tf32(br * (xs[e] - __uint_as_float(v[q4 * 4 + e])));
+                for (int i = 0; i < 8; ++i) {
+                    const int j = j0 + i;
+                    at<uint32_t>(sm, OFF_R + kr + j * 128 + ((rch ^ (j & 7)) << 4)) =
+                        tc::f2tf32(br * (xs[i] - __uint_as_float(v[i])));
+                    v[i] = 0u;
                 }
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) v[jj] = 0u;
-                tc::st32(tc::taddr(tm, warp, TM_D1 + half * 64 + j0), v);
+                tc::st8(ta, v);
             }
         }
         publish();
@@ -569,7 +567,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- MMA2: D1 += [Minv; P Minv] Diag(beta) X = [U; P U].
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
-#pragma unroll
+#pragma unroll 1
             for (int ks = 0; ks < C / 8; ++ks) {
                 const int kb = ks >> 2, kin = ks & 3;
                 tc::mma_ts(tm + TM_D1, tm + TM_DT + ks * 8,
@@ -579,33 +577,35 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         wt.wait();
 
-        // ---- F: U -> operand of MMA3; O_pre -> RMSNorm, gamma, gate -> o.
-        float op[64];
+        // ---- F: U -> operand of MMA3 (rows 0..63); sum of squares of O_pre
+        //      (rows 64..127).
         if ((warp & 3) < 2) {
             const int r = qrow;
-#pragma unroll
-            for (int j0 = 0; j0 < 64; j0 += 32) {
-                uint32_t v[32];
-                tc::ld32(tc::taddr(tm, warp, TM_D1 + half * 64 + j0), v);
+            const uint32_t kr = (uint32_t)((r >> 5) * 128 * 128 + (r & 3) * 4);
+            const int rch = (r >> 2) & 7;
+#pragma unroll 1
+            for (int g8 = 0; g8 < 8; ++g8) {
+                const int j0 = half * 64 + g8 * 8;
+                uint32_t v[8];
+                tc::ld8(tc::taddr(tm, warp, TM_D1 + j0), v);
                 tc::wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    at<uint32_t>(sm, OFF_R + tc::sw128(half * 64 + j0 + jj, r, 128)) =
-                        tc::f2tf32(__uint_as_float(v[jj]));
+                for (int i = 0; i < 8; ++i) {
+                    const int j = j0 + i;
+                    at<uint32_t>(sm, OFF_R + kr + j * 128 + ((rch ^ (j & 7)) << 4)) =
+                        tc::f2tf32(__uint_as_float(v[i]));
+                }
             }
         } else {
             const int r = qrow - C;
             float ss = 0.f;
-#pragma unroll
-            for (int j0 = 0; j0 < 64; j0 += 32) {
-                uint32_t v[32];
-                tc::ld32(tc::taddr(tm, warp, TM_D1 + half * 64 + j0), v);
+#pragma unroll 1
+            for (int g8 = 0; g8 < 8; ++g8) {
+                uint32_t v[8];
+                tc::ld8(tc::taddr(tm, warp, TM_D1 + half * 64 + g8 * 8), v);
                 tc::wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    op[j0 + jj] = __uint_as_float(v[jj]);
-                    ss = fmaf(op[j0 + jj], op[j0 + jj], ss);
-                }
+                for (int i = 0; i < 8; ++i) ss = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss);
             }
             s_part[half * C + r] = ss;
         }
@@ -614,7 +614,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- MMA3 (issued now, overlaps the output epilogue): M += R^T U.
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
-#pragma unroll
+#pragma unroll 1
             for (int ks = 0; ks < C / 8; ++ks) {
                 const int kb = ks >> 2, kin = ks & 3;
                 tc::mma_ts(tm + TM_S, tm + TM_RT + ks * 8,
@@ -622,24 +622,36 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             tc::commit(s_bar);
         }
+        // O_pre -> RMSNorm, gamma, sigmoid gate -> o (D1 rows 64..127 are not
+        // touched by MMA3).
         if ((warp & 3) >= 2) {
+            // tcgen05.ld is warp-collective: every lane loads, only rows r < n store.
             const int r = qrow - C;
-            if (r < n) {
-                const float ms = (s_part[r] + s_part[C + r]) * (1.0f / D);
-                const float inv = 1.0f / sqrtf(ms + p.rms_eps);
-                const size_t orow = row0 + (size_t)r * tstride + half * 64;
-                const float* gl = io.gate_logit + orow;
-                const float* gm = p.gamma + h * D + half * 64;
-#pragma unroll
-                for (int j = 0; j < 64; j += 4) {
-                    const float4 g = *reinterpret_cast<const float4*>(gl + j);
-                    const float4 gg = *reinterpret_cast<const float4*>(gm + j);
-                    float4 o;
-                    o.x = gg.x * op[j] * inv * sigmoidf_(g.x);
-                    o.y = gg.y * op[j + 1] * inv * sigmoidf_(g.y);
-                    o.z = gg.z * op[j + 2] * inv * sigmoidf_(g.z);
-                    o.w = gg.w * op[j + 3] * inv * sigmoidf_(g.w);
-                    *reinterpret_cast<float4*>(io.o + orow + j) = o;
+            const bool live = r < n;
+            const float inv = rsqrtf((s_part[r] + s_part[C + r]) * (1.0f / D) + p.rms_eps);
+            const size_t orow = row0 + (size_t)(live ? r : 0) * tstride;
+#pragma unroll 1
+            for (int g8 = 0; g8 < 8; ++g8) {
+                const int j0 = half * 64 + g8 * 8;
+                uint32_t v[8];
+                tc::ld8(tc::taddr(tm, warp, TM_D1 + j0), v);
+                tc::wait_ld();
+                if (live) {
+                    const float4 ga = *reinterpret_cast<const float4*>(io.gate_logit + orow + j0);
+                    const float4 gb = *reinterpret_cast<const float4*>(io.gate_logit + orow + j0 + 4);
+                    const float4 ma = *reinterpret_cast<const float4*>(p.gamma + h * D + j0);
+                    const float4 mb = *reinterpret_cast<const float4*>(p.gamma + h * D + j0 + 4);
+                    float4 oa, ob;
+                    oa.x = ma.x * __uint_as_float(v[0]) * inv * sigmoidf_(ga.x);
+                    oa.y = ma.y * __uint_as_float(v[1]) * inv * sigmoidf_(ga.y);
+                    oa.z = ma.z * __uint_as_float(v[2]) * inv * sigmoidf_(ga.z);
+                    oa.w = ma.w * __uint_as_float(v[3]) * inv * sigmoidf_(ga.w);
+                    ob.x = mb.x * __uint_as_float(v[4]) * inv * sigmoidf_(gb.x);
+                    ob.y = mb.y * __uint_as_float(v[5]) * inv * sigmoidf_(gb.y);
+                    ob.z = mb.z * __uint_as_float(v[6]) * inv * sigmoidf_(gb.z);
+                    ob.w = mb.w * __uint_as_float(v[7]) * inv * sigmoidf_(gb.w);
+                    *reinterpret_cast<float4*>(io.o + orow + j0) = oa;
+                    *reinterpret_cast<float4*>(io.o + orow + j0 + 4) = ob;
                 }
             }
         }
@@ -648,14 +660,15 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- G: S_new = e^{G_last - rho_R} M.
         {
             const float e = s_esc[qrow];
-#pragma unroll
-            for (int j0 = 0; j0 < 64; j0 += 32) {
-                uint32_t s[32];
-                tc::ld32(tc::taddr(tm, warp, TM_S + half * 64 + j0), s);
+#pragma unroll 1
+            for (int g8 = 0; g8 < 8; ++g8) {
+                uint32_t v[8];
+                const uint32_t ta = tc::taddr(tm, warp, TM_S + half * 64 + g8 * 8);
+                tc::ld8(ta, v);
                 tc::wait_ld();
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) s[jj] = __float_as_uint(__uint_as_float(s[jj]) * e);
-                tc::st32(tc::taddr(tm, warp, TM_S + half * 64 + j0), s);
+                for (int i = 0; i < 8; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * e);
+                tc::st8(ta, v);
             }
         }
         tc::wait_st();

@@ -14,7 +14,14 @@ namespace ptx {
 constexpr int kErrDecodeLoadWait = 1 << 0;
 constexpr int kErrPrefillWait = 1 << 1;
 
-constexpr int kMaxPolls = 1 << 22;
+// Longest a kernel waits on one barrier phase before it reports an error.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -50,10 +57,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; bounded.
-__device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity, int* err, int bit) {
-    for (int i = 0; i < kMaxPolls; ++i)
+// Wait for the phase with the given parity to complete.  Bounded in wall
+// time (kWaitLimitNs) and, when `abort` is given, cut short as soon as
+// another thread of the CTA has set *abort.  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t* m, uint32_t parity, const int* abort = nullptr) {
+    if (mbar_try_wait(m, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (unsigned i = 1;; ++i) {
         if (mbar_try_wait(m, parity)) return true;
+        if ((i & 63) == 0) {
+            if (abort && *(volatile const int*)abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+// As mbar_wait_timed, recording `bit` in the error word when it gives up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity, int* err, int bit) {
+    if (mbar_wait_timed(m, parity)) return true;
     atomicOr(err, bit);
     return false;
 }

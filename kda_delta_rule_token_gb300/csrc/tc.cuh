@@ -101,6 +101,19 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
         : "memory");
 }
 
+// 8 consecutive 32-bit TMEM columns of this thread's lane (warp-wide).
+__device__ __forceinline__ void ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : KDA_R8(0)
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"r"(taddr), KDA_W8(0)
+                 : "memory");
+}
+
 #undef KDA_R8
 #undef KDA_W8
 
