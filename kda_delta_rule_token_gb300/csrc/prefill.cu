@@ -32,7 +32,8 @@
 //         with D1's top half cleared after X = V - K_g S0 was read, so D1 =
 //         [U; O_pre]
 //   MMA3  M  += R^T U               A from TMEM       (N = 128, K = 64)
-//         on the TMEM master M = Diag(e^rho) S0; then S_new = e^{G_last-rho} M.
+//         on the TMEM master M = Diag(e^rho) S0; S_new = e^{G_last-rho} M, that
+//         row scale being applied by the next chunk's pass over the master.
 // The unit-lower inverse is a forward substitution on CUDA cores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -145,17 +146,23 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     const int nchunks = (T + C - 1) / C;
     // Thread 0 stages chunk ci's q, k, v, z tiles with four TMA box loads and
     // asks L2 for its gate rows; rows past T come back as zeros.
-    auto stage = [&](int ci) {
+    // Staging of chunk ci's input tiles with TMA box loads (rows past T come
+    // back as zeros).  q, k, z land in the S^T operand region and may be
+    // issued once MMA1 has read it; v lands in the Minv^T region and may be
+    // issued once MMA_T has read it.  One barrier phase covers all four.
+    auto stage_qkz = [&](int ci) {
         if (tid == 0) {
             ptx::mbar_arrive_expect_tx(s_tbar, kStageBytes);
             ptx::tma_load_4d(sm + STG_Q, &maps.q, 0, h, ci * C, b, s_tbar);
             ptx::tma_load_4d(sm + STG_K, &maps.k, 0, h, ci * C, b, s_tbar);
-            ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, ci * C, b, s_tbar);
             ptx::tma_load_4d(sm + STG_Z, &maps.z, 0, h, ci * C, b, s_tbar);
         }
-        const int r = tid >> 2;
+        const int r = tid >> 2;   // and ask L2 for the chunk's gate rows
         if (ci * C + r < T)
             ptx::prefetch_l2(io.gate_logit + (((size_t)(b * T + ci * C + r)) * H + h) * D + (tid & 3) * 32);
+    };
+    auto stage_v = [&](int ci) {
+        if (tid == 0) ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, ci * C, b, s_tbar);
     };
     if (tid == 0) {
         ptx::mbar_init(s_bar, 1);
@@ -167,7 +174,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     const uint32_t tm = *s_tmem;
     Waiter wt{s_bar, s_dead, err, 0u};
     Waiter wtma{s_tbar, s_dead, err, 0u};
-    stage(0);
+    stage_qkz(0);
+    stage_v(0);
 
     // Per-thread roles: c = channel for the thread-per-channel passes; the
     // TMEM quadrant of this warp is (warp & 3), its column half is warp >> 2.
@@ -192,26 +200,32 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         tc::wait_st();
     }
 
-    // Conv taps, windows and decay constants of this thread's channel(s).
+    // Conv / decay roles: tensor a1t = tid / 64 (q, k, v, decay), channel pair
+    // c2, c2 + 1 -- two independent chains per thread.
     float* win = io.conv_state + (size_t)b * 3 * HD3;
-    float4 w_a, w_b;            // half 0: taps of q and k; half 1: taps of v
-    float wa[3], wb[3];         // windows (oldest first)
-    float expA = 0.f, dtb = 0.f;
-    {
-        const size_t ga = (size_t)(half == 0 ? 0 : 2) * HD + (size_t)h * D + c;
-        const size_t gb = HD + (size_t)h * D + c;   // k (half 0 only)
-        w_a = *reinterpret_cast<const float4*>(p.conv_w + ga * 4);
-        w_b = *reinterpret_cast<const float4*>(p.conv_w + gb * 4);
+    const int a1t = tid >> 6;
+    const int c2 = (tid & 63) * 2;
+    float4 w0 = make_float4(0.f, 0.f, 0.f, 0.f), w1 = w0;   // taps
+    float win0[3] = {0.f, 0.f, 0.f}, win1[3] = {0.f, 0.f, 0.f};   // windows, oldest first
+    float expA0 = 0.f, expA1 = 0.f, dtb0 = 0.f, dtb1 = 0.f;
+    const size_t g0 = (size_t)(a1t < 3 ? a1t : 0) * HD + (size_t)h * D + c2;
+    if (a1t < 3) {
+        w0 = *reinterpret_cast<const float4*>(p.conv_w + g0 * 4);
+        w1 = *reinterpret_cast<const float4*>(p.conv_w + (g0 + 1) * 4);
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
-            wa[j] = win[j * HD3 + ga];
-            wb[j] = win[j * HD3 + gb];
+            win0[j] = win[j * HD3 + g0];
+            win1[j] = win[j * HD3 + g0 + 1];
         }
-        if (half == 1) {
-            expA = expf(p.A_log[h * D + c]);
-            dtb = p.dt_bias[h * D + c];
-        }
+    } else {
+        expA0 = expf(p.A_log[h * D + c2]);
+        expA1 = expf(p.A_log[h * D + c2 + 1]);
+        dtb0 = p.dt_bias[h * D + c2];
+        dtb1 = p.dt_bias[h * D + c2 + 1];
     }
+    const uint32_t k2L = (uint32_t)((c2 >> 5) * 128 * 128 + (c2 & 3) * 4);   // 128-row operands
+    const uint32_t k2R = (uint32_t)((c2 >> 5) * 64 * 128 + (c2 & 3) * 4);    // 64-row operands
+    const int ch2 = (c2 >> 2) & 7;
 
     // Swizzled addressing for the thread-per-channel passes: channel c is the
     // K index of the L / R / V layouts (fixed per thread), rows vary.
@@ -220,6 +234,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     const int cch = (c >> 2) & 7;
     auto rowoff = [&](int r) -> uint32_t { return (uint32_t)(r * 128 + ((cch ^ (r & 7)) << 4)); };
 
+    float esc_prev = 1.0f;   // pending e^{G_last - rho_R} of the previous chunk, per state row
     for (int ci = 0; ci < nchunks; ++ci) {
         const int t0 = ci * C;
         const int n = min(C, T - t0);
@@ -230,49 +245,99 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         //      tiles); decay and its cumulative sum.
         wtma.wait();
         bool big = false;
-        if (half == 0) {
-            const uint16_t* tq = reinterpret_cast<const uint16_t*>(sm + STG_Q) + c;
-            const uint16_t* tkk = reinterpret_cast<const uint16_t*>(sm + STG_K) + c;
-#pragma unroll 4
-            for (int r = 0; r < C; ++r) {
-                const float xq = bf16f(tq[r * D]);
-                const float xk = bf16f(tkk[r * D]);
-                const bool ok = r < n;
-                const float pq = fmaf(w_a.w, xq, fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
-                const float pk = fmaf(w_b.w, xk, fmaf(w_b.z, wb[2], fmaf(w_b.y, wb[1], w_b.x * wb[0])));
-                wa[0] = ok ? wa[1] : wa[0]; wa[1] = ok ? wa[2] : wa[1]; wa[2] = ok ? xq : wa[2];
-                wb[0] = ok ? wb[1] : wb[0]; wb[1] = ok ? wb[2] : wb[1]; wb[2] = ok ? xk : wb[2];
-                const uint32_t ro = rowoff(r);
-                at<float>(sm, OFF_L + cL + ro) = ok ? siluf_(pk) : 0.f;
-                at<float>(sm, OFF_L + cL + C * 128 + ro) = ok ? siluf_(pq) : 0.f;
+        if (a1t < 3) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(
+                sm + (a1t == 0 ? STG_Q : (a1t == 1 ? STG_K : STG_V))) + (c2 >> 1);
+            const uint32_t dst = a1t == 0 ? OFF_L + k2L + C * 128 : (a1t == 1 ? OFF_L + k2L : OFF_V + k2R);
+            // Loads of group g + 1 are issued before the stores of group g (the
+            // compiler may not move loads across possibly aliasing stores).
+            uint32_t nxt[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) nxt[i] = src[i * (D / 2)];
+#pragma unroll 1
+            for (int g = 0; g < C / 8; ++g) {
+                uint32_t cur[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+                if (g + 1 < C / 8) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) nxt[i] = src[((g + 1) * 8 + i) * (D / 2)];
+                }
+                float2 y[8];
+                if (n == C) {   // full chunk: the window shift is register renaming
+                    float a[11], bb[11];
+                    a[0] = win0[0]; a[1] = win0[1]; a[2] = win0[2];
+                    bb[0] = win1[0]; bb[1] = win1[1]; bb[2] = win1[2];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        a[3 + i] = __uint_as_float(cur[i] << 16);
+                        bb[3 + i] = __uint_as_float(cur[i] & 0xffff0000u);
+                        const float p0 = fmaf(w0.w, a[3 + i], fmaf(w0.z, a[2 + i], fmaf(w0.y, a[1 + i], w0.x * a[i])));
+                        const float p1 = fmaf(w1.w, bb[3 + i], fmaf(w1.z, bb[2 + i], fmaf(w1.y, bb[1 + i], w1.x * bb[i])));
+                        y[i] = make_float2(siluf_(p0), siluf_(p1));
+                    }
+                    win0[0] = a[8]; win0[1] = a[9]; win0[2] = a[10];
+                    win1[0] = bb[8]; win1[1] = bb[9]; win1[2] = bb[10];
+                } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = g * 8 + i;
+                    const float x0 = __uint_as_float(cur[i] << 16);
+                    const float x1 = __uint_as_float(cur[i] & 0xffff0000u);
+                    const bool ok = r < n;
+                    const float p0 = fmaf(w0.w, x0, fmaf(w0.z, win0[2], fmaf(w0.y, win0[1], w0.x * win0[0])));
+                    const float p1 = fmaf(w1.w, x1, fmaf(w1.z, win1[2], fmaf(w1.y, win1[1], w1.x * win1[0])));
+                    win0[0] = ok ? win0[1] : win0[0]; win0[1] = ok ? win0[2] : win0[1]; win0[2] = ok ? x0 : win0[2];
+                    win1[0] = ok ? win1[1] : win1[0]; win1[1] = ok ? win1[2] : win1[1]; win1[2] = ok ? x1 : win1[2];
+                    y[i] = make_float2(ok ? siluf_(p0) : 0.f, ok ? siluf_(p1) : 0.f);
+                }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    at<float2>(sm, dst + (g * 8 + i) * 128 + ((ch2 ^ i) << 4)) = y[i];
             }
         } else {
-            const uint16_t* tv = reinterpret_cast<const uint16_t*>(sm + STG_V) + c;
-            const float* tz = reinterpret_cast<const float*>(sm + STG_Z) + c;
-            float G = 0.f;
-#pragma unroll 4
-            for (int r = 0; r < C; ++r) {
-                const float xv = bf16f(tv[r * D]);
-                const float xz = tz[r * D];
-                const bool ok = r < n;
-                const float pv = fmaf(w_a.w, xv, fmaf(w_a.z, wa[2], fmaf(w_a.y, wa[1], w_a.x * wa[0])));
-                wa[0] = ok ? wa[1] : wa[0]; wa[1] = ok ? wa[2] : wa[1]; wa[2] = ok ? xv : wa[2];
-                G -= ok ? expA * softplusf_(xz + dtb) : 0.f;
-                const uint32_t ro = rowoff(r);
-                at<float>(sm, OFF_V + cR + ro) = ok ? siluf_(pv) : 0.f;
-                at<float>(sm, OFF_R + cR + ro) = G;
+            const float2* src = reinterpret_cast<const float2*>(sm + STG_Z) + (c2 >> 1);
+            float G0 = 0.f, G1 = 0.f;
+            float2 nxt[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) nxt[i] = src[i * (D / 2)];
+#pragma unroll 1
+            for (int g = 0; g < C / 8; ++g) {
+                float2 cur[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+                if (g + 1 < C / 8) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) nxt[i] = src[((g + 1) * 8 + i) * (D / 2)];
+                }
+                float2 gg[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const bool ok = g * 8 + i < n;
+                    G0 -= ok ? expA0 * softplusf_(cur[i].x + dtb0) : 0.f;
+                    G1 -= ok ? expA1 * softplusf_(cur[i].y + dtb1) : 0.f;
+                    gg[i] = make_float2(G0, G1);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    at<float2>(sm, OFF_R + k2R + (g * 8 + i) * 128 + ((ch2 ^ i) << 4)) = gg[i];
             }
-            big = -G > kMaxSpan;
-            s_esc[c] = G;   // G_last for now
+            big = (-G0 > kMaxSpan) || (-G1 > kMaxSpan);
+            s_esc[c2] = G0;   // G_last for now
+            s_esc[c2 + 1] = G1;
         }
         const bool fb = __syncthreads_or(big) != 0;
-        if (half == 1) {
-            const float G = s_esc[c];
-            const float rl = fb ? 0.f : 0.5f * G;
-            const float rr = fb ? G : 0.5f * G;
-            s_rhoL[c] = rl;
-            s_rhoR[c] = rr;
-            s_esc[c] = __expf(G - rr);
+        if (a1t == 3) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float G = s_esc[c2 + e];
+                const float rl = fb ? 0.f : 0.5f * G;
+                const float rr = fb ? G : 0.5f * G;
+                s_rhoL[c2 + e] = rl;
+                s_rhoR[c2 + e] = rr;
+                s_esc[c2 + e] = __expf(G - rr);
+            }
         }
 
         // ---- A2: per-token norms of the conv outputs and beta.
@@ -330,18 +395,24 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
 #pragma unroll 1
             for (int g8 = 0; g8 < 4; ++g8) {
                 uint32_t rt[8];
+                float g[8], yk[8], yq[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int r = half * 32 + g8 * 8 + i;
                     const uint32_t ro = rowoff(r);
-                    const float g = at<float>(sm, OFF_R + cR + ro);
-                    const float yk = at<float>(sm, OFF_L + cL + ro) * s_rk[r];
-                    const float yq = at<float>(sm, OFF_L + cL + C * 128 + ro) * s_rq[r];
-                    const float eL = __expf(g - rl);
-                    const float eR = __expf(rr - g);
-                    rt[i] = tc::f2tf32(yk * eR);
-                    at<uint32_t>(sm, OFF_L + cL + ro) = tc::f2tf32(yk * eL);
-                    at<uint32_t>(sm, OFF_L + cL + C * 128 + ro) = tc::f2tf32(yq * eL);
+                    g[i] = at<float>(sm, OFF_R + cR + ro);
+                    yk[i] = at<float>(sm, OFF_L + cL + ro) * s_rk[r];
+                    yq[i] = at<float>(sm, OFF_L + cL + C * 128 + ro) * s_rq[r];
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = half * 32 + g8 * 8 + i;
+                    const uint32_t ro = rowoff(r);
+                    const float eL = __expf(g[i] - rl);
+                    const float eR = __expf(rr - g[i]);
+                    rt[i] = tc::f2tf32(yk[i] * eR);
+                    at<uint32_t>(sm, OFF_L + cL + ro) = tc::f2tf32(yk[i] * eL);
+                    at<uint32_t>(sm, OFF_L + cL + C * 128 + ro) = tc::f2tf32(yq[i] * eL);
                     at<uint32_t>(sm, OFF_R + cR + ro) = rt[i];
                 }
                 tc::st8(tc::taddr(tm, warp, TM_RT + half * 32 + g8 * 8), rt);
@@ -349,21 +420,57 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         publish();
 
-        // ---- MMA0: [A'; P] = L R^T.
-        if (!fb) {
-            if (tid == 0) {
-                constexpr uint32_t id = tc::idesc_tf32(128, 64);
+        // ---- MMA0: [A'; P] = L R^T (runs under the state pass).
+        if (!fb && tid == 0) {
+            constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll 1
-                for (int ks = 0; ks < D / 8; ++ks) {
-                    const int kb = ks >> 2, kin = ks & 3;
-                    tc::mma_ss(tm + TM_D0,
-                               tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)),
-                               tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 8192 + kin * 32)), id,
-                               ks > 0);
-                }
-                tc::commit(s_bar);
+            for (int ks = 0; ks < D / 8; ++ks) {
+                const int kb = ks >> 2, kin = ks & 3;
+                tc::mma_ss(tm + TM_D0,
+                           tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)),
+                           tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 8192 + kin * 32)), id, ks > 0);
             }
-            wt.wait();
+            tc::commit(s_bar);
+        }
+
+        // ---- D: state pass: S^T operand scaled by e^{rho_L}, master scaled by e^{rho_R}.
+        {
+            const float eL = esc_prev * __expf(s_rhoL[qrow]);
+            const float eR = esc_prev * __expf(s_rhoR[qrow]);
+            // S^T operand element (row j, K = qrow): K block and chunk are fixed per thread.
+            const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
+            const int kch = (qrow >> 2) & 7;
+#pragma unroll 1
+            for (int g8 = 0; g8 < 8; ++g8) {
+                uint32_t v[8];
+                const int j0 = half * 64 + g8 * 8;
+                const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
+                tc::ld8(ta, v);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int j = j0 + i;
+                    const float sv = __uint_as_float(v[i]);
+                    at<uint32_t>(sm, OFF_ST + kq + j * 128 + ((kch ^ (j & 7)) << 4)) = tc::f2tf32(sv * eL);
+                    v[i] = __float_as_uint(sv * eR);
+                }
+                tc::st8(ta, v);
+            }
+        }
+        publish();
+        if (!fb) wt.wait();   // MMA0
+
+        // ---- MMA1: D1 = L (Diag(e^rho_L) S0) = [K_g S0; Q_g S0] (runs under the inverse).
+        if (tid == 0) {
+            constexpr uint32_t id = tc::idesc_tf32(128, 128);
+#pragma unroll 1
+            for (int ks = 0; ks < D / 8; ++ks) {
+                const int kb = ks >> 2, kin = ks & 3;
+                tc::mma_ss(tm + TM_D1,
+                           tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)),
+                           tc::desc_sw128(ptx::smem_u32(sm + OFF_ST + kb * 16384 + kin * 32)), id, ks > 0);
+            }
+            tc::commit(s_bar);
         }
 
         // ---- C1: Diag(beta) A' to shared memory, D0 -> [I; P] in TMEM
@@ -467,7 +574,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         publish();
 
-        // ---- MMA_T: [Minv; P Minv] = [I; P] Minv.
+        wt.wait();   // MMA1
+        if (ci + 1 < nchunks) stage_qkz(ci + 1);   // the S^T region is free now
+
+        // ---- MMA_T: [Minv; P Minv] = [I; P] Minv (runs under the X epilogue).
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll 1
@@ -478,59 +588,6 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             tc::commit(s_bar);
         }
-        wt.wait();
-
-        // ---- C4 + D: round DT to tf32 in place; state pass: S^T operand
-        //      scaled by e^{rho_L}, master scaled by e^{rho_R}.
-        {
-#pragma unroll 1
-            for (int g8 = 0; g8 < 4; ++g8) {
-                uint32_t v[8];
-                const uint32_t ta = tc::taddr(tm, warp, TM_DT + half * 32 + g8 * 8);
-                tc::ld8(ta, v);
-                tc::wait_ld();
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = tc::f2tf32(__uint_as_float(v[i]));
-                tc::st8(ta, v);
-            }
-            const float eL = __expf(s_rhoL[qrow]);
-            const float eR = __expf(s_rhoR[qrow]);
-            // S^T operand element (row j, K = qrow): K block and chunk are fixed per thread.
-            const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
-            const int kch = (qrow >> 2) & 7;
-#pragma unroll 1
-            for (int g8 = 0; g8 < 8; ++g8) {
-                uint32_t v[8];
-                const int j0 = half * 64 + g8 * 8;
-                const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
-                tc::ld8(ta, v);
-                tc::wait_ld();
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = j0 + i;
-                    const float sv = __uint_as_float(v[i]);
-                    at<uint32_t>(sm, OFF_ST + kq + j * 128 + ((kch ^ (j & 7)) << 4)) = tc::f2tf32(sv * eL);
-                    v[i] = __float_as_uint(sv * eR);
-                }
-                tc::st8(ta, v);
-            }
-        }
-        publish();
-
-        // ---- MMA1: D1 = L (Diag(e^rho_L) S0) = [K_g S0; Q_g S0].
-        if (tid == 0) {
-            constexpr uint32_t id = tc::idesc_tf32(128, 128);
-#pragma unroll 1
-            for (int ks = 0; ks < D / 8; ++ks) {
-                const int kb = ks >> 2, kin = ks & 3;
-                tc::mma_ss(tm + TM_D1,
-                           tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)),
-                           tc::desc_sw128(ptx::smem_u32(sm + OFF_ST + kb * 16384 + kin * 32)), id, ks > 0);
-            }
-            tc::commit(s_bar);
-        }
-        wt.wait();
-        if (ci + 1 < nchunks) stage(ci + 1);   // S^T and Minv^T regions are free now
 
         // ---- E: X = V - K_g S0 -> Diag(beta) X operand (N=128 x K=64); clear D1 top.
         //      The operand element (row j, K = token r) has a fixed K block and
@@ -564,6 +621,22 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         publish();
 
+        wt.wait();   // MMA_T
+        if (ci + 1 < nchunks) stage_v(ci + 1);     // the Minv^T region is free now
+
+        // ---- DT -> tf32 in place (A operand of MMA2).
+#pragma unroll 1
+        for (int g8 = 0; g8 < 4; ++g8) {
+            uint32_t v[8];
+            const uint32_t ta = tc::taddr(tm, warp, TM_DT + half * 32 + g8 * 8);
+            tc::ld8(ta, v);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = tc::f2tf32(__uint_as_float(v[i]));
+            tc::st8(ta, v);
+        }
+        publish();
+
         // ---- MMA2: D1 += [Minv; P Minv] Diag(beta) X = [U; P U].
         if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
@@ -579,6 +652,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
 
         // ---- F: U -> operand of MMA3 (rows 0..63); sum of squares of O_pre
         //      (rows 64..127).
+        float4 gate4[16];
         if ((warp & 3) < 2) {
             const int r = qrow;
             const uint32_t kr = (uint32_t)((r >> 5) * 128 * 128 + (r & 3) * 4);
@@ -598,6 +672,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
         } else {
             const int r = qrow - C;
+            // Gate logits of this row are loaded now, their latency hidden by the
+            // sum of squares and the MMA3 issue.
+            const size_t orow = row0 + (size_t)(r < n ? r : 0) * tstride + half * 64;
+#pragma unroll
+            for (int q4 = 0; q4 < 16; ++q4)
+                gate4[q4] = *reinterpret_cast<const float4*>(io.gate_logit + orow + q4 * 4);
             float ss = 0.f;
 #pragma unroll 1
             for (int g8 = 0; g8 < 8; ++g8) {
@@ -629,49 +709,36 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const int r = qrow - C;
             const bool live = r < n;
             const float inv = rsqrtf((s_part[r] + s_part[C + r]) * (1.0f / D) + p.rms_eps);
-            const size_t orow = row0 + (size_t)(live ? r : 0) * tstride;
-#pragma unroll 1
+            const size_t orow = row0 + (size_t)(live ? r : 0) * tstride + half * 64;
+            const float* gm = p.gamma + h * D + half * 64;
+#pragma unroll
             for (int g8 = 0; g8 < 8; ++g8) {
-                const int j0 = half * 64 + g8 * 8;
                 uint32_t v[8];
-                tc::ld8(tc::taddr(tm, warp, TM_D1 + j0), v);
+                tc::ld8(tc::taddr(tm, warp, TM_D1 + half * 64 + g8 * 8), v);
+                const float4 ma = *reinterpret_cast<const float4*>(gm + g8 * 8);
+                const float4 mb = *reinterpret_cast<const float4*>(gm + g8 * 8 + 4);
                 tc::wait_ld();
+                const float4 ga = gate4[2 * g8], gb = gate4[2 * g8 + 1];
+                float4 oa, ob;
+                oa.x = ma.x * __uint_as_float(v[0]) * inv * sigmoidf_(ga.x);
+                oa.y = ma.y * __uint_as_float(v[1]) * inv * sigmoidf_(ga.y);
+                oa.z = ma.z * __uint_as_float(v[2]) * inv * sigmoidf_(ga.z);
+                oa.w = ma.w * __uint_as_float(v[3]) * inv * sigmoidf_(ga.w);
+                ob.x = mb.x * __uint_as_float(v[4]) * inv * sigmoidf_(gb.x);
+                ob.y = mb.y * __uint_as_float(v[5]) * inv * sigmoidf_(gb.y);
+                ob.z = mb.z * __uint_as_float(v[6]) * inv * sigmoidf_(gb.z);
+                ob.w = mb.w * __uint_as_float(v[7]) * inv * sigmoidf_(gb.w);
                 if (live) {
-                    const float4 ga = *reinterpret_cast<const float4*>(io.gate_logit + orow + j0);
-                    const float4 gb = *reinterpret_cast<const float4*>(io.gate_logit + orow + j0 + 4);
-                    const float4 ma = *reinterpret_cast<const float4*>(p.gamma + h * D + j0);
-                    const float4 mb = *reinterpret_cast<const float4*>(p.gamma + h * D + j0 + 4);
-                    float4 oa, ob;
-                    oa.x = ma.x * __uint_as_float(v[0]) * inv * sigmoidf_(ga.x);
-                    oa.y = ma.y * __uint_as_float(v[1]) * inv * sigmoidf_(ga.y);
-                    oa.z = ma.z * __uint_as_float(v[2]) * inv * sigmoidf_(ga.z);
-                    oa.w = ma.w * __uint_as_float(v[3]) * inv * sigmoidf_(ga.w);
-                    ob.x = mb.x * __uint_as_float(v[4]) * inv * sigmoidf_(gb.x);
-                    ob.y = mb.y * __uint_as_float(v[5]) * inv * sigmoidf_(gb.y);
-                    ob.z = mb.z * __uint_as_float(v[6]) * inv * sigmoidf_(gb.z);
-                    ob.w = mb.w * __uint_as_float(v[7]) * inv * sigmoidf_(gb.w);
-                    *reinterpret_cast<float4*>(io.o + orow + j0) = oa;
-                    *reinterpret_cast<float4*>(io.o + orow + j0 + 4) = ob;
+                    *reinterpret_cast<float4*>(io.o + orow + g8 * 8) = oa;
+                    *reinterpret_cast<float4*>(io.o + orow + g8 * 8 + 4) = ob;
                 }
             }
         }
         wt.wait();
 
-        // ---- G: S_new = e^{G_last - rho_R} M.
-        {
-            const float e = s_esc[qrow];
-#pragma unroll 1
-            for (int g8 = 0; g8 < 8; ++g8) {
-                uint32_t v[8];
-                const uint32_t ta = tc::taddr(tm, warp, TM_S + half * 64 + g8 * 8);
-                tc::ld8(ta, v);
-                tc::wait_ld();
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * e);
-                tc::st8(ta, v);
-            }
-        }
-        tc::wait_st();
+        // S_new = e^{G_last - rho_R} M: the scale is carried in a register and
+        // applied by the next chunk's state pass (or the final write-back).
+        esc_prev = s_esc[qrow];
         sync_tc();
     }
 
@@ -686,15 +753,15 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<float4*>(dst + j0 + j) =
-                    make_float4(__uint_as_float(s[j]), __uint_as_float(s[j + 1]),
-                                __uint_as_float(s[j + 2]), __uint_as_float(s[j + 3]));
+                    make_float4(esc_prev * __uint_as_float(s[j]), esc_prev * __uint_as_float(s[j + 1]),
+                                esc_prev * __uint_as_float(s[j + 2]), esc_prev * __uint_as_float(s[j + 3]));
         }
-        const size_t ga = (size_t)(half == 0 ? 0 : 2) * HD + (size_t)h * D + c;
-        const size_t gb = HD + (size_t)h * D + c;
+        if (a1t < 3) {
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            win[j * HD3 + ga] = wa[j];
-            if (half == 0) win[j * HD3 + gb] = wb[j];
+            for (int j = 0; j < 3; ++j) {
+                win[j * HD3 + g0] = win0[j];
+                win[j * HD3 + g0 + 1] = win1[j];
+            }
         }
     }
     sync_tc();
