@@ -127,6 +127,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def replica_aggregate(local_ms, units_per_rank, dist=None, device="cpu"):
+    """Replicas across ranks: returns (slowest rank's ms, units of all ranks per s).
+
+    Each rank runs an independent replica of the workload (the (sequence,
+    head) units never interact), so the job's throughput is the units all
+    ranks processed over the slowest rank's time.
+    """
+    world = 1
+    ms = float(local_ms)
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * units_per_rank / (ms * 1e-3)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -165,11 +183,7 @@ class Ours:
         self.torch.cuda.synchronize()
 
     def max_over_ranks(self, x):
-        if self.dist is None:
-            return x
-        t = self.torch.tensor([x], device=self.dev, dtype=self.torch.float64)
-        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
-        return float(t.item())
+        return replica_aggregate(x, 1, self.dist, self.dev)[0]
 
     def flush_l2(self):
         self.flush_w.fill_(1.0)
@@ -416,7 +430,8 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": DECODE_WL, "B": wl.B, "H": wl.H, "d": D,
-                   "calls": wl.T, "l2": "n/a (CPU)"},
+                   "calls_cycled": wl.T, "state_MiB": wl.B * wl.H * D * D * 4 / 2**20,
+                   "l2": "n/a (CPU)", "parallelism": "rank 0 only"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": r["threads"],
                          "kind": "oracle", "sample": r["sample"]},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
