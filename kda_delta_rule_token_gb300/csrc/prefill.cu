@@ -47,7 +47,7 @@ namespace {
 
 constexpr int D = kHeadDim;  // 128
 constexpr int C = kChunk;    // 64
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr float kMaxSpan = 160.0f;
 
 // Dynamic shared memory map (bytes).
@@ -121,6 +121,9 @@ struct Maps {
     CUtensorMap q, k, v, z;   // 4-D (d, H, T, B) boxes of (128, 1, 64, 1)
 };
 
+// 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and takes column group
+// w / 4 of every TMEM pass; in the thread-per-channel passes the same thread
+// owns channel c = its TMEM lane and group grp = w / 4.
 __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __grid_constant__ Maps maps) {
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -130,8 +133,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     float* s_rhoL = s_rk + 64;                                    // [128]
     float* s_rhoR = s_rhoL + 128;                                 // [128]
     float* s_esc = s_rhoR + 128;                                  // [128] e^{G_last - rho_R}
-    float* s_part = s_esc + 128;                                  // [2][64] RMS partial sums
-    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_part + 128);
+    float* s_part = s_esc + 128;                                  // [4][64] RMS partial sums
+    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_part + 256);
     uint64_t* s_tbar = s_bar + 1;                                 // input tiles landed
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 2);
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
@@ -141,11 +144,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     const int b = bh / p.H, h = bh - b * p.H;
     const int H = p.H, T = io.T;
     const size_t HD = (size_t)H * D, HD3 = 3 * HD;
+    const int nchunks = (T + C - 1) / C;
+    const int qrow = (warp & 3) * 32 + lane;   // TMEM lane; channel of the per-channel passes
+    const int grp = warp >> 2;                  // column group / per-channel role (0..3)
+    const int c = qrow;
 
     if (warp == 0) tc::alloc(s_tmem, 512);
-    const int nchunks = (T + C - 1) / C;
-    // Thread 0 stages chunk ci's q, k, v, z tiles with four TMA box loads and
-    // asks L2 for its gate rows; rows past T come back as zeros.
     // Staging of chunk ci's input tiles with TMA box loads (rows past T come
     // back as zeros).  q, k, z land in the S^T operand region and may be
     // issued once MMA1 has read it; v lands in the Minv^T region and may be
@@ -157,9 +161,9 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             ptx::tma_load_4d(sm + STG_K, &maps.k, 0, h, ci * C, b, s_tbar);
             ptx::tma_load_4d(sm + STG_Z, &maps.z, 0, h, ci * C, b, s_tbar);
         }
-        const int r = tid >> 2;   // and ask L2 for the chunk's gate rows
+        const int r = tid >> 3;   // and ask L2 for the chunk's gate rows
         if (ci * C + r < T)
-            ptx::prefetch_l2(io.gate_logit + (((size_t)(b * T + ci * C + r)) * H + h) * D + (tid & 3) * 32);
+            ptx::prefetch_l2(io.gate_logit + (((size_t)(b * T + ci * C + r)) * H + h) * D + (tid & 7) * 16);
     };
     auto stage_v = [&](int ci) {
         if (tid == 0) ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, ci * C, b, s_tbar);
@@ -177,62 +181,40 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     stage_qkz(0);
     stage_v(0);
 
-    // Per-thread roles: c = channel for the thread-per-channel passes; the
-    // TMEM quadrant of this warp is (warp & 3), its column half is warp >> 2.
-    const int c = tid & (D - 1);
-    const int half = tid >> 7;
-    const int qrow = (warp & 3) * 32 + lane;   // TMEM lane of this thread
-
-    // Initial state into the TMEM master.
+    // Initial state into the TMEM master (row qrow, columns of this group).
     {
-        const float* src = io.S + ((size_t)bh * D + qrow) * D + half * 64;
+        const float* src = io.S + ((size_t)bh * D + qrow) * D + grp * 32;
+        uint32_t r[32];
 #pragma unroll
-        for (int j0 = 0; j0 < 64; j0 += 32) {
-            uint32_t r[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 v = *reinterpret_cast<const float4*>(src + j0 + j);
-                r[j] = __float_as_uint(v.x); r[j + 1] = __float_as_uint(v.y);
-                r[j + 2] = __float_as_uint(v.z); r[j + 3] = __float_as_uint(v.w);
-            }
-            tc::st32(tc::taddr(tm, warp, TM_S + half * 64 + j0), r);
+        for (int j = 0; j < 32; j += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src + j);
+            r[j] = __float_as_uint(v.x); r[j + 1] = __float_as_uint(v.y);
+            r[j + 2] = __float_as_uint(v.z); r[j + 3] = __float_as_uint(v.w);
         }
+        tc::st32(tc::taddr(tm, warp, TM_S + grp * 32), r);
         tc::wait_st();
     }
 
-    // Conv / decay roles: tensor a1t = tid / 64 (q, k, v, decay), channel pair
-    // c2, c2 + 1 -- two independent chains per thread.
+    // Conv / decay roles: grp 0, 1, 2 = conv of q, k, v on channel c; grp 3 =
+    // decay of channel c.
     float* win = io.conv_state + (size_t)b * 3 * HD3;
-    const int a1t = tid >> 6;
-    const int c2 = (tid & 63) * 2;
-    float4 w0 = make_float4(0.f, 0.f, 0.f, 0.f), w1 = w0;   // taps
-    float win0[3] = {0.f, 0.f, 0.f}, win1[3] = {0.f, 0.f, 0.f};   // windows, oldest first
-    float expA0 = 0.f, expA1 = 0.f, dtb0 = 0.f, dtb1 = 0.f;
-    const size_t g0 = (size_t)(a1t < 3 ? a1t : 0) * HD + (size_t)h * D + c2;
-    if (a1t < 3) {
-        w0 = *reinterpret_cast<const float4*>(p.conv_w + g0 * 4);
-        w1 = *reinterpret_cast<const float4*>(p.conv_w + (g0 + 1) * 4);
+    const size_t gch = (size_t)(grp < 3 ? grp : 0) * HD + (size_t)h * D + c;
+    float4 wt4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wv[3] = {0.f, 0.f, 0.f};   // window, oldest first
+    float expA = 0.f, dtb = 0.f;
+    if (grp < 3) {
+        wt4 = *reinterpret_cast<const float4*>(p.conv_w + gch * 4);
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            win0[j] = win[j * HD3 + g0];
-            win1[j] = win[j * HD3 + g0 + 1];
-        }
+        for (int j = 0; j < 3; ++j) wv[j] = win[j * HD3 + gch];
     } else {
-        expA0 = expf(p.A_log[h * D + c2]);
-        expA1 = expf(p.A_log[h * D + c2 + 1]);
-        dtb0 = p.dt_bias[h * D + c2];
-        dtb1 = p.dt_bias[h * D + c2 + 1];
+        expA = expf(p.A_log[h * D + c]);
+        dtb = p.dt_bias[h * D + c];
     }
-    const uint32_t k2L = (uint32_t)((c2 >> 5) * 128 * 128 + (c2 & 3) * 4);   // 128-row operands
-    const uint32_t k2R = (uint32_t)((c2 >> 5) * 64 * 128 + (c2 & 3) * 4);    // 64-row operands
-    const int ch2 = (c2 >> 2) & 7;
-
-    // Swizzled addressing for the thread-per-channel passes: channel c is the
-    // K index of the L / R / V layouts (fixed per thread), rows vary.
-    const uint32_t cL = (uint32_t)((c >> 5) * 128 * 128 + (c & 3) * 4);   // 128-row operands
-    const uint32_t cR = (uint32_t)((c >> 5) * 64 * 128 + (c & 3) * 4);    // 64-row operands
+    // Swizzled addressing of channel c as the K index of the L (128-row) and
+    // R / V (64-row) operand layouts.
+    const uint32_t kcL = (uint32_t)((c >> 5) * 128 * 128 + (c & 3) * 4);
+    const uint32_t kcR = (uint32_t)((c >> 5) * 64 * 128 + (c & 3) * 4);
     const int cch = (c >> 2) & 7;
-    auto rowoff = [&](int r) -> uint32_t { return (uint32_t)(r * 128 + ((cch ^ (r & 7)) << 4)); };
 
     float esc_prev = 1.0f;   // pending e^{G_last - rho_R} of the previous chunk, per state row
     for (int ci = 0; ci < nchunks; ++ci) {
@@ -242,133 +224,114 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         const size_t tstride = HD;                                   // elements between tokens
 
         // ---- A1: conv + SiLU per channel over the chunk (from the staged
-        //      tiles); decay and its cumulative sum.
+        //      tiles); decay and its cumulative sum.  Loads of token group
+        //      g + 1 are issued before the stores of group g.
         wtma.wait();
         bool big = false;
-        if (a1t < 3) {
-            const uint32_t* src = reinterpret_cast<const uint32_t*>(
-                sm + (a1t == 0 ? STG_Q : (a1t == 1 ? STG_K : STG_V))) + (c2 >> 1);
-            const uint32_t dst = a1t == 0 ? OFF_L + k2L + C * 128 : (a1t == 1 ? OFF_L + k2L : OFF_V + k2R);
-            // Loads of group g + 1 are issued before the stores of group g (the
-            // compiler may not move loads across possibly aliasing stores).
-            uint32_t nxt[8];
+        if (grp < 3) {
+            const uint16_t* src = reinterpret_cast<const uint16_t*>(
+                sm + (grp == 0 ? STG_Q : (grp == 1 ? STG_K : STG_V))) + c;
+            const uint32_t dst = grp == 0 ? OFF_L + kcL + C * 128 : (grp == 1 ? OFF_L + kcL : OFF_V + kcR);
+            uint16_t nxt[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) nxt[i] = src[i * (D / 2)];
+            for (int i = 0; i < 8; ++i) nxt[i] = src[i * D];
 #pragma unroll 1
             for (int g = 0; g < C / 8; ++g) {
-                uint32_t cur[8];
+                float x[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+                for (int i = 0; i < 8; ++i) x[i] = bf16f(nxt[i]);
                 if (g + 1 < C / 8) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) nxt[i] = src[((g + 1) * 8 + i) * (D / 2)];
+                    for (int i = 0; i < 8; ++i) nxt[i] = src[((g + 1) * 8 + i) * D];
                 }
-                float2 y[8];
+                float y[8];
                 if (n == C) {   // full chunk: the window shift is register renaming
-                    float a[11], bb[11];
-                    a[0] = win0[0]; a[1] = win0[1]; a[2] = win0[2];
-                    bb[0] = win1[0]; bb[1] = win1[1]; bb[2] = win1[2];
+                    float a[11];
+                    a[0] = wv[0]; a[1] = wv[1]; a[2] = wv[2];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        a[3 + i] = __uint_as_float(cur[i] << 16);
-                        bb[3 + i] = __uint_as_float(cur[i] & 0xffff0000u);
-                        const float p0 = fmaf(w0.w, a[3 + i], fmaf(w0.z, a[2 + i], fmaf(w0.y, a[1 + i], w0.x * a[i])));
-                        const float p1 = fmaf(w1.w, bb[3 + i], fmaf(w1.z, bb[2 + i], fmaf(w1.y, bb[1 + i], w1.x * bb[i])));
-                        y[i] = make_float2(siluf_(p0), siluf_(p1));
+                        a[3 + i] = x[i];
+                        y[i] = siluf_(fmaf(wt4.w, a[3 + i], fmaf(wt4.z, a[2 + i], fmaf(wt4.y, a[1 + i], wt4.x * a[i]))));
                     }
-                    win0[0] = a[8]; win0[1] = a[9]; win0[2] = a[10];
-                    win1[0] = bb[8]; win1[1] = bb[9]; win1[2] = bb[10];
+                    wv[0] = a[8]; wv[1] = a[9]; wv[2] = a[10];
                 } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int r = g * 8 + i;
-                    const float x0 = __uint_as_float(cur[i] << 16);
-                    const float x1 = __uint_as_float(cur[i] & 0xffff0000u);
-                    const bool ok = r < n;
-                    const float p0 = fmaf(w0.w, x0, fmaf(w0.z, win0[2], fmaf(w0.y, win0[1], w0.x * win0[0])));
-                    const float p1 = fmaf(w1.w, x1, fmaf(w1.z, win1[2], fmaf(w1.y, win1[1], w1.x * win1[0])));
-                    win0[0] = ok ? win0[1] : win0[0]; win0[1] = ok ? win0[2] : win0[1]; win0[2] = ok ? x0 : win0[2];
-                    win1[0] = ok ? win1[1] : win1[0]; win1[1] = ok ? win1[2] : win1[1]; win1[2] = ok ? x1 : win1[2];
-                    y[i] = make_float2(ok ? siluf_(p0) : 0.f, ok ? siluf_(p1) : 0.f);
-                }
+                    for (int i = 0; i < 8; ++i) {
+                        const bool ok = g * 8 + i < n;
+                        const float pre = fmaf(wt4.w, x[i], fmaf(wt4.z, wv[2], fmaf(wt4.y, wv[1], wt4.x * wv[0])));
+                        wv[0] = ok ? wv[1] : wv[0]; wv[1] = ok ? wv[2] : wv[1]; wv[2] = ok ? x[i] : wv[2];
+                        y[i] = ok ? siluf_(pre) : 0.f;
+                    }
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    at<float2>(sm, dst + (g * 8 + i) * 128 + ((ch2 ^ i) << 4)) = y[i];
+                for (int i = 0; i < 8; ++i) at<float>(sm, dst + (g * 8 + i) * 128 + ((cch ^ i) << 4)) = y[i];
             }
         } else {
-            const float2* src = reinterpret_cast<const float2*>(sm + STG_Z) + (c2 >> 1);
-            float G0 = 0.f, G1 = 0.f;
-            float2 nxt[8];
+            const float* src = reinterpret_cast<const float*>(sm + STG_Z) + c;
+            float G = 0.f;
+            float nxt[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) nxt[i] = src[i * (D / 2)];
+            for (int i = 0; i < 8; ++i) nxt[i] = src[i * D];
 #pragma unroll 1
             for (int g = 0; g < C / 8; ++g) {
-                float2 cur[8];
+                float zc[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+                for (int i = 0; i < 8; ++i) zc[i] = nxt[i];
                 if (g + 1 < C / 8) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) nxt[i] = src[((g + 1) * 8 + i) * (D / 2)];
+                    for (int i = 0; i < 8; ++i) nxt[i] = src[((g + 1) * 8 + i) * D];
                 }
-                float2 gg[8];
+                float gg[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const bool ok = g * 8 + i < n;
-                    G0 -= ok ? expA0 * softplusf_(cur[i].x + dtb0) : 0.f;
-                    G1 -= ok ? expA1 * softplusf_(cur[i].y + dtb1) : 0.f;
-                    gg[i] = make_float2(G0, G1);
+                    G -= (g * 8 + i < n) ? expA * softplusf_(zc[i] + dtb) : 0.f;
+                    gg[i] = G;
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    at<float2>(sm, OFF_R + k2R + (g * 8 + i) * 128 + ((ch2 ^ i) << 4)) = gg[i];
+                for (int i = 0; i < 8; ++i) at<float>(sm, OFF_R + kcR + (g * 8 + i) * 128 + ((cch ^ i) << 4)) = gg[i];
             }
-            big = (-G0 > kMaxSpan) || (-G1 > kMaxSpan);
-            s_esc[c2] = G0;   // G_last for now
-            s_esc[c2 + 1] = G1;
+            big = -G > kMaxSpan;
+            s_esc[c] = G;   // G_last for now
         }
         const bool fb = __syncthreads_or(big) != 0;
-        if (a1t == 3) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float G = s_esc[c2 + e];
-                const float rl = fb ? 0.f : 0.5f * G;
-                const float rr = fb ? G : 0.5f * G;
-                s_rhoL[c2 + e] = rl;
-                s_rhoR[c2 + e] = rr;
-                s_esc[c2 + e] = __expf(G - rr);
-            }
+        if (grp == 3) {
+            const float G = s_esc[c];
+            const float rl = fb ? 0.f : 0.5f * G;
+            const float rr = fb ? G : 0.5f * G;
+            s_rhoL[c] = rl;
+            s_rhoR[c] = rr;
+            s_esc[c] = __expf(G - rr);
         }
 
-        // ---- A2: per-token norms of the conv outputs and beta.
-        if (tid < 2 * C) {
-            const int r = tid & (C - 1);
-            const int rowL = tid < C ? r : C + r;   // y_k rows first, then y_q
+        // ---- A2: per-token norms of the conv outputs (4 threads per row) and beta.
+        {
+            const int R = tid >> 2, part = tid & 3;   // L row: y_k rows 0..63, y_q rows 64..127
             float ss = 0.f;
-#pragma unroll 8
-            for (int k4 = 0; k4 < D; k4 += 4) {
-                const float4 v = at<float4>(sm, OFF_L + tc::sw128(rowL, k4, 128));
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 v = at<float4>(sm, OFF_L + tc::sw128(R, part * 32 + j, 128));
                 ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
             }
-            (tid < C ? s_rk : s_rq)[r] = rsqrtf(ss + p.l2_eps);
-        } else if (tid < 3 * C) {
-            const int r = tid - 2 * C;
-            s_beta[r] = r < n ? sigmoidf_(io.beta_logit[((size_t)(b * T + t0 + r)) * H + h]) : 0.f;
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            if (part == 0) (R < C ? s_rk : s_rq)[R & (C - 1)] = rsqrtf(ss + p.l2_eps);
+            if (tid < C)
+                s_beta[tid] = tid < n ? sigmoidf_(io.beta_logit[((size_t)(b * T + t0 + tid)) * H + h]) : 0.f;
         }
         __syncthreads();
 
         // ---- A2b (rare): exact [A'; P] when the chunk decays by more than kMaxSpan.
         if (fb) {
-            const int R = tid & 127;           // D0 row: A' rows 0..63, P rows 64..127
+            const int R = qrow;                // D0 row: A' rows 0..63, P rows 64..127
             const int r = R & (C - 1);
             const bool isP = R >= C;
             const float rn = isP ? s_rq[r] : s_rk[r];
 #pragma unroll 1
-            for (int g8 = 0; g8 < 4; ++g8) {
+            for (int g8 = 0; g8 < 2; ++g8) {
                 uint32_t out[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int col = half * 32 + g8 * 8 + i;
+                    const int col = grp * 16 + g8 * 8 + i;
                     float acc = 0.f;
                     if (isP ? col <= r : col < r) {
 #pragma unroll 4
@@ -382,40 +345,40 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                     }
                     out[i] = __float_as_uint(acc * rn * s_rk[col]);
                 }
-                tc::st8(tc::taddr(tm, warp, TM_D0 + half * 32 + g8 * 8), out);
+                tc::st8(tc::taddr(tm, warp, TM_D0 + grp * 16 + g8 * 8), out);
             }
             tc::wait_st();
             __syncthreads();
         }
 
         // ---- A3: L, R (shared memory, in place over the staging) and R^T
-        //      (TMEM), 8 tokens at a time.
+        //      (TMEM), channel c, tokens [16 grp, 16 grp + 16), 8 at a time.
         {
             const float rl = s_rhoL[c], rr = s_rhoR[c];
 #pragma unroll 1
-            for (int g8 = 0; g8 < 4; ++g8) {
+            for (int g8 = 0; g8 < 2; ++g8) {
                 uint32_t rt[8];
                 float g[8], yk[8], yq[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int r = half * 32 + g8 * 8 + i;
-                    const uint32_t ro = rowoff(r);
-                    g[i] = at<float>(sm, OFF_R + cR + ro);
-                    yk[i] = at<float>(sm, OFF_L + cL + ro) * s_rk[r];
-                    yq[i] = at<float>(sm, OFF_L + cL + C * 128 + ro) * s_rq[r];
+                    const int r = grp * 16 + g8 * 8 + i;
+                    const uint32_t ro = (uint32_t)(r * 128 + ((cch ^ (r & 7)) << 4));
+                    g[i] = at<float>(sm, OFF_R + kcR + ro);
+                    yk[i] = at<float>(sm, OFF_L + kcL + ro) * s_rk[r];
+                    yq[i] = at<float>(sm, OFF_L + kcL + C * 128 + ro) * s_rq[r];
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int r = half * 32 + g8 * 8 + i;
-                    const uint32_t ro = rowoff(r);
+                    const int r = grp * 16 + g8 * 8 + i;
+                    const uint32_t ro = (uint32_t)(r * 128 + ((cch ^ (r & 7)) << 4));
                     const float eL = __expf(g[i] - rl);
                     const float eR = __expf(rr - g[i]);
                     rt[i] = tc::f2tf32(yk[i] * eR);
-                    at<uint32_t>(sm, OFF_L + cL + ro) = tc::f2tf32(yk[i] * eL);
-                    at<uint32_t>(sm, OFF_L + cL + C * 128 + ro) = tc::f2tf32(yq[i] * eL);
-                    at<uint32_t>(sm, OFF_R + cR + ro) = rt[i];
+                    at<uint32_t>(sm, OFF_L + kcL + ro) = tc::f2tf32(yk[i] * eL);
+                    at<uint32_t>(sm, OFF_L + kcL + C * 128 + ro) = tc::f2tf32(yq[i] * eL);
+                    at<uint32_t>(sm, OFF_R + kcR + ro) = rt[i];
                 }
-                tc::st8(tc::taddr(tm, warp, TM_RT + half * 32 + g8 * 8), rt);
+                tc::st8(tc::taddr(tm, warp, TM_RT + grp * 16 + g8 * 8), rt);
             }
         }
         publish();
@@ -433,7 +396,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             tc::commit(s_bar);
         }
 
-        // ---- D: state pass: S^T operand scaled by e^{rho_L}, master scaled by e^{rho_R}.
+        // ---- D: state pass: S^T operand scaled by e^{rho_L}, master scaled by
+        //      e^{rho_R} (both also by the previous chunk's pending scale).
         {
             const float eL = esc_prev * __expf(s_rhoL[qrow]);
             const float eR = esc_prev * __expf(s_rhoR[qrow]);
@@ -441,9 +405,9 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
             const int kch = (qrow >> 2) & 7;
 #pragma unroll 1
-            for (int g8 = 0; g8 < 8; ++g8) {
+            for (int g8 = 0; g8 < 4; ++g8) {
                 uint32_t v[8];
-                const int j0 = half * 64 + g8 * 8;
+                const int j0 = grp * 32 + g8 * 8;
                 const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
                 tc::ld8(ta, v);
                 tc::wait_ld();
@@ -474,15 +438,15 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
 
         // ---- C1: Diag(beta) A' to shared memory, D0 -> [I; P] in TMEM
-        //      (warp quadrant = 32 rows, warp >> 2 = 32-column half).
+        //      (row qrow, columns [16 grp, 16 grp + 16)).
         {
             float* sM = reinterpret_cast<float*>(sm + OFF_R);   // [64][64], R is no longer needed
             const bool isA = qrow < C;
             const int r = isA ? qrow : qrow - C;
             const float br = s_beta[r];
 #pragma unroll 1
-            for (int g8 = 0; g8 < 4; ++g8) {
-                const int i0 = half * 32 + g8 * 8;
+            for (int g8 = 0; g8 < 2; ++g8) {
+                const int i0 = grp * 16 + g8 * 8;
                 uint32_t v[8];
                 tc::ld8(tc::taddr(tm, warp, TM_D0 + i0), v);
                 tc::wait_ld();
@@ -561,7 +525,6 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 __syncthreads();
             }
             // Minv^T operand: row j holds Minv[.][j]; zero above the diagonal.
-#pragma unroll 1
             for (int e = tid; e < C * C / 4; e += kThreads) {
                 const int j = e >> 4, i = (e & 15) * 4;
                 uint4 u;
@@ -573,7 +536,6 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
         }
         publish();
-
         wt.wait();   // MMA1
         if (ci + 1 < nchunks) stage_qkz(ci + 1);   // the S^T region is free now
 
@@ -597,10 +559,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const float br = s_beta[r];
             const uint32_t kr = (uint32_t)((r >> 5) * 128 * 128 + (r & 3) * 4);
             const int rch = (r >> 2) & 7;
-            const uint32_t vrow = OFF_V + r * 128;   // + K block of j, swizzled chunk
+            const uint32_t vrow = OFF_V + r * 128;
 #pragma unroll 1
-            for (int g8 = 0; g8 < 8; ++g8) {
-                const int j0 = half * 64 + g8 * 8;
+            for (int g8 = 0; g8 < 4; ++g8) {
+                const int j0 = grp * 32 + g8 * 8;
                 uint32_t v[8];
                 const uint32_t ta = tc::taddr(tm, warp, TM_D1 + j0);
                 tc::ld8(ta, v);
@@ -620,15 +582,14 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
         }
         publish();
-
         wt.wait();   // MMA_T
         if (ci + 1 < nchunks) stage_v(ci + 1);     // the Minv^T region is free now
 
         // ---- DT -> tf32 in place (A operand of MMA2).
 #pragma unroll 1
-        for (int g8 = 0; g8 < 4; ++g8) {
+        for (int g8 = 0; g8 < 2; ++g8) {
             uint32_t v[8];
-            const uint32_t ta = tc::taddr(tm, warp, TM_DT + half * 32 + g8 * 8);
+            const uint32_t ta = tc::taddr(tm, warp, TM_DT + grp * 16 + g8 * 8);
             tc::ld8(ta, v);
             tc::wait_ld();
 #pragma unroll
@@ -651,15 +612,15 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         wt.wait();
 
         // ---- F: U -> operand of MMA3 (rows 0..63); sum of squares of O_pre
-        //      (rows 64..127).
-        float4 gate4[16];
+        //      (rows 64..127, gate logits loaded alongside).
+        float4 gate4[8];
         if ((warp & 3) < 2) {
             const int r = qrow;
             const uint32_t kr = (uint32_t)((r >> 5) * 128 * 128 + (r & 3) * 4);
             const int rch = (r >> 2) & 7;
 #pragma unroll 1
-            for (int g8 = 0; g8 < 8; ++g8) {
-                const int j0 = half * 64 + g8 * 8;
+            for (int g8 = 0; g8 < 4; ++g8) {
+                const int j0 = grp * 32 + g8 * 8;
                 uint32_t v[8];
                 tc::ld8(tc::taddr(tm, warp, TM_D1 + j0), v);
                 tc::wait_ld();
@@ -672,22 +633,20 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
         } else {
             const int r = qrow - C;
-            // Gate logits of this row are loaded now, their latency hidden by the
-            // sum of squares and the MMA3 issue.
-            const size_t orow = row0 + (size_t)(r < n ? r : 0) * tstride + half * 64;
+            const size_t orow = row0 + (size_t)(r < n ? r : 0) * tstride + grp * 32;
 #pragma unroll
-            for (int q4 = 0; q4 < 16; ++q4)
+            for (int q4 = 0; q4 < 8; ++q4)
                 gate4[q4] = *reinterpret_cast<const float4*>(io.gate_logit + orow + q4 * 4);
             float ss = 0.f;
 #pragma unroll 1
-            for (int g8 = 0; g8 < 8; ++g8) {
+            for (int g8 = 0; g8 < 4; ++g8) {
                 uint32_t v[8];
-                tc::ld8(tc::taddr(tm, warp, TM_D1 + half * 64 + g8 * 8), v);
+                tc::ld8(tc::taddr(tm, warp, TM_D1 + grp * 32 + g8 * 8), v);
                 tc::wait_ld();
 #pragma unroll
                 for (int i = 0; i < 8; ++i) ss = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss);
             }
-            s_part[half * C + r] = ss;
+            s_part[grp * C + r] = ss;
         }
         publish();   // U operand visible; partial sums visible
 
@@ -708,13 +667,14 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             // tcgen05.ld is warp-collective: every lane loads, only rows r < n store.
             const int r = qrow - C;
             const bool live = r < n;
-            const float inv = rsqrtf((s_part[r] + s_part[C + r]) * (1.0f / D) + p.rms_eps);
-            const size_t orow = row0 + (size_t)(live ? r : 0) * tstride + half * 64;
-            const float* gm = p.gamma + h * D + half * 64;
+            const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
+                                         (1.0f / D) + p.rms_eps);
+            const size_t orow = row0 + (size_t)(live ? r : 0) * tstride + grp * 32;
+            const float* gm = p.gamma + h * D + grp * 32;
 #pragma unroll
-            for (int g8 = 0; g8 < 8; ++g8) {
+            for (int g8 = 0; g8 < 4; ++g8) {
                 uint32_t v[8];
-                tc::ld8(tc::taddr(tm, warp, TM_D1 + half * 64 + g8 * 8), v);
+                tc::ld8(tc::taddr(tm, warp, TM_D1 + grp * 32 + g8 * 8), v);
                 const float4 ma = *reinterpret_cast<const float4*>(gm + g8 * 8);
                 const float4 mb = *reinterpret_cast<const float4*>(gm + g8 * 8 + 4);
                 tc::wait_ld();
@@ -744,24 +704,18 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
 
     // Final state and conv window back to global memory.
     {
-        float* dst = io.S + ((size_t)bh * D + qrow) * D + half * 64;
+        float* dst = io.S + ((size_t)bh * D + qrow) * D + grp * 32;
+        uint32_t s[32];
+        tc::ld32(tc::taddr(tm, warp, TM_S + grp * 32), s);
+        tc::wait_ld();
 #pragma unroll
-        for (int j0 = 0; j0 < 64; j0 += 32) {
-            uint32_t s[32];
-            tc::ld32(tc::taddr(tm, warp, TM_S + half * 64 + j0), s);
-            tc::wait_ld();
+        for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(dst + j) =
+                make_float4(esc_prev * __uint_as_float(s[j]), esc_prev * __uint_as_float(s[j + 1]),
+                            esc_prev * __uint_as_float(s[j + 2]), esc_prev * __uint_as_float(s[j + 3]));
+        if (grp < 3) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(dst + j0 + j) =
-                    make_float4(esc_prev * __uint_as_float(s[j]), esc_prev * __uint_as_float(s[j + 1]),
-                                esc_prev * __uint_as_float(s[j + 2]), esc_prev * __uint_as_float(s[j + 3]));
-        }
-        if (a1t < 3) {
-#pragma unroll
-            for (int j = 0; j < 3; ++j) {
-                win[j * HD3 + g0] = win0[j];
-                win[j * HD3 + g0 + 1] = win1[j];
-            }
+            for (int j = 0; j < 3; ++j) win[j * HD3 + gch] = wv[j];
         }
     }
     sync_tc();
