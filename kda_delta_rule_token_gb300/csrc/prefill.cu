@@ -61,7 +61,9 @@ constexpr uint32_t OFF_R = OFF_L + 65536;     // R operand 64 x 128; staging of 
 constexpr uint32_t OFF_V = OFF_R + 32768;     // v conv output, fp32 64 x 128 (SW128 layout)
 constexpr uint32_t OFF_MT = OFF_V + 32768;    // Minv^T operand N=64 x K=64; stages the v tile
 constexpr uint32_t OFF_SMALL = OFF_MT + 16384;
-constexpr uint32_t kSmemBytes = OFF_SMALL + 4096;
+constexpr uint32_t OFF_WIN = OFF_SMALL + 4096;   // conv window for the next chunk's first half, [3][3][128] fp32
+constexpr uint32_t OFF_WIN0 = OFF_WIN + 4608;    // the initial conv window, [3][3][128] fp32
+constexpr uint32_t kSmemBytes = OFF_WIN0 + 4608;
 constexpr uint32_t STG_Q = OFF_ST, STG_K = OFF_ST + 16384, STG_Z = OFF_ST + 32768, STG_V = OFF_MT;
 constexpr uint32_t kStageBytes = 3 * C * D * 2 + C * D * 4;   // 80 KiB per chunk
 
@@ -72,12 +74,84 @@ constexpr int TM_D0 = 256;  // [A'; P] -> [I; P] (A operand of MMA_T)
 constexpr int TM_DT = 320;  // [Minv; P Minv] (A operand of MMA2)
 constexpr int TM_RT = 384;  // R^T (A operand of MMA3), lane = channel, column = token
 
-__device__ __forceinline__ float bf16f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
 // Fast-intrinsic forms (relative error ~1e-6, far inside the tf32 operand rounding).
 __device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float siluf_(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
-__device__ __forceinline__ float softplusf_(float x) {
-    return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x)));
+
+// Packed pairs of fp32 (fma/mul/add .f32x2) and single-instruction
+// approximations of 2^x, log2(x) and 1/x.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pk(float a, float b) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk(f32x2 v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float ex2f_(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2f_(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcpf_(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
+constexpr float kLn2 = 0.6931471805599453f;     // ln(2)
+
+// SiLU of a pair: x / (1 + e^{-x}).
+__device__ __forceinline__ f32x2 silu2(f32x2 x) {
+    float a, b;
+    upk(mul2(x, pk(-kLog2e, -kLog2e)), a, b);
+    float d0, d1;
+    upk(add2(pk(ex2f_(a), ex2f_(b)), pk(1.0f, 1.0f)), d0, d1);
+    return mul2(x, pk(rcpf_(d0), rcpf_(d1)));
+}
+
+// softplus of a pair: max(x, 0) + ln(1 + e^{-|x|}).
+__device__ __forceinline__ f32x2 softplus2(f32x2 x) {
+    float a, b;
+    upk(x, a, b);
+    const f32x2 ax = pk(fabsf(a), fabsf(b));
+    float e0, e1;
+    upk(mul2(ax, pk(-kLog2e, -kLog2e)), e0, e1);
+    float l0, l1;
+    upk(add2(pk(ex2f_(e0), ex2f_(e1)), pk(1.0f, 1.0f)), l0, l1);
+    const f32x2 relu = mul2(add2(x, ax), pk(0.5f, 0.5f));
+    return fma2(pk(lg2f_(l0), lg2f_(l1)), pk(kLn2, kLn2), relu);
+}
+
+// Warp-level D (16 x 8, fp32) += A (16 x 8, tf32, row-major) * B (8 x 8, tf32):
+// lane (g = lane / 4, t = lane % 4) holds A (g, t), (g + 8, t), (g, t + 4),
+// (g + 8, t + 4); B (t, g), (t + 4, g); D (g, 2t), (g, 2t + 1), (g + 8, 2t),
+// (g + 8, 2t + 1).
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 template <typename T>
@@ -134,7 +208,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     float* s_rhoR = s_rhoL + 128;                                 // [128]
     float* s_esc = s_rhoR + 128;                                  // [128] e^{G_last - rho_R}
     float* s_part = s_esc + 128;                                  // [4][64] RMS partial sums
-    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_part + 256);
+    float* s_gtot = s_part + 256;                                 // [128] decay total of tokens 0..31
+    float* s_win = reinterpret_cast<float*>(sm + OFF_WIN);        // [3][3][128]
+    float* s_win0 = reinterpret_cast<float*>(sm + OFF_WIN0);      // [3][3][128]
+    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_gtot + 128);
     uint64_t* s_tbar = s_bar + 1;                                 // input tiles landed
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 2);
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
@@ -195,21 +272,38 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         tc::wait_st();
     }
 
-    // Conv / decay roles: grp 0, 1, 2 = conv of q, k, v on channel c; grp 3 =
-    // decay of channel c.
+    // Conv / decay roles: grp 0, 1, 2 = conv of q, k, v; grp 3 = decay; each
+    // thread takes the channel pair (cp, cp + 1) for tokens [32 th, 32 th + 32).
     float* win = io.conv_state + (size_t)b * 3 * HD3;
-    const size_t gch = (size_t)(grp < 3 ? grp : 0) * HD + (size_t)h * D + c;
-    float4 wt4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wv[3] = {0.f, 0.f, 0.f};   // window, oldest first
-    float expA = 0.f, dtb = 0.f;
+    const int cp = (tid & 63) * 2;
+    const int th = (tid >> 6) & 1;
+    const size_t gcp = (size_t)(grp < 3 ? grp : 0) * HD + (size_t)h * D + cp;
+    f32x2 W0 = 0, W1 = 0, W2 = 0, W3 = 0;   // taps (tap 3 multiplies the current token)
+    f32x2 nEA = 0, DTB = 0;                 // -exp(A_log), dt_bias
     if (grp < 3) {
-        wt4 = *reinterpret_cast<const float4*>(p.conv_w + gch * 4);
+        const float4 a = *reinterpret_cast<const float4*>(p.conv_w + gcp * 4);
+        const float4 bq = *reinterpret_cast<const float4*>(p.conv_w + (gcp + 1) * 4);
+        W0 = pk(a.x, bq.x); W1 = pk(a.y, bq.y); W2 = pk(a.z, bq.z); W3 = pk(a.w, bq.w);
+        if (th == 0) {
 #pragma unroll
-        for (int j = 0; j < 3; ++j) wv[j] = win[j * HD3 + gch];
+            for (int j = 0; j < 3; ++j) {
+                const float2 w = *reinterpret_cast<const float2*>(win + j * HD3 + gcp);
+                *reinterpret_cast<float2*>(s_win + (grp * 3 + j) * D + cp) = w;
+                *reinterpret_cast<float2*>(s_win0 + (grp * 3 + j) * D + cp) = w;
+            }
+        }
     } else {
-        expA = expf(p.A_log[h * D + c]);
-        dtb = p.dt_bias[h * D + c];
+        nEA = pk(-expf(p.A_log[h * D + cp]), -expf(p.A_log[h * D + cp + 1]));
+        DTB = pk(p.dt_bias[h * D + cp], p.dt_bias[h * D + cp + 1]);
     }
+    // Swizzled addressing of the channel pair as the K index of the L
+    // (128-row) and R / V (64-row) operand layouts.
+    const uint32_t kpL = (uint32_t)((cp >> 5) * 128 * 128 + (cp & 3) * 4);
+    const uint32_t kpR = (uint32_t)((cp >> 5) * 64 * 128 + (cp & 3) * 4);
+    const int pch = (cp >> 2) & 7;
+    f32x2 keep0 = 0, keep1 = 0, keep2 = 0;   // last three inputs of a second-half conv thread
+    f32x2 g1sum = 0;                         // decay total of a second-half decay thread
+
     // Swizzled addressing of channel c as the K index of the L (128-row) and
     // R / V (64-row) operand layouts.
     const uint32_t kcL = (uint32_t)((c >> 5) * 128 * 128 + (c & 3) * 4);
@@ -226,81 +320,130 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- A1: conv + SiLU per channel over the chunk (from the staged
         //      tiles); decay and its cumulative sum.  Loads of token group
         //      g + 1 are issued before the stores of group g.
+        // beta logits of the chunk, consumed after the conv phase.
+        const float blog = tid < n ? io.beta_logit[((size_t)(b * T + t0 + tid)) * H + h] : 0.f;
         wtma.wait();
-        bool big = false;
         if (grp < 3) {
-            const uint16_t* src = reinterpret_cast<const uint16_t*>(
-                sm + (grp == 0 ? STG_Q : (grp == 1 ? STG_K : STG_V))) + c;
-            const uint32_t dst = grp == 0 ? OFF_L + kcL + C * 128 : (grp == 1 ? OFF_L + kcL : OFF_V + kcR);
-            uint16_t nxt[8];
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(
+                sm + (grp == 0 ? STG_Q : (grp == 1 ? STG_K : STG_V))) + (cp >> 1);
+            const uint32_t dst = grp == 0 ? OFF_L + kpL + C * 128 : (grp == 1 ? OFF_L + kpL : OFF_V + kpR);
+            auto unpk_bf2 = [](uint32_t u) { return pk(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)); };
+            f32x2 M3, M2, M1;   // window, oldest first
+            if (th == 0) {
+                const float* w = s_win + grp * 3 * D + cp;
+                M3 = pk(w[0], w[1]); M2 = pk(w[D], w[D + 1]); M1 = pk(w[2 * D], w[2 * D + 1]);
+            } else {
+                M3 = unpk_bf2(src[29 * (D / 2)]); M2 = unpk_bf2(src[30 * (D / 2)]); M1 = unpk_bf2(src[31 * (D / 2)]);
+            }
+            const int r0 = th * 32;
+            uint32_t nxt[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) nxt[i] = src[i * D];
+            for (int i = 0; i < 8; ++i) nxt[i] = src[(r0 + i) * (D / 2)];
 #pragma unroll 1
-            for (int g = 0; g < C / 8; ++g) {
-                float x[8];
+            for (int g = 0; g < 4; ++g) {
+                f32x2 x[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = bf16f(nxt[i]);
-                if (g + 1 < C / 8) {
+                for (int i = 0; i < 8; ++i) x[i] = unpk_bf2(nxt[i]);
+                if (g < 3) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) nxt[i] = src[((g + 1) * 8 + i) * D];
+                    for (int i = 0; i < 8; ++i) nxt[i] = src[(r0 + (g + 1) * 8 + i) * (D / 2)];
                 }
-                float y[8];
+                f32x2 y[8];
                 if (n == C) {   // full chunk: the window shift is register renaming
-                    float a[11];
-                    a[0] = wv[0]; a[1] = wv[1]; a[2] = wv[2];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        a[3 + i] = x[i];
-                        y[i] = siluf_(fmaf(wt4.w, a[3 + i], fmaf(wt4.z, a[2 + i], fmaf(wt4.y, a[1 + i], wt4.x * a[i]))));
+                        f32x2 pre = mul2(W0, M3);
+                        pre = fma2(W1, M2, pre);
+                        pre = fma2(W2, M1, pre);
+                        pre = fma2(W3, x[i], pre);
+                        y[i] = silu2(pre);
+                        M3 = M2; M2 = M1; M1 = x[i];
                     }
-                    wv[0] = a[8]; wv[1] = a[9]; wv[2] = a[10];
                 } else {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const bool ok = g * 8 + i < n;
-                        const float pre = fmaf(wt4.w, x[i], fmaf(wt4.z, wv[2], fmaf(wt4.y, wv[1], wt4.x * wv[0])));
-                        wv[0] = ok ? wv[1] : wv[0]; wv[1] = ok ? wv[2] : wv[1]; wv[2] = ok ? x[i] : wv[2];
-                        y[i] = ok ? siluf_(pre) : 0.f;
+                        const bool ok = r0 + g * 8 + i < n;
+                        f32x2 pre = mul2(W0, M3);
+                        pre = fma2(W1, M2, pre);
+                        pre = fma2(W2, M1, pre);
+                        pre = fma2(W3, x[i], pre);
+                        y[i] = ok ? silu2(pre) : 0ull;
+                        if (ok) { M3 = M2; M2 = M1; M1 = x[i]; }
                     }
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) at<float>(sm, dst + (g * 8 + i) * 128 + ((cch ^ i) << 4)) = y[i];
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + g * 8 + i;
+                    at<f32x2>(sm, dst + r * 128 + ((pch ^ (r & 7)) << 4)) = y[i];
+                }
             }
+            keep0 = M3; keep1 = M2; keep2 = M1;
         } else {
-            const float* src = reinterpret_cast<const float*>(sm + STG_Z) + c;
-            float G = 0.f;
-            float nxt[8];
+            const f32x2* src = reinterpret_cast<const f32x2*>(sm + STG_Z) + (cp >> 1);
+            const int r0 = th * 32;
+            f32x2 G = 0;   // (0, 0)
+            f32x2 nxt[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) nxt[i] = src[i * D];
+            for (int i = 0; i < 8; ++i) nxt[i] = src[(r0 + i) * (D / 2)];
 #pragma unroll 1
-            for (int g = 0; g < C / 8; ++g) {
-                float zc[8];
+            for (int g = 0; g < 4; ++g) {
+                f32x2 zc[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) zc[i] = nxt[i];
-                if (g + 1 < C / 8) {
+                if (g < 3) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) nxt[i] = src[((g + 1) * 8 + i) * D];
+                    for (int i = 0; i < 8; ++i) nxt[i] = src[(r0 + (g + 1) * 8 + i) * (D / 2)];
                 }
-                float gg[8];
+                f32x2 gg[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    G -= (g * 8 + i < n) ? expA * softplusf_(zc[i] + dtb) : 0.f;
+                    const f32x2 sp = softplus2(add2(zc[i], DTB));
+                    if (r0 + g * 8 + i < n) G = fma2(nEA, sp, G);
                     gg[i] = G;
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) at<float>(sm, OFF_R + kcR + (g * 8 + i) * 128 + ((cch ^ i) << 4)) = gg[i];
+                for (int i = 0; i < 8; ++i) {
+                    const int r = r0 + g * 8 + i;
+                    at<f32x2>(sm, OFF_R + kpR + r * 128 + ((pch ^ (r & 7)) << 4)) = gg[i];
+                }
             }
-            big = -G > kMaxSpan;
-            s_esc[c] = G;   // G_last for now
+            if (th == 0) *reinterpret_cast<f32x2*>(s_gtot + cp) = G;
+            else g1sum = G;
+        }
+        __syncthreads();
+
+        // ---- A1b: second-half decay threads add the first half's total; the
+        //      second-half conv threads hand the next chunk its window.
+        bool big = false;
+        if (grp == 3 && th == 1) {
+            const f32x2 off = *reinterpret_cast<const f32x2*>(s_gtot + cp);
+#pragma unroll 4
+            for (int r = 32; r < C; ++r) {
+                const uint32_t o = OFF_R + kpR + r * 128 + ((pch ^ (r & 7)) << 4);
+                at<f32x2>(sm, o) = add2(at<f32x2>(sm, o), off);
+            }
+            float g0, g1;
+            upk(add2(off, g1sum), g0, g1);   // G_last
+            big = (-g0 > kMaxSpan) || (-g1 > kMaxSpan);
+            s_esc[cp] = g0;                   // G_last for now
+            s_esc[cp + 1] = g1;
+        } else if (grp < 3 && th == 1) {
+            float* w = s_win + grp * 3 * D + cp;
+            upk(keep0, w[0], w[1]);
+            upk(keep1, w[D], w[D + 1]);
+            upk(keep2, w[2 * D], w[2 * D + 1]);
         }
         const bool fb = __syncthreads_or(big) != 0;
-        if (grp == 3) {
-            const float G = s_esc[c];
-            const float rl = fb ? 0.f : 0.5f * G;
-            const float rr = fb ? G : 0.5f * G;
-            s_rhoL[c] = rl;
-            s_rhoR[c] = rr;
-            s_esc[c] = __expf(G - rr);
+        if (grp == 3 && th == 1) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const float G = s_esc[cp + e];
+                const float rl = fb ? 0.f : 0.5f * G;
+                const float rr = fb ? G : 0.5f * G;
+                s_rhoL[cp + e] = rl;
+                s_rhoR[cp + e] = rr;
+                s_esc[cp + e] = __expf(G - rr);
+            }
         }
 
         // ---- A2: per-token norms of the conv outputs (4 threads per row) and beta.
@@ -316,7 +459,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             ss += __shfl_xor_sync(0xffffffffu, ss, 2);
             if (part == 0) (R < C ? s_rk : s_rq)[R & (C - 1)] = rsqrtf(ss + p.l2_eps);
             if (tid < C)
-                s_beta[tid] = tid < n ? sigmoidf_(io.beta_logit[((size_t)(b * T + t0 + tid)) * H + h]) : 0.f;
+                s_beta[tid] = tid < n ? sigmoidf_(blog) : 0.f;
         }
         __syncthreads();
 
@@ -437,10 +580,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             tc::commit(s_bar);
         }
 
-        // ---- C1: Diag(beta) A' to shared memory, D0 -> [I; P] in TMEM
-        //      (row qrow, columns [16 grp, 16 grp + 16)).
+        // ---- C1: N = Diag(beta) A' to shared memory as N^T (row b holds
+        //      column b of N; 64-row SW128 layout), D0 -> [I; P] in TMEM (row
+        //      qrow, columns [16 grp, 16 grp + 16)).
         {
-            float* sM = reinterpret_cast<float*>(sm + OFF_R);   // [64][64], R is no longer needed
             const bool isA = qrow < C;
             const int r = isA ? qrow : qrow - C;
             const float br = s_beta[r];
@@ -451,14 +594,11 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 tc::ld8(tc::taddr(tm, warp, TM_D0 + i0), v);
                 tc::wait_ld();
                 if (isA) {
-                    float m[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        m[i] = (i0 + i) < r ? br * __uint_as_float(v[i]) : 0.f;
+                        at<float>(sm, OFF_R + tc::sw128(i0 + i, r, C)) = (i0 + i) < r ? br * __uint_as_float(v[i]) : 0.f;
                         v[i] = (i0 + i) == r ? tc::f2tf32(1.0f) : 0u;
                     }
-                    *reinterpret_cast<float4*>(sM + r * C + i0) = make_float4(m[0], m[1], m[2], m[3]);
-                    *reinterpret_cast<float4*>(sM + r * C + i0 + 4) = make_float4(m[4], m[5], m[6], m[7]);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
@@ -470,69 +610,126 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         tc::wait_st();
         sync_tc();
 
-        // ---- C2: Minv = (I + N)^{-1}, N = Diag(beta) A' (strictly lower), by
-        //      16 x 16 blocks: diagonal blocks by forward substitution, then
-        //      Minv[I][J] = -Minv[I][I] sum_{J<=K<I} N[I][K] Minv[K][J] level by
-        //      level (I - J = 1, 2, 3).  fp32 in shared memory, then the
-        //      N=64 x K=64 tf32 operand Minv^T.
+        // ---- C2: Minv = (I + N)^{-1} (N strictly lower) by 16 x 16 blocks.
+        //      Pass 1: forward substitution with the diagonal block I + N_II
+        //      on the right-hand sides [I | N_I0 .. N_I(I-1)], giving Minv_II
+        //      and E_IK = Minv_II N_IK.  Passes 2..4, level by level
+        //      (I - J = 1, 2, 3): Minv_IJ = -sum_{J <= K < I} E_IK Minv_KJ, one
+        //      warp per block.
+        //      Minv is kept transposed in the SW128 layout of the MMA_T operand
+        //      (row j holds column j of Minv), fp32 until the final rounding.
         {
-            const float* sN = reinterpret_cast<const float*>(sm + OFF_R);    // [64][64]
-            float* sMi = reinterpret_cast<float*>(sm + OFF_R + 16384);       // [64][64]
-            float* sTmp = reinterpret_cast<float*>(sm + OFF_MT);             // [3][16][16]
-            if (tid < C) {
-                const int I = tid >> 4, jj = tid & 15, j = I * 16 + jj;
-                const float* nb = sN + I * 16 * C + I * 16;
+            auto NT = [&](int row, int k) { return OFF_R + tc::sw128(row, k, C); };    // N^T
+            auto MT = [&](int row, int k) { return OFF_MT + tc::sw128(row, k, C); };   // Minv^T
+            // E_IK column-major (column stride 24 floats, pair stride 384 floats);
+            // (I, K) pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2): index I (I - 1) / 2 + K.
+            const uint32_t OFF_E = OFF_R + 16384;
+            auto EC = [&](int pr, int col, int row) { return OFF_E + (uint32_t)(pr * 384 + col * 24 + row) * 4; };
+            if (tid < 160) {
+                // block row I takes threads [8 I (I + 1), 8 (I + 1) (I + 2)): column u of [I | N_I*]
+                const int I = tid < 16 ? 0 : (tid < 48 ? 1 : (tid < 96 ? 2 : 3));
+                const int u = tid - 8 * I * (I + 1);
+                const int K = (u >> 4) - 1, cc = u & 15;
                 float x[16];
+                if (K < 0) {
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    float a0 = 0.f, a1 = 0.f;
+                    for (int rr = 0; rr < 16; ++rr) x[rr] = rr == cc ? 1.0f : 0.0f;
+                } else {
 #pragma unroll
-                    for (int i = 0; i < rr; ++i) {
-                        if (i & 1) a1 = fmaf(nb[rr * C + i], x[i], a1);
-                        else a0 = fmaf(nb[rr * C + i], x[i], a0);
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 v = at<float4>(sm, NT(K * 16 + cc, I * 16 + q * 4));   // N[16I + 4q + t][16K + cc]
+                        x[4 * q] = v.x; x[4 * q + 1] = v.y; x[4 * q + 2] = v.z; x[4 * q + 3] = v.w;
                     }
-                    x[rr] = (rr == jj ? 1.0f : 0.0f) - (a0 + a1);
                 }
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) sMi[(I * 16 + rr) * C + j] = x[rr];
+                for (int i = 0; i < 15; ++i) {
+#pragma unroll
+                    for (int q = (i + 1) >> 2; q < 4; ++q) {
+                        const float4 v = at<float4>(sm, NT(I * 16 + i, I * 16 + q * 4));   // N[16I + 4q + t][16I + i]
+                        const float nv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            if (4 * q + t > i) x[4 * q + t] = fmaf(-nv[t], x[i], x[4 * q + t]);
+                    }
+                }
+                if (K < 0) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        at<float4>(sm, MT(I * 16 + cc, I * 16 + q * 4)) =
+                            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        at<float4>(sm, EC((I * (I - 1)) / 2 + K, cc, q * 4)) =
+                            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                }
+            } else {
+                // zero the blocks above the diagonal of Minv (K block < row block of Minv^T)
+                for (int it = tid - 160; it < 384; it += kThreads - 160) {
+                    const int pr = it >> 6, rr = (it >> 2) & 15, q = it & 3;
+                    const int J = pr < 1 ? 1 : (pr < 3 ? 2 : 3);
+                    const int I = pr - (J * (J - 1)) / 2;
+                    at<float4>(sm, MT(J * 16 + rr, I * 16 + q * 4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
             __syncthreads();
-#pragma unroll 1
+            // Levels: warp J < 4 - lev computes the 16 x 16 block Minv_{J+lev, J}
+            // with warp-level m16n8k8 tf32 MMAs, each product split into
+            // hi + lo tf32 parts (hi*hi + hi*lo + lo*hi) for fp32-level accuracy.
+#pragma unroll
             for (int lev = 1; lev < 4; ++lev) {
-                const int nblk = 4 - lev;
-                // tmp[blk] = sum_{K=J}^{I-1} N[I][K] Minv[K][J], I = J + lev
-                for (int e = tid; e < nblk * 256; e += kThreads) {
-                    const int J = e >> 8, row = (e >> 4) & 15, col = e & 15, I = J + lev;
-                    const float* nrow = sN + (I * 16 + row) * C;
-                    float acc = 0.f;
-#pragma unroll 1
-                    for (int K = J; K < I; ++K) {
+                if (warp < 4 - lev) {
+                    const int J = warp, I = J + lev, g = lane >> 2, t4 = lane & 3;
+                    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                        for (int m = 0; m < 16; ++m)
-                            acc = fmaf(nrow[K * 16 + m], sMi[(K * 16 + m) * C + J * 16 + col], acc);
+                    for (int kk = 0; kk < lev; ++kk) {
+                        const int K = J + kk, pr = (I * (I - 1)) / 2 + K;
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks) {
+                            const int m0 = ks * 8;
+                            // A = E_IK rows (g, g + 8), columns (m0 + t4, m0 + t4 + 4)
+                            const float av[4] = {at<float>(sm, EC(pr, m0 + t4, g)), at<float>(sm, EC(pr, m0 + t4, g + 8)),
+                                                 at<float>(sm, EC(pr, m0 + t4 + 4, g)), at<float>(sm, EC(pr, m0 + t4 + 4, g + 8))};
+                            uint32_t ah[4], al[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                ah[i] = tc::f2tf32(av[i]);
+                                al[i] = tc::f2tf32(av[i] - __uint_as_float(ah[i]));
+                            }
+#pragma unroll
+                            for (int nt = 0; nt < 2; ++nt) {
+                                // B = Minv_KJ rows (m0 + t4, m0 + t4 + 4), column 8 nt + g
+                                const float b0 = at<float>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4));
+                                const float b1 = at<float>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4 + 4));
+                                const uint32_t bh0 = tc::f2tf32(b0), bh1 = tc::f2tf32(b1);
+                                const uint32_t bl0 = tc::f2tf32(b0 - __uint_as_float(bh0));
+                                const uint32_t bl1 = tc::f2tf32(b1 - __uint_as_float(bh1));
+                                mma_tf32_16x8x8(d[nt], ah, bh0, bh1);
+                                mma_tf32_16x8x8(d[nt], ah, bl0, bl1);
+                                mma_tf32_16x8x8(d[nt], al, bh0, bh1);
+                            }
+                        }
                     }
-                    sTmp[e] = acc;
-                }
-                __syncthreads();
-                for (int e = tid; e < nblk * 256; e += kThreads) {
-                    const int J = e >> 8, row = (e >> 4) & 15, col = e & 15, I = J + lev;
-                    const float* mrow = sMi + (I * 16 + row) * C + I * 16;
-                    float acc = 0.f;
+                    // D rows (g, g + 8), columns (8 nt + 2 t4, + 1) -> Minv^T rows 16 J + column
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) acc = fmaf(mrow[m], sTmp[(J << 8) + m * 16 + col], acc);
-                    sMi[(I * 16 + row) * C + J * 16 + col] = -acc;
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int cA = J * 16 + nt * 8 + 2 * t4;
+                        at<float>(sm, MT(cA, I * 16 + g)) = -d[nt][0];
+                        at<float>(sm, MT(cA + 1, I * 16 + g)) = -d[nt][1];
+                        at<float>(sm, MT(cA, I * 16 + g + 8)) = -d[nt][2];
+                        at<float>(sm, MT(cA + 1, I * 16 + g + 8)) = -d[nt][3];
+                    }
                 }
                 __syncthreads();
             }
-            // Minv^T operand: row j holds Minv[.][j]; zero above the diagonal.
+            // tf32 rounding of the operand in place.
             for (int e = tid; e < C * C / 4; e += kThreads) {
-                const int j = e >> 4, i = (e & 15) * 4;
-                uint4 u;
-                u.x = (i + 0) >= j ? tc::f2tf32(sMi[(i + 0) * C + j]) : 0u;
-                u.y = (i + 1) >= j ? tc::f2tf32(sMi[(i + 1) * C + j]) : 0u;
-                u.z = (i + 2) >= j ? tc::f2tf32(sMi[(i + 2) * C + j]) : 0u;
-                u.w = (i + 3) >= j ? tc::f2tf32(sMi[(i + 3) * C + j]) : 0u;
-                at<uint4>(sm, OFF_MT + tc::sw128(j, i, C)) = u;
+                uint4 u = at<uint4>(sm, OFF_MT + e * 16);
+                u.x = tc::f2tf32(__uint_as_float(u.x));
+                u.y = tc::f2tf32(__uint_as_float(u.y));
+                u.z = tc::f2tf32(__uint_as_float(u.z));
+                u.w = tc::f2tf32(__uint_as_float(u.w));
+                at<uint4>(sm, OFF_MT + e * 16) = u;
             }
         }
         publish();
@@ -713,9 +910,22 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             *reinterpret_cast<float4*>(dst + j) =
                 make_float4(esc_prev * __uint_as_float(s[j]), esc_prev * __uint_as_float(s[j + 1]),
                             esc_prev * __uint_as_float(s[j + 2]), esc_prev * __uint_as_float(s[j + 3]));
-        if (grp < 3) {
+        // Final window: the last three inputs of the sequence (older taps from
+        // the initial window when T < 3).
+        if (grp < 3 && th == 0) {
+            const uint16_t* x = grp == 0 ? io.q : (grp == 1 ? io.k : io.v);
 #pragma unroll
-            for (int j = 0; j < 3; ++j) win[j * HD3 + gch] = wv[j];
+            for (int j = 0; j < 3; ++j) {
+                const int t = T - 3 + j;
+                float2 w;
+                if (t >= 0) {
+                    const uint32_t u = *reinterpret_cast<const uint32_t*>(x + (((size_t)(b * T + t)) * H + h) * D + cp);
+                    w = make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+                } else {
+                    w = *reinterpret_cast<const float2*>(s_win0 + (grp * 3 + j + T) * D + cp);
+                }
+                *reinterpret_cast<float2*>(win + j * HD3 + gcp) = w;
+            }
         }
     }
     sync_tc();
