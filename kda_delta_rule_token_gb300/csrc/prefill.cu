@@ -65,6 +65,9 @@ constexpr uint32_t OFF_WIN = OFF_SMALL + 4096;   // conv window for the next chu
 constexpr uint32_t OFF_WIN0 = OFF_WIN + 4608;    // the initial conv window, [3][3][128] fp32
 constexpr uint32_t kSmemBytes = OFF_WIN0 + 4608;
 constexpr uint32_t STG_Q = OFF_ST, STG_K = OFF_ST + 16384, STG_Z = OFF_ST + 32768, STG_V = OFF_MT;
+// Gate tile of the chunk, then its output tile: four 64-row x 32-channel SW128
+// boxes in the Q_g halves of the L operand (free once MMA1 has read them).
+constexpr uint32_t OFF_OG = OFF_L + 8192;
 constexpr uint32_t kStageBytes = 3 * C * D * 2 + C * D * 4;   // 80 KiB per chunk
 
 // TMEM column map (512 columns allocated).
@@ -193,7 +196,15 @@ __device__ __forceinline__ void publish() {
 
 struct Maps {
     CUtensorMap q, k, v, z;   // 4-D (d, H, T, B) boxes of (128, 1, 64, 1)
+    CUtensorMap g, o;         // 4-D (d, H, T, B) boxes of (32, 1, 64, 1), 128-byte swizzle
 };
+
+// Issuing threads.  Issuing a group of MMAs stalls the issuing warp for
+// about the group's execution time, so MMA1 (under the inverse) and MMA_T
+// (under the X epilogue) come from warp 15 and the staging copies from warp
+// 14, warps with little work in the phases that follow; MMA0, MMA2 and MMA3
+// come from thread 0 (warp 0 has no rows in the output epilogue).
+constexpr int kIssuerB = 480, kStager = 448;
 
 // 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and takes column group
 // w / 4 of every TMEM pass; in the thread-per-channel passes the same thread
@@ -213,7 +224,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     float* s_win0 = reinterpret_cast<float*>(sm + OFF_WIN0);      // [3][3][128]
     uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_gtot + 128);
     uint64_t* s_tbar = s_bar + 1;                                 // input tiles landed
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 2);
+    uint64_t* s_gbar = s_bar + 2;                                 // gate tile landed
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 3);
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -232,15 +244,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     // issued once MMA1 has read it; v lands in the Minv^T region and may be
     // issued once MMA_T has read it.  One barrier phase covers all four.
     auto stage_qkz = [&](int ci) {
-        if (tid == 0) {
+        if (tid == kStager) {
             ptx::mbar_arrive_expect_tx(s_tbar, kStageBytes);
             ptx::tma_load_4d(sm + STG_Q, &maps.q, 0, h, ci * C, b, s_tbar);
             ptx::tma_load_4d(sm + STG_K, &maps.k, 0, h, ci * C, b, s_tbar);
             ptx::tma_load_4d(sm + STG_Z, &maps.z, 0, h, ci * C, b, s_tbar);
         }
-        const int r = tid >> 3;   // and ask L2 for the chunk's gate rows
-        if (ci * C + r < T)
-            ptx::prefetch_l2(io.gate_logit + (((size_t)(b * T + ci * C + r)) * H + h) * D + (tid & 7) * 16);
     };
     auto stage_v = [&](int ci) {
         if (tid == 0) ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, ci * C, b, s_tbar);
@@ -248,6 +257,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     if (tid == 0) {
         ptx::mbar_init(s_bar, 1);
         ptx::mbar_init(s_tbar, 1);
+        ptx::mbar_init(s_gbar, 1);
         ptx::fence_mbar_init();
         *s_dead = 0;
     }
@@ -255,6 +265,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     const uint32_t tm = *s_tmem;
     Waiter wt{s_bar, s_dead, err, 0u};
     Waiter wtma{s_tbar, s_dead, err, 0u};
+    Waiter wgate{s_gbar, s_dead, err, 0u};
     stage_qkz(0);
     stage_v(0);
 
@@ -314,8 +325,6 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     for (int ci = 0; ci < nchunks; ++ci) {
         const int t0 = ci * C;
         const int n = min(C, T - t0);
-        const size_t row0 = ((size_t)(b * T + t0) * H + h) * D;   // token t0, channel 0
-        const size_t tstride = HD;                                   // elements between tokens
 
         // ---- A1: conv + SiLU per channel over the chunk (from the staged
         //      tiles); decay and its cumulative sum.  Loads of token group
@@ -568,7 +577,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         if (!fb) wt.wait();   // MMA0
 
         // ---- MMA1: D1 = L (Diag(e^rho_L) S0) = [K_g S0; Q_g S0] (runs under the inverse).
-        if (tid == 0) {
+        if (tid == kIssuerB) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
 #pragma unroll 1
             for (int ks = 0; ks < D / 8; ++ks) {
@@ -735,9 +744,15 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         publish();
         wt.wait();   // MMA1
         if (ci + 1 < nchunks) stage_qkz(ci + 1);   // the S^T region is free now
+        if (tid == kStager) {                        // this chunk's gate tile into the Q_g half of L
+            ptx::mbar_arrive_expect_tx(s_gbar, C * D * 4);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                ptx::tma_load_4d(sm + OFF_OG + j * 16384, &maps.g, j * 32, h, t0, b, s_gbar);
+        }
 
         // ---- MMA_T: [Minv; P Minv] = [I; P] Minv (runs under the X epilogue).
-        if (tid == 0) {
+        if (tid == kIssuerB) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll 1
             for (int ks = 0; ks < C / 8; ++ks) {
@@ -809,8 +824,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         wt.wait();
 
         // ---- F: U -> operand of MMA3 (rows 0..63); sum of squares of O_pre
-        //      (rows 64..127, gate logits loaded alongside).
-        float4 gate4[8];
+        //      (rows 64..127).
         if ((warp & 3) < 2) {
             const int r = qrow;
             const uint32_t kr = (uint32_t)((r >> 5) * 128 * 128 + (r & 3) * 4);
@@ -830,10 +844,6 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
         } else {
             const int r = qrow - C;
-            const size_t orow = row0 + (size_t)(r < n ? r : 0) * tstride + grp * 32;
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-                gate4[q4] = *reinterpret_cast<const float4*>(io.gate_logit + orow + q4 * 4);
             float ss = 0.f;
 #pragma unroll 1
             for (int g8 = 0; g8 < 4; ++g8) {
@@ -859,23 +869,25 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             tc::commit(s_bar);
         }
         // O_pre -> RMSNorm, gamma, sigmoid gate -> o (D1 rows 64..127 are not
-        // touched by MMA3).
+        // touched by MMA3), written over the gate tile in shared memory and
+        // stored by TMA (rows past T are clipped by the copy).
         if ((warp & 3) >= 2) {
-            // tcgen05.ld is warp-collective: every lane loads, only rows r < n store.
             const int r = qrow - C;
-            const bool live = r < n;
             const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
                                          (1.0f / D) + p.rms_eps);
-            const size_t orow = row0 + (size_t)(live ? r : 0) * tstride + grp * 32;
             const float* gm = p.gamma + h * D + grp * 32;
+            const uint32_t gbase = OFF_OG + grp * 16384 + r * 128;   // row r of box grp (SW128)
+            wgate.wait();
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 uint32_t v[8];
                 tc::ld8(tc::taddr(tm, warp, TM_D1 + grp * 32 + g8 * 8), v);
                 const float4 ma = *reinterpret_cast<const float4*>(gm + g8 * 8);
                 const float4 mb = *reinterpret_cast<const float4*>(gm + g8 * 8 + 4);
+                const uint32_t oa_at = gbase + (((2 * g8) ^ (r & 7)) << 4);
+                const uint32_t ob_at = gbase + (((2 * g8 + 1) ^ (r & 7)) << 4);
+                const float4 ga = at<float4>(sm, oa_at), gb = at<float4>(sm, ob_at);
                 tc::wait_ld();
-                const float4 ga = gate4[2 * g8], gb = gate4[2 * g8 + 1];
                 float4 oa, ob;
                 oa.x = ma.x * __uint_as_float(v[0]) * inv * sigmoidf_(ga.x);
                 oa.y = ma.y * __uint_as_float(v[1]) * inv * sigmoidf_(ga.y);
@@ -885,13 +897,20 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 ob.y = mb.y * __uint_as_float(v[5]) * inv * sigmoidf_(gb.y);
                 ob.z = mb.z * __uint_as_float(v[6]) * inv * sigmoidf_(gb.z);
                 ob.w = mb.w * __uint_as_float(v[7]) * inv * sigmoidf_(gb.w);
-                if (live) {
-                    *reinterpret_cast<float4*>(io.o + orow + g8 * 8) = oa;
-                    *reinterpret_cast<float4*>(io.o + orow + g8 * 8 + 4) = ob;
-                }
+                at<float4>(sm, oa_at) = oa;
+                at<float4>(sm, ob_at) = ob;
             }
+            ptx::fence_proxy_async_smem();
+        }
+        __syncthreads();
+        if (tid == kStager) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ptx::tma_store_4d(&maps.o, j * 32, h, t0, b, sm + OFF_OG + j * 16384);
+            ptx::bulk_commit();
         }
         wt.wait();
+        // the next chunk's conv phase overwrites the tile: its reads must be done
+        if (tid == kStager) ptx::bulk_wait_read_all();
 
         // S_new = e^{G_last - rho_R} M: the scale is carried in a register and
         // applied by the next chunk's state pass (or the final write-back).
@@ -928,6 +947,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
         }
     }
+    if (tid == kStager) ptx::bulk_wait_all();
     sync_tc();
     if (warp == 0) tc::dealloc(tm, 512);
 }
@@ -947,18 +967,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [B][T][H][d] tensor seen as 4-D (d, H, T, B); boxes of one head x 64 tokens.
+// [B][T][H][d] tensor seen as 4-D (d, H, T, B); boxes of `bd` channels of one
+// head x 64 tokens.
 bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize, int H, int T,
-              int B) {
+              int B, int bd = D, CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)D * esize, (cuuint64_t)H * D * esize,
                                    (cuuint64_t)T * H * D * esize};
-    const cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)C, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)bd, 1, (cuuint32_t)C, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return fn(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -980,7 +1001,11 @@ cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const Devi
     if (!make_map(&maps.q, io.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, io.B) ||
         !make_map(&maps.k, io.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, io.B) ||
         !make_map(&maps.v, io.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, io.B) ||
-        !make_map(&maps.z, io.z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, io.B))
+        !make_map(&maps.z, io.z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, io.B) ||
+        !make_map(&maps.g, io.gate_logit, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, io.B, 32,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&maps.o, io.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, io.B, 32,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     kda_prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p, io, err_word, maps);
     count_launches(1);

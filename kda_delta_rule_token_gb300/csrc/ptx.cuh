@@ -118,6 +118,14 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0,
         : "memory");
 }
 
+// Tiled TMA store of a 4-D box from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_4d(const void* tmap, int c0, int c1, int c2, int c3, const void* src) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+        ::"l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+        : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (cp.async, L2 only); when !ok
 // the destination is zero-filled and nothing is read.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool ok) {
