@@ -61,9 +61,8 @@ constexpr uint32_t OFF_R = OFF_L + 65536;     // R operand 64 x 128; staging of 
 constexpr uint32_t OFF_V = OFF_R + 32768;     // v conv output, fp32 64 x 128 (SW128 layout)
 constexpr uint32_t OFF_MT = OFF_V + 32768;    // Minv^T operand N=64 x K=64; stages the v tile
 constexpr uint32_t OFF_SMALL = OFF_MT + 16384;
-constexpr uint32_t OFF_WIN = OFF_SMALL + 4096;   // conv window for the next chunk's first half, [3][3][128] fp32
-constexpr uint32_t OFF_WIN0 = OFF_WIN + 4608;    // the initial conv window, [3][3][128] fp32
-constexpr uint32_t kSmemBytes = OFF_WIN0 + 4608;
+constexpr uint32_t OFF_WIN = OFF_SMALL + 4096;   // conv window of a chunk's first half, 2 x [3][3][128] fp32
+constexpr uint32_t kSmemBytes = OFF_WIN + 2 * 4608;
 constexpr uint32_t STG_Q = OFF_ST, STG_K = OFF_ST + 16384, STG_Z = OFF_ST + 32768, STG_V = OFF_MT;
 // Gate tile of the chunk, then its output tile: four 64-row x 32-channel SW128
 // boxes in the Q_g halves of the L operand (free once MMA1 has read them).
@@ -215,14 +214,11 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     float* s_beta = reinterpret_cast<float*>(sm + OFF_SMALL);   // [64]
     float* s_rq = s_beta + 64;                                    // [64]
     float* s_rk = s_rq + 64;                                      // [64]
-    float* s_rhoL = s_rk + 64;                                    // [128]
-    float* s_rhoR = s_rhoL + 128;                                 // [128]
-    float* s_esc = s_rhoR + 128;                                  // [128] e^{G_last - rho_R}
-    float* s_part = s_esc + 128;                                  // [4][64] RMS partial sums
-    float* s_gtot = s_part + 256;                                 // [128] decay total of tokens 0..31
-    float* s_win = reinterpret_cast<float*>(sm + OFF_WIN);        // [3][3][128]
-    float* s_win0 = reinterpret_cast<float*>(sm + OFF_WIN0);      // [3][3][128]
-    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_gtot + 128);
+    float* s_part = s_rk + 64;                                    // [4][64] RMS partial sums
+    float* s_gh0 = s_part + 256;                                  // [128] decay sum over tokens 0..31
+    float* s_gh1 = s_gh0 + 128;                                   // [128] decay sum over tokens 32..63
+    float* s_win = reinterpret_cast<float*>(sm + OFF_WIN);        // [2][3][3][128], by chunk parity
+    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_gh1 + 128);
     uint64_t* s_tbar = s_bar + 1;                                 // input tiles landed
     uint64_t* s_gbar = s_bar + 2;                                 // gate tile landed
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 3);
@@ -297,11 +293,9 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         W0 = pk(a.x, bq.x); W1 = pk(a.y, bq.y); W2 = pk(a.z, bq.z); W3 = pk(a.w, bq.w);
         if (th == 0) {
 #pragma unroll
-            for (int j = 0; j < 3; ++j) {
-                const float2 w = *reinterpret_cast<const float2*>(win + j * HD3 + gcp);
-                *reinterpret_cast<float2*>(s_win + (grp * 3 + j) * D + cp) = w;
-                *reinterpret_cast<float2*>(s_win0 + (grp * 3 + j) * D + cp) = w;
-            }
+            for (int j = 0; j < 3; ++j)
+                *reinterpret_cast<float2*>(s_win + (grp * 3 + j) * D + cp) =
+                    *reinterpret_cast<const float2*>(win + j * HD3 + gcp);
         }
     } else {
         nEA = pk(-expf(p.A_log[h * D + cp]), -expf(p.A_log[h * D + cp + 1]));
@@ -312,8 +306,6 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     const uint32_t kpL = (uint32_t)((cp >> 5) * 128 * 128 + (cp & 3) * 4);
     const uint32_t kpR = (uint32_t)((cp >> 5) * 64 * 128 + (cp & 3) * 4);
     const int pch = (cp >> 2) & 7;
-    f32x2 keep0 = 0, keep1 = 0, keep2 = 0;   // last three inputs of a second-half conv thread
-    f32x2 g1sum = 0;                         // decay total of a second-half decay thread
 
     // Swizzled addressing of channel c as the K index of the L (128-row) and
     // R / V (64-row) operand layouts.
@@ -339,7 +331,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             auto unpk_bf2 = [](uint32_t u) { return pk(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)); };
             f32x2 M3, M2, M1;   // window, oldest first
             if (th == 0) {
-                const float* w = s_win + grp * 3 * D + cp;
+                const float* w = s_win + ((ci & 1) * 9 + grp * 3) * D + cp;
                 M3 = pk(w[0], w[1]); M2 = pk(w[D], w[D + 1]); M1 = pk(w[2 * D], w[2 * D + 1]);
             } else {
                 M3 = unpk_bf2(src[29 * (D / 2)]); M2 = unpk_bf2(src[30 * (D / 2)]); M1 = unpk_bf2(src[31 * (D / 2)]);
@@ -386,7 +378,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                     at<f32x2>(sm, dst + r * 128 + ((pch ^ (r & 7)) << 4)) = y[i];
                 }
             }
-            keep0 = M3; keep1 = M2; keep2 = M1;
+            if (th == 1) {   // the next chunk's first half starts from this window
+                float* w = s_win + (((ci + 1) & 1) * 9 + grp * 3) * D + cp;
+                upk(M3, w[0], w[1]);
+                upk(M2, w[D], w[D + 1]);
+                upk(M1, w[2 * D], w[2 * D + 1]);
+            }
         } else {
             const f32x2* src = reinterpret_cast<const f32x2*>(sm + STG_Z) + (cp >> 1);
             const int r0 = th * 32;
@@ -416,44 +413,9 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                     at<f32x2>(sm, OFF_R + kpR + r * 128 + ((pch ^ (r & 7)) << 4)) = gg[i];
                 }
             }
-            if (th == 0) *reinterpret_cast<f32x2*>(s_gtot + cp) = G;
-            else g1sum = G;
+            *reinterpret_cast<f32x2*>((th == 0 ? s_gh0 : s_gh1) + cp) = G;
         }
         __syncthreads();
-
-        // ---- A1b: second-half decay threads add the first half's total; the
-        //      second-half conv threads hand the next chunk its window.
-        bool big = false;
-        if (grp == 3 && th == 1) {
-            const f32x2 off = *reinterpret_cast<const f32x2*>(s_gtot + cp);
-#pragma unroll 4
-            for (int r = 32; r < C; ++r) {
-                const uint32_t o = OFF_R + kpR + r * 128 + ((pch ^ (r & 7)) << 4);
-                at<f32x2>(sm, o) = add2(at<f32x2>(sm, o), off);
-            }
-            float g0, g1;
-            upk(add2(off, g1sum), g0, g1);   // G_last
-            big = (-g0 > kMaxSpan) || (-g1 > kMaxSpan);
-            s_esc[cp] = g0;                   // G_last for now
-            s_esc[cp + 1] = g1;
-        } else if (grp < 3 && th == 1) {
-            float* w = s_win + grp * 3 * D + cp;
-            upk(keep0, w[0], w[1]);
-            upk(keep1, w[D], w[D + 1]);
-            upk(keep2, w[2 * D], w[2 * D + 1]);
-        }
-        const bool fb = __syncthreads_or(big) != 0;
-        if (grp == 3 && th == 1) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float G = s_esc[cp + e];
-                const float rl = fb ? 0.f : 0.5f * G;
-                const float rr = fb ? G : 0.5f * G;
-                s_rhoL[cp + e] = rl;
-                s_rhoR[cp + e] = rr;
-                s_esc[cp + e] = __expf(G - rr);
-            }
-        }
 
         // ---- A2: per-token norms of the conv outputs (4 threads per row) and beta.
         {
@@ -470,7 +432,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             if (tid < C)
                 s_beta[tid] = tid < n ? sigmoidf_(blog) : 0.f;
         }
-        __syncthreads();
+        // G_last per channel; the exact fallback when a chunk decays by more than kMaxSpan.
+        const bool fb = __syncthreads_or(tid < D && -(s_gh0[tid] + s_gh1[tid]) > kMaxSpan) != 0;
 
         // ---- A2b (rare): exact [A'; P] when the chunk decays by more than kMaxSpan.
         if (fb) {
@@ -489,9 +452,9 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
 #pragma unroll 4
                         for (int ch = 0; ch < D; ++ch) {
                             const float a = at<float>(sm, OFF_L + tc::sw128(R, ch, 128));
-                            const float gr = at<float>(sm, OFF_R + tc::sw128(r, ch, C));
+                            const float gr = at<float>(sm, OFF_R + tc::sw128(r, ch, C)) + (r >= 32 ? s_gh0[ch] : 0.f);
                             const float kk = at<float>(sm, OFF_L + tc::sw128(col, ch, 128));
-                            const float gi = at<float>(sm, OFF_R + tc::sw128(col, ch, C));
+                            const float gi = at<float>(sm, OFF_R + tc::sw128(col, ch, C)) + (col >= 32 ? s_gh0[ch] : 0.f);
                             acc = fmaf(a * kk, expf(gr - gi), acc);
                         }
                     }
@@ -506,7 +469,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- A3: L, R (shared memory, in place over the staging) and R^T
         //      (TMEM), channel c, tokens [16 grp, 16 grp + 16), 8 at a time.
         {
-            const float rl = s_rhoL[c], rr = s_rhoR[c];
+            // rho_L = rho_R = G_last / 2, or (0, G_last) on the fallback path
+            const float gl = s_gh0[c] + s_gh1[c];
+            const float rl = fb ? 0.f : 0.5f * gl, rr = fb ? gl : 0.5f * gl;
+            const float goff = grp >= 2 ? s_gh0[c] : 0.f;   // tokens 32..63 add the first half
 #pragma unroll 1
             for (int g8 = 0; g8 < 2; ++g8) {
                 uint32_t rt[8];
@@ -515,7 +481,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 for (int i = 0; i < 8; ++i) {
                     const int r = grp * 16 + g8 * 8 + i;
                     const uint32_t ro = (uint32_t)(r * 128 + ((cch ^ (r & 7)) << 4));
-                    g[i] = at<float>(sm, OFF_R + kcR + ro);
+                    g[i] = at<float>(sm, OFF_R + kcR + ro) + goff;
                     yk[i] = at<float>(sm, OFF_L + kcL + ro) * s_rk[r];
                     yq[i] = at<float>(sm, OFF_L + kcL + C * 128 + ro) * s_rq[r];
                 }
@@ -551,8 +517,9 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- D: state pass: S^T operand scaled by e^{rho_L}, master scaled by
         //      e^{rho_R} (both also by the previous chunk's pending scale).
         {
-            const float eL = esc_prev * __expf(s_rhoL[qrow]);
-            const float eR = esc_prev * __expf(s_rhoR[qrow]);
+            const float gl = s_gh0[qrow] + s_gh1[qrow];
+            const float eL = esc_prev * (fb ? 1.0f : __expf(0.5f * gl));
+            const float eR = esc_prev * __expf(fb ? gl : 0.5f * gl);
             // S^T operand element (row j, K = qrow): K block and chunk are fixed per thread.
             const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
             const int kch = (qrow >> 2) & 7;
@@ -914,7 +881,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
 
         // S_new = e^{G_last - rho_R} M: the scale is carried in a register and
         // applied by the next chunk's state pass (or the final write-back).
-        esc_prev = s_esc[qrow];
+        {
+            const float gl = s_gh0[qrow] + s_gh1[qrow];
+            esc_prev = __expf(fb ? 0.f : 0.5f * gl);   // e^{G_last - rho_R}
+        }
         sync_tc();
     }
 
@@ -940,8 +910,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 if (t >= 0) {
                     const uint32_t u = *reinterpret_cast<const uint32_t*>(x + (((size_t)(b * T + t)) * H + h) * D + cp);
                     w = make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
-                } else {
-                    w = *reinterpret_cast<const float2*>(s_win0 + (grp * 3 + j + T) * D + cp);
+                } else {   // an older tap of the initial window (not yet overwritten: j + T > j)
+                    w = *reinterpret_cast<const float2*>(win + (j + T) * HD3 + gcp);
                 }
                 *reinterpret_cast<float2*>(win + j * HD3 + gcp) = w;
             }
