@@ -591,9 +591,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         //      on the right-hand sides [I | N_I0 .. N_I(I-1)], giving Minv_II
         //      and E_IK = Minv_II N_IK.  Passes 2..4, level by level
         //      (I - J = 1, 2, 3): Minv_IJ = -sum_{J <= K < I} E_IK Minv_KJ, one
-        //      warp per block.
-        //      Minv is kept transposed in the SW128 layout of the MMA_T operand
-        //      (row j holds column j of Minv), fp32 until the final rounding.
+        //      warp per block.  Minv is kept transposed and tf32-rounded in the
+        //      SW128 layout of the MMA_T operand (row j holds column j of Minv).
         {
             auto NT = [&](int row, int k) { return OFF_R + tc::sw128(row, k, C); };    // N^T
             auto MT = [&](int row, int k) { return OFF_MT + tc::sw128(row, k, C); };   // Minv^T
@@ -628,16 +627,11 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                             if (4 * q + t > i) x[4 * q + t] = fmaf(-nv[t], x[i], x[4 * q + t]);
                     }
                 }
-                if (K < 0) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        at<float4>(sm, MT(I * 16 + cc, I * 16 + q * 4)) =
-                            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        at<float4>(sm, EC((I * (I - 1)) / 2 + K, cc, q * 4)) =
-                            make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                for (int q = 0; q < 4; ++q) {   // tf32-rounded: operands of the level MMAs and of MMA_T
+                    const uint4 u = make_uint4(tc::f2tf32(x[4 * q]), tc::f2tf32(x[4 * q + 1]),
+                                               tc::f2tf32(x[4 * q + 2]), tc::f2tf32(x[4 * q + 3]));
+                    at<uint4>(sm, K < 0 ? MT(I * 16 + cc, I * 16 + q * 4) : EC((I * (I - 1)) / 2 + K, cc, q * 4)) = u;
                 }
             } else {
                 // zero the blocks above the diagonal of Minv (K block < row block of Minv^T)
@@ -650,8 +644,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             __syncthreads();
             // Levels: warp J < 4 - lev computes the 16 x 16 block Minv_{J+lev, J}
-            // with warp-level m16n8k8 tf32 MMAs, each product split into
-            // hi + lo tf32 parts (hi*hi + hi*lo + lo*hi) for fp32-level accuracy.
+            // with warp-level m16n8k8 tf32 MMAs (operands stored tf32-rounded;
+            // the result is rounded once more when stored).
 #pragma unroll
             for (int lev = 1; lev < 4; ++lev) {
                 if (warp < 4 - lev) {
@@ -664,48 +658,26 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                         for (int ks = 0; ks < 2; ++ks) {
                             const int m0 = ks * 8;
                             // A = E_IK rows (g, g + 8), columns (m0 + t4, m0 + t4 + 4)
-                            const float av[4] = {at<float>(sm, EC(pr, m0 + t4, g)), at<float>(sm, EC(pr, m0 + t4, g + 8)),
-                                                 at<float>(sm, EC(pr, m0 + t4 + 4, g)), at<float>(sm, EC(pr, m0 + t4 + 4, g + 8))};
-                            uint32_t ah[4], al[4];
+                            const uint32_t a[4] = {at<uint32_t>(sm, EC(pr, m0 + t4, g)), at<uint32_t>(sm, EC(pr, m0 + t4, g + 8)),
+                                                   at<uint32_t>(sm, EC(pr, m0 + t4 + 4, g)),
+                                                   at<uint32_t>(sm, EC(pr, m0 + t4 + 4, g + 8))};
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                ah[i] = tc::f2tf32(av[i]);
-                                al[i] = tc::f2tf32(av[i] - __uint_as_float(ah[i]));
-                            }
-#pragma unroll
-                            for (int nt = 0; nt < 2; ++nt) {
-                                // B = Minv_KJ rows (m0 + t4, m0 + t4 + 4), column 8 nt + g
-                                const float b0 = at<float>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4));
-                                const float b1 = at<float>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4 + 4));
-                                const uint32_t bh0 = tc::f2tf32(b0), bh1 = tc::f2tf32(b1);
-                                const uint32_t bl0 = tc::f2tf32(b0 - __uint_as_float(bh0));
-                                const uint32_t bl1 = tc::f2tf32(b1 - __uint_as_float(bh1));
-                                mma_tf32_16x8x8(d[nt], ah, bh0, bh1);
-                                mma_tf32_16x8x8(d[nt], ah, bl0, bl1);
-                                mma_tf32_16x8x8(d[nt], al, bh0, bh1);
-                            }
+                            for (int nt = 0; nt < 2; ++nt)   // B = Minv_KJ rows (m0 + t4, + 4), column 8 nt + g
+                                mma_tf32_16x8x8(d[nt], a, at<uint32_t>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4)),
+                                                at<uint32_t>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4 + 4)));
                         }
                     }
                     // D rows (g, g + 8), columns (8 nt + 2 t4, + 1) -> Minv^T rows 16 J + column
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt) {
                         const int cA = J * 16 + nt * 8 + 2 * t4;
-                        at<float>(sm, MT(cA, I * 16 + g)) = -d[nt][0];
-                        at<float>(sm, MT(cA + 1, I * 16 + g)) = -d[nt][1];
-                        at<float>(sm, MT(cA, I * 16 + g + 8)) = -d[nt][2];
-                        at<float>(sm, MT(cA + 1, I * 16 + g + 8)) = -d[nt][3];
+                        at<uint32_t>(sm, MT(cA, I * 16 + g)) = tc::f2tf32(-d[nt][0]);
+                        at<uint32_t>(sm, MT(cA + 1, I * 16 + g)) = tc::f2tf32(-d[nt][1]);
+                        at<uint32_t>(sm, MT(cA, I * 16 + g + 8)) = tc::f2tf32(-d[nt][2]);
+                        at<uint32_t>(sm, MT(cA + 1, I * 16 + g + 8)) = tc::f2tf32(-d[nt][3]);
                     }
                 }
-                __syncthreads();
-            }
-            // tf32 rounding of the operand in place.
-            for (int e = tid; e < C * C / 4; e += kThreads) {
-                uint4 u = at<uint4>(sm, OFF_MT + e * 16);
-                u.x = tc::f2tf32(__uint_as_float(u.x));
-                u.y = tc::f2tf32(__uint_as_float(u.y));
-                u.z = tc::f2tf32(__uint_as_float(u.z));
-                u.w = tc::f2tf32(__uint_as_float(u.w));
-                at<uint4>(sm, OFF_MT + e * 16) = u;
+                if (lev < 3) __syncthreads();
             }
         }
         publish();
