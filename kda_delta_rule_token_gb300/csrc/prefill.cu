@@ -180,6 +180,11 @@ struct Waiter {
     }
 };
 
+// Barrier over `count` threads (whole warps) with id `id` (0 is __syncthreads).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void sync_tc() {
     tc::fence_before();
     __syncthreads();
@@ -199,11 +204,12 @@ struct Maps {
 };
 
 // Issuing threads.  Issuing a group of MMAs stalls the issuing warp for
-// about the group's execution time, so MMA1 (under the inverse) and MMA_T
-// (under the X epilogue) come from warp 15 and the staging copies from warp
-// 14, warps with little work in the phases that follow; MMA0, MMA2 and MMA3
-// come from thread 0 (warp 0 has no rows in the output epilogue).
-constexpr int kIssuerB = 480, kStager = 448;
+// about the group's execution time, so MMA1 (under the inverse) comes from
+// warp 15, which has little work in C1; MMA_T from warp 15 as soon as it has
+// written the last inverse block; the staging copies and the output store
+// from warp 12 (it waits for MMA1 anyway); MMA0, MMA2 and MMA3 from thread 0
+// (warp 0 has no rows in the output epilogue).
+constexpr int kIssuerB = 480, kStager = 384;
 
 // 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and takes column group
 // w / 4 of every TMEM pass; in the thread-per-channel passes the same thread
@@ -221,7 +227,9 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_gh1 + 128);
     uint64_t* s_tbar = s_bar + 1;                                 // input tiles landed
     uint64_t* s_gbar = s_bar + 2;                                 // gate tile landed
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 3);
+    uint64_t* s_tbarT = s_bar + 3;                                // MMA_T done
+    uint64_t* s_bar1 = s_bar + 4;                                 // MMA1 done
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 5);
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -245,6 +253,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             ptx::tma_load_4d(sm + STG_Q, &maps.q, 0, h, ci * C, b, s_tbar);
             ptx::tma_load_4d(sm + STG_K, &maps.k, 0, h, ci * C, b, s_tbar);
             ptx::tma_load_4d(sm + STG_Z, &maps.z, 0, h, ci * C, b, s_tbar);
+            ptx::tma_prefetch_4d(&maps.v, 0, h, ci * C, b);   // v lands later; have it in L2
         }
     };
     auto stage_v = [&](int ci) {
@@ -254,6 +263,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         ptx::mbar_init(s_bar, 1);
         ptx::mbar_init(s_tbar, 1);
         ptx::mbar_init(s_gbar, 1);
+        ptx::mbar_init(s_tbarT, 1);
+        ptx::mbar_init(s_bar1, 1);
         ptx::fence_mbar_init();
         *s_dead = 0;
     }
@@ -262,6 +273,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     Waiter wt{s_bar, s_dead, err, 0u};
     Waiter wtma{s_tbar, s_dead, err, 0u};
     Waiter wgate{s_gbar, s_dead, err, 0u};
+    Waiter wtT{s_tbarT, s_dead, err, 0u};
+    Waiter wt1{s_bar1, s_dead, err, 0u};
     stage_qkz(0);
     stage_v(0);
 
@@ -417,17 +430,19 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         __syncthreads();
 
-        // ---- A2: per-token norms of the conv outputs (4 threads per row) and beta.
+        // ---- A2: per-token norms of the conv outputs (4 threads per row, one
+        //      per 32-channel block; the 8 lanes of a quarter warp take 8 rows of
+        //      one block, so their 16-byte loads hit 8 different bank groups) and beta.
         {
-            const int R = tid >> 2, part = tid & 3;   // L row: y_k rows 0..63, y_q rows 64..127
+            const int R = (tid & 7) + 8 * (tid >> 5), part = (tid >> 3) & 3;   // y_k rows 0..63, y_q rows 64..127
             float ss = 0.f;
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
                 const float4 v = at<float4>(sm, OFF_L + tc::sw128(R, part * 32 + j, 128));
                 ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
             }
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 16);
             if (part == 0) (R < C ? s_rk : s_rq)[R & (C - 1)] = rsqrtf(ss + p.l2_eps);
             if (tid < C)
                 s_beta[tid] = tid < n ? sigmoidf_(blog) : 0.f;
@@ -553,7 +568,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                            tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)),
                            tc::desc_sw128(ptx::smem_u32(sm + OFF_ST + kb * 16384 + kin * 32)), id, ks > 0);
             }
-            tc::commit(s_bar);
+            tc::commit(s_bar1);
         }
 
         // ---- C1: N = Diag(beta) A' to shared memory as N^T (row b holds
@@ -642,73 +657,82 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                     at<float4>(sm, MT(J * 16 + rr, I * 16 + q * 4)) = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
+            ptx::fence_proxy_async_smem();   // Minv^T blocks: smem operand of MMA_T
             __syncthreads();
-            // Levels: warp J < 4 - lev computes the 16 x 16 block Minv_{J+lev, J}
-            // with warp-level m16n8k8 tf32 MMAs (operands stored tf32-rounded;
-            // the result is rounded once more when stored).
+            // Levels, on warps 15, 14, 11 (blocks J = 0, 1, 2), which have no rows
+            // in the X epilogue running meanwhile: warp J computes the 16 x 16
+            // block Minv_{J+lev, J} with warp-level m16n8k8 tf32 MMAs (operands
+            // stored tf32-rounded; the result is rounded once more when stored).
+            const int J = warp == 15 ? 0 : (warp == 14 ? 1 : (warp == 11 ? 2 : -1));
+            if (J >= 0) {
 #pragma unroll
-            for (int lev = 1; lev < 4; ++lev) {
-                if (warp < 4 - lev) {
-                    const int J = warp, I = J + lev, g = lane >> 2, t4 = lane & 3;
-                    float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                for (int lev = 1; lev < 4; ++lev) {
+                    if (J < 4 - lev) {
+                        const int I = J + lev, g = lane >> 2, t4 = lane & 3;
+                        float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-                    for (int kk = 0; kk < lev; ++kk) {
-                        const int K = J + kk, pr = (I * (I - 1)) / 2 + K;
+                        for (int kk = 0; kk < lev; ++kk) {
+                            const int K = J + kk, pr = (I * (I - 1)) / 2 + K;
 #pragma unroll
-                        for (int ks = 0; ks < 2; ++ks) {
-                            const int m0 = ks * 8;
-                            // A = E_IK rows (g, g + 8), columns (m0 + t4, m0 + t4 + 4)
-                            const uint32_t a[4] = {at<uint32_t>(sm, EC(pr, m0 + t4, g)), at<uint32_t>(sm, EC(pr, m0 + t4, g + 8)),
-                                                   at<uint32_t>(sm, EC(pr, m0 + t4 + 4, g)),
-                                                   at<uint32_t>(sm, EC(pr, m0 + t4 + 4, g + 8))};
+                            for (int ks = 0; ks < 2; ++ks) {
+                                const int m0 = ks * 8;
+                                // A = E_IK rows (g, g + 8), columns (m0 + t4, m0 + t4 + 4)
+                                const uint32_t a[4] = {at<uint32_t>(sm, EC(pr, m0 + t4, g)),
+                                                       at<uint32_t>(sm, EC(pr, m0 + t4, g + 8)),
+                                                       at<uint32_t>(sm, EC(pr, m0 + t4 + 4, g)),
+                                                       at<uint32_t>(sm, EC(pr, m0 + t4 + 4, g + 8))};
 #pragma unroll
-                            for (int nt = 0; nt < 2; ++nt)   // B = Minv_KJ rows (m0 + t4, + 4), column 8 nt + g
-                                mma_tf32_16x8x8(d[nt], a, at<uint32_t>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4)),
-                                                at<uint32_t>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4 + 4)));
+                                for (int nt = 0; nt < 2; ++nt)   // B = Minv_KJ rows (m0 + t4, + 4), column 8 nt + g
+                                    mma_tf32_16x8x8(d[nt], a, at<uint32_t>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4)),
+                                                    at<uint32_t>(sm, MT(J * 16 + nt * 8 + g, K * 16 + m0 + t4 + 4)));
+                            }
+                        }
+                        // D rows (g, g + 8), columns (8 nt + 2 t4, + 1) -> Minv^T rows 16 J + column
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const int cA = J * 16 + nt * 8 + 2 * t4;
+                            at<uint32_t>(sm, MT(cA, I * 16 + g)) = tc::f2tf32(-d[nt][0]);
+                            at<uint32_t>(sm, MT(cA + 1, I * 16 + g)) = tc::f2tf32(-d[nt][1]);
+                            at<uint32_t>(sm, MT(cA, I * 16 + g + 8)) = tc::f2tf32(-d[nt][2]);
+                            at<uint32_t>(sm, MT(cA + 1, I * 16 + g + 8)) = tc::f2tf32(-d[nt][3]);
                         }
                     }
-                    // D rows (g, g + 8), columns (8 nt + 2 t4, + 1) -> Minv^T rows 16 J + column
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const int cA = J * 16 + nt * 8 + 2 * t4;
-                        at<uint32_t>(sm, MT(cA, I * 16 + g)) = tc::f2tf32(-d[nt][0]);
-                        at<uint32_t>(sm, MT(cA + 1, I * 16 + g)) = tc::f2tf32(-d[nt][1]);
-                        at<uint32_t>(sm, MT(cA, I * 16 + g + 8)) = tc::f2tf32(-d[nt][2]);
-                        at<uint32_t>(sm, MT(cA + 1, I * 16 + g + 8)) = tc::f2tf32(-d[nt][3]);
-                    }
+                    ptx::fence_proxy_async_smem();   // Minv^T is the smem operand of MMA_T
+                    if (lev < 3) named_barrier_sync(1, 96);
                 }
-                if (lev < 3) __syncthreads();
+                // ---- MMA_T: [Minv; P Minv] = [I; P] Minv, issued by the warp that
+                //      wrote the last block (runs under the rest of the X epilogue).
+                if (tid == kIssuerB) {
+                    tc::fence_after();
+                    constexpr uint32_t id = tc::idesc_tf32(128, 64);
+#pragma unroll 1
+                    for (int ks = 0; ks < C / 8; ++ks) {
+                        const int kb = ks >> 2, kin = ks & 3;
+                        tc::mma_ts(tm + TM_DT, tm + TM_D0 + ks * 8,
+                                   tc::desc_sw128(ptx::smem_u32(sm + OFF_MT + kb * 8192 + kin * 32)), id, ks > 0);
+                    }
+                    tc::commit(s_tbarT);
+                }
             }
         }
-        publish();
-        wt.wait();   // MMA1
-        if (ci + 1 < nchunks) stage_qkz(ci + 1);   // the S^T region is free now
-        if (tid == kStager) {                        // this chunk's gate tile into the Q_g half of L
+        wt1.wait();   // MMA1
+        if (tid == kStager) {
+            if (ci + 1 < nchunks) stage_qkz(ci + 1);   // the S^T region is free now
+            // this chunk's gate tile into the Q_g half of L
             ptx::mbar_arrive_expect_tx(s_gbar, C * D * 4);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 ptx::tma_load_4d(sm + OFF_OG + j * 16384, &maps.g, j * 32, h, t0, b, s_gbar);
         }
 
-        // ---- MMA_T: [Minv; P Minv] = [I; P] Minv (runs under the X epilogue).
-        if (tid == kIssuerB) {
-            constexpr uint32_t id = tc::idesc_tf32(128, 64);
-#pragma unroll 1
-            for (int ks = 0; ks < C / 8; ++ks) {
-                const int kb = ks >> 2, kin = ks & 3;
-                tc::mma_ts(tm + TM_DT, tm + TM_D0 + ks * 8,
-                           tc::desc_sw128(ptx::smem_u32(sm + OFF_MT + kb * 8192 + kin * 32)), id, ks > 0);
-            }
-            tc::commit(s_bar);
-        }
-
-        // ---- E: X = V - K_g S0 -> Diag(beta) X operand (N=128 x K=64); clear D1 top.
-        //      The operand element (row j, K = token r) has a fixed K block and
-        //      chunk per thread.
+        // ---- E (lane quadrants 0, 1, under the levels): X = V - K_g S0 ->
+        //      Diag(beta) X, the B operand of MMA2 as two N = 64 halves (value
+        //      channels) x 2 K blocks (tokens) in the K_g quarters of L (free
+        //      since MMA1); clear D1 top.
         if ((warp & 3) < 2) {
             const int r = qrow;   // token
             const float br = s_beta[r];
-            const uint32_t kr = (uint32_t)((r >> 5) * 128 * 128 + (r & 3) * 4);
+            const uint32_t kr = OFF_L + (uint32_t)(((grp >> 1) * 2 + (r >> 5)) * 16384 + (grp & 1) * 32 * 128 + (r & 3) * 4);
             const int rch = (r >> 2) & 7;
             const uint32_t vrow = OFF_V + r * 128;
 #pragma unroll 1
@@ -723,9 +747,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 tc::wait_ld();
                 const float xs[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = j0 + i;
-                    at<uint32_t>(sm, OFF_R + kr + j * 128 + ((rch ^ (j & 7)) << 4)) =
+                for (int i = 0; i < 8; ++i) {   // row j = j0 + i of the operand (j & 7 = i)
+                    at<uint32_t>(sm, kr + (g8 * 8 + i) * 128 + ((rch ^ i) << 4)) =
                         tc::f2tf32(br * (xs[i] - __uint_as_float(v[i])));
                     v[i] = 0u;
                 }
@@ -733,7 +756,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
         }
         publish();
-        wt.wait();   // MMA_T
+        wtT.wait();   // MMA_T
         if (ci + 1 < nchunks) stage_v(ci + 1);     // the Minv^T region is free now
 
         // ---- DT -> tf32 in place (A operand of MMA2).
@@ -749,14 +772,17 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         publish();
 
-        // ---- MMA2: D1 += [Minv; P Minv] Diag(beta) X = [U; P U].
+        // ---- MMA2: D1 += [Minv; P Minv] Diag(beta) X = [U; P U], as two N = 64 halves.
         if (tid == 0) {
-            constexpr uint32_t id = tc::idesc_tf32(128, 128);
+            constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll 1
-            for (int ks = 0; ks < C / 8; ++ks) {
-                const int kb = ks >> 2, kin = ks & 3;
-                tc::mma_ts(tm + TM_D1, tm + TM_DT + ks * 8,
-                           tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 16384 + kin * 32)), id, 1u);
+            for (int hv = 0; hv < 2; ++hv) {
+#pragma unroll 1
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const int kb = ks >> 2, kin = ks & 3;
+                    tc::mma_ts(tm + TM_D1 + hv * 64, tm + TM_DT + ks * 8,
+                               tc::desc_sw128(ptx::smem_u32(sm + OFF_L + (hv * 2 + kb) * 16384 + kin * 32)), id, 1u);
+                }
             }
             tc::commit(s_bar);
         }
