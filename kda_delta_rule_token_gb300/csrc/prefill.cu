@@ -786,6 +786,17 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             tc::commit(s_bar);
         }
+        // Under MMA2: the gate tile becomes gamma * sigmoid(gate) in place
+        // (warp 0, which issues MMA2, sits this out).
+        wgate.wait();
+        for (int e = tid - 32; e >= 0 && e < C * D / 4; e += kThreads - 32) {
+            const int box = e >> 9, r = (e >> 3) & (C - 1), ch = e & 7;
+            const uint32_t o = OFF_OG + box * 16384 + r * 128 + ((ch ^ (r & 7)) << 4);
+            const float4 gm = *reinterpret_cast<const float4*>(p.gamma + h * D + box * 32 + ch * 4);
+            const float4 gv = at<float4>(sm, o);
+            at<float4>(sm, o) = make_float4(gm.x * sigmoidf_(gv.x), gm.y * sigmoidf_(gv.y), gm.z * sigmoidf_(gv.z),
+                                            gm.w * sigmoidf_(gv.w));
+        }
         wt.wait();
 
         // ---- F: U -> operand of MMA3 (rows 0..63); sum of squares of O_pre
@@ -833,37 +844,26 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             tc::commit(s_bar);
         }
-        // O_pre -> RMSNorm, gamma, sigmoid gate -> o (D1 rows 64..127 are not
+        // O_pre -> RMSNorm x gamma sigmoid(gate) -> o (D1 rows 64..127 are not
         // touched by MMA3), written over the gate tile in shared memory and
         // stored by TMA (rows past T are clipped by the copy).
         if ((warp & 3) >= 2) {
             const int r = qrow - C;
             const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
                                          (1.0f / D) + p.rms_eps);
-            const float* gm = p.gamma + h * D + grp * 32;
             const uint32_t gbase = OFF_OG + grp * 16384 + r * 128;   // row r of box grp (SW128)
-            wgate.wait();
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 uint32_t v[8];
                 tc::ld8(tc::taddr(tm, warp, TM_D1 + grp * 32 + g8 * 8), v);
-                const float4 ma = *reinterpret_cast<const float4*>(gm + g8 * 8);
-                const float4 mb = *reinterpret_cast<const float4*>(gm + g8 * 8 + 4);
                 const uint32_t oa_at = gbase + (((2 * g8) ^ (r & 7)) << 4);
                 const uint32_t ob_at = gbase + (((2 * g8 + 1) ^ (r & 7)) << 4);
                 const float4 ga = at<float4>(sm, oa_at), gb = at<float4>(sm, ob_at);
                 tc::wait_ld();
-                float4 oa, ob;
-                oa.x = ma.x * __uint_as_float(v[0]) * inv * sigmoidf_(ga.x);
-                oa.y = ma.y * __uint_as_float(v[1]) * inv * sigmoidf_(ga.y);
-                oa.z = ma.z * __uint_as_float(v[2]) * inv * sigmoidf_(ga.z);
-                oa.w = ma.w * __uint_as_float(v[3]) * inv * sigmoidf_(ga.w);
-                ob.x = mb.x * __uint_as_float(v[4]) * inv * sigmoidf_(gb.x);
-                ob.y = mb.y * __uint_as_float(v[5]) * inv * sigmoidf_(gb.y);
-                ob.z = mb.z * __uint_as_float(v[6]) * inv * sigmoidf_(gb.z);
-                ob.w = mb.w * __uint_as_float(v[7]) * inv * sigmoidf_(gb.w);
-                at<float4>(sm, oa_at) = oa;
-                at<float4>(sm, ob_at) = ob;
+                at<float4>(sm, oa_at) = make_float4(ga.x * __uint_as_float(v[0]) * inv, ga.y * __uint_as_float(v[1]) * inv,
+                                                    ga.z * __uint_as_float(v[2]) * inv, ga.w * __uint_as_float(v[3]) * inv);
+                at<float4>(sm, ob_at) = make_float4(gb.x * __uint_as_float(v[4]) * inv, gb.y * __uint_as_float(v[5]) * inv,
+                                                    gb.z * __uint_as_float(v[6]) * inv, gb.w * __uint_as_float(v[7]) * inv);
             }
             ptx::fence_proxy_async_smem();
         }
