@@ -204,12 +204,13 @@ struct Maps {
 };
 
 // Issuing threads.  Issuing a group of MMAs stalls the issuing warp for
-// about the group's execution time, so MMA1 (under the inverse) comes from
-// warp 15, which has little work in C1; MMA_T from warp 15 as soon as it has
+// about the group's execution time, so MMA1 comes from warp 10 (little work
+// in C1 and the inverse's first pass); MMA_T from warp 15 as soon as it has
 // written the last inverse block; the staging copies and the output store
-// from warp 12 (it waits for MMA1 anyway); MMA0, MMA2 and MMA3 from thread 0
-// (warp 0 has no rows in the output epilogue).
-constexpr int kIssuerB = 480, kStager = 384;
+// from warp 12 (it waits for MMA1 anyway); MMA0 from thread 0 spread over its
+// state pass, MMA2 and MMA3 from thread 0 (warp 0 has no rows in the output
+// epilogue and skips the gate pass).
+constexpr int kIssuerB = 480, kIssuer1 = 320, kStager = 384;
 
 // 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and takes column group
 // w / 4 of every TMEM pass; in the thread-per-channel passes the same thread
@@ -516,18 +517,16 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         publish();
 
-        // ---- MMA0: [A'; P] = L R^T (runs under the state pass).
-        if (!fb && tid == 0) {
+        // ---- MMA0: [A'; P] = L R^T, issued by thread 0 a quarter (one K block)
+        //      per step of its state pass, so that the issue never waits long.
+        auto mma0_part = [&](int kb) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
-#pragma unroll 1
-            for (int ks = 0; ks < D / 8; ++ks) {
-                const int kb = ks >> 2, kin = ks & 3;
-                tc::mma_ss(tm + TM_D0,
-                           tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)),
-                           tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 8192 + kin * 32)), id, ks > 0);
-            }
-            tc::commit(s_bar);
-        }
+#pragma unroll
+            for (int kin = 0; kin < 4; ++kin)
+                tc::mma_ss(tm + TM_D0, tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)),
+                           tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 8192 + kin * 32)), id, (kb | kin) != 0);
+            if (kb == 3) tc::commit(s_bar);
+        };
 
         // ---- D: state pass: S^T operand scaled by e^{rho_L}, master scaled by
         //      e^{rho_R} (both also by the previous chunk's pending scale).
@@ -540,6 +539,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const int kch = (qrow >> 2) & 7;
 #pragma unroll 1
             for (int g8 = 0; g8 < 4; ++g8) {
+                if (!fb && tid == 0) mma0_part(g8);
                 uint32_t v[8];
                 const int j0 = grp * 32 + g8 * 8;
                 const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
@@ -558,18 +558,21 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         publish();
         if (!fb) wt.wait();   // MMA0
 
-        // ---- MMA1: D1 = L (Diag(e^rho_L) S0) = [K_g S0; Q_g S0] (runs under the inverse).
-        if (tid == kIssuerB) {
+        // ---- MMA1: D1 = L (Diag(e^rho_L) S0) = [K_g S0; Q_g S0] (runs under the
+        //      inverse), issued by warp 10 in two halves: K blocks 0, 1 before
+        //      C1 and 2, 3 after it (warp 10 has little work in C1 and C2).
+        auto mma1_part = [&](int half) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
 #pragma unroll 1
-            for (int ks = 0; ks < D / 8; ++ks) {
+            for (int ks = half * 8; ks < half * 8 + 8; ++ks) {
                 const int kb = ks >> 2, kin = ks & 3;
                 tc::mma_ss(tm + TM_D1,
                            tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)),
                            tc::desc_sw128(ptx::smem_u32(sm + OFF_ST + kb * 16384 + kin * 32)), id, ks > 0);
             }
-            tc::commit(s_bar1);
-        }
+            if (half == 1) tc::commit(s_bar1);
+        };
+        if (tid == kIssuer1) mma1_part(0);
 
         // ---- C1: N = Diag(beta) A' to shared memory as N^T (row b holds
         //      column b of N; 64-row SW128 layout), D0 -> [I; P] in TMEM (row
@@ -600,6 +603,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         tc::wait_st();
         sync_tc();
+
+        if (tid == kIssuer1) mma1_part(1);
 
         // ---- C2: Minv = (I + N)^{-1} (N strictly lower) by 16 x 16 blocks.
         //      Pass 1: forward substitution with the diagonal block I + N_II
@@ -789,13 +794,16 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // Under MMA2: the gate tile becomes gamma * sigmoid(gate) in place
         // (warp 0, which issues MMA2, sits this out).
         wgate.wait();
-        for (int e = tid - 32; e >= 0 && e < C * D / 4; e += kThreads - 32) {
-            const int box = e >> 9, r = (e >> 3) & (C - 1), ch = e & 7;
-            const uint32_t o = OFF_OG + box * 16384 + r * 128 + ((ch ^ (r & 7)) << 4);
-            const float4 gm = *reinterpret_cast<const float4*>(p.gamma + h * D + box * 32 + ch * 4);
-            const float4 gv = at<float4>(sm, o);
-            at<float4>(sm, o) = make_float4(gm.x * sigmoidf_(gv.x), gm.y * sigmoidf_(gv.y), gm.z * sigmoidf_(gv.z),
-                                            gm.w * sigmoidf_(gv.w));
+        if (warp > 0) {   // lane = (box, 16-byte chunk) of a row: channels 4 lane .. 4 lane + 3
+            const int box = lane >> 3, ch = lane & 7;
+            const float4 gm = *reinterpret_cast<const float4*>(p.gamma + h * D + lane * 4);
+#pragma unroll 1
+            for (int r = warp - 1; r < C; r += 15) {
+                const uint32_t o = OFF_OG + box * 16384 + r * 128 + ((ch ^ (r & 7)) << 4);
+                const float4 gv = at<float4>(sm, o);
+                at<float4>(sm, o) = make_float4(gm.x * sigmoidf_(gv.x), gm.y * sigmoidf_(gv.y), gm.z * sigmoidf_(gv.z),
+                                                gm.w * sigmoidf_(gv.w));
+            }
         }
         wt.wait();
 
