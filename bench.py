@@ -511,7 +511,7 @@ def main():
     if pre is not None:
         pw = pre["wl"]
         tf32_peak = peaks["bf16_tflops"] * 0.5
-        psha = source_sha("prefill.cu")
+        psha = source_sha("prefill.cu", "ptx.cuh", "tc.cuh")
         line["prefill"] = {
             "workload": pw.name, "B": pw.B, "H": pw.H, "T": pw.T, "chunk": pw.chunk,
             "value": round(pre["tokens_s"], 1), "unit": "tokens/s",
