@@ -495,13 +495,18 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             for (int g8 = 0; g8 < 2; ++g8) {
                 uint32_t rt[8];
                 float g[8], yk[8], yq[8];
+                const int r0 = grp * 16 + g8 * 8;
+                const float4 nk0 = *reinterpret_cast<const float4*>(s_rk + r0), nk1 = *reinterpret_cast<const float4*>(s_rk + r0 + 4);
+                const float4 nq0 = *reinterpret_cast<const float4*>(s_rq + r0), nq1 = *reinterpret_cast<const float4*>(s_rq + r0 + 4);
+                const float nk[8] = {nk0.x, nk0.y, nk0.z, nk0.w, nk1.x, nk1.y, nk1.z, nk1.w};
+                const float nq[8] = {nq0.x, nq0.y, nq0.z, nq0.w, nq1.x, nq1.y, nq1.z, nq1.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int r = grp * 16 + g8 * 8 + i;
+                    const int r = r0 + i;
                     const uint32_t ro = (uint32_t)(r * 128 + ((cch ^ (r & 7)) << 4));
                     g[i] = at<float>(sm, OFF_R + kcR + ro) + goff;
-                    yk[i] = at<float>(sm, OFF_L + kcL + ro) * s_rk[r];
-                    yq[i] = at<float>(sm, OFF_L + kcL + C * 128 + ro) * s_rq[r];
+                    yk[i] = at<float>(sm, OFF_L + kcL + ro) * nk[i];
+                    yq[i] = at<float>(sm, OFF_L + kcL + C * 128 + ro) * nq[i];
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -539,22 +544,24 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             // S^T operand element (row j, K = qrow): K block and chunk are fixed per thread.
             const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
             const int kch = (qrow >> 2) & 7;
-#pragma unroll 1
-            for (int g8 = 0; g8 < 4; ++g8) {
-                if (!fb && tid == 0) mma0_part(g8);
-                uint32_t v[8];
-                const int j0 = grp * 32 + g8 * 8;
+            {
+                uint32_t v[32];
+                const int j0 = grp * 32;
                 const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
-                tc::ld8(ta, v);
+                tc::ld32(ta, v);
                 tc::wait_ld();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = j0 + i;
-                    const float sv = __uint_as_float(v[i]);
-                    at<uint32_t>(sm, OFF_ST + kq + j * 128 + ((kch ^ (j & 7)) << 4)) = tc::f2tf32(sv * eL);
-                    v[i] = __float_as_uint(sv * eR);
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    if (!fb && tid == 0) mma0_part(g8);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int j = j0 + g8 * 8 + i;
+                        const float sv = __uint_as_float(v[g8 * 8 + i]);
+                        at<uint32_t>(sm, OFF_ST + kq + j * 128 + ((kch ^ (j & 7)) << 4)) = tc::f2tf32(sv * eL);
+                        v[g8 * 8 + i] = __float_as_uint(sv * eR);
+                    }
                 }
-                tc::st8(ta, v);
+                tc::st32(ta, v);
             }
         }
         publish();
@@ -583,25 +590,22 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const bool isA = qrow < C;
             const int r = isA ? qrow : qrow - C;
             const float br = s_beta[r];
-#pragma unroll 1
-            for (int g8 = 0; g8 < 2; ++g8) {
-                const int i0 = grp * 16 + g8 * 8;
-                uint32_t v[8];
-                tc::ld8(tc::taddr(tm, warp, TM_D0 + i0), v);
-                tc::wait_ld();
-                if (isA) {
+            const int i0 = grp * 16;
+            uint32_t v[16];
+            tc::ld16(tc::taddr(tm, warp, TM_D0 + i0), v);
+            tc::wait_ld();
+            if (isA) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        at<float>(sm, OFF_R + tc::sw128(i0 + i, r, C)) = (i0 + i) < r ? br * __uint_as_float(v[i]) : 0.f;
-                        v[i] = (i0 + i) == r ? tc::f2tf32(1.0f) : 0u;
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        v[i] = (i0 + i) <= r ? tc::f2tf32(__uint_as_float(v[i])) : 0u;
+                for (int i = 0; i < 16; ++i) {
+                    at<float>(sm, OFF_R + tc::sw128(i0 + i, r, C)) = (i0 + i) < r ? br * __uint_as_float(v[i]) : 0.f;
+                    v[i] = (i0 + i) == r ? tc::f2tf32(1.0f) : 0u;
                 }
-                tc::st8(tc::taddr(tm, warp, TM_D0 + i0), v);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[i] = (i0 + i) <= r ? tc::f2tf32(__uint_as_float(v[i])) : 0u;
             }
+            tc::st16(tc::taddr(tm, warp, TM_D0 + i0), v);
         }
         tc::wait_st();
         sync_tc();
@@ -742,40 +746,38 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const uint32_t kr = OFF_L + (uint32_t)(((grp >> 1) * 2 + (r >> 5)) * 16384 + (grp & 1) * 32 * 128 + (r & 3) * 4);
             const int rch = (r >> 2) & 7;
             const uint32_t vrow = OFF_V + r * 128;
-#pragma unroll 1
+            uint32_t v[32];
+            const uint32_t ta = tc::taddr(tm, warp, TM_D1 + grp * 32);
+            tc::ld32(ta, v);
+            const uint32_t vb = vrow + grp * 64 * 128;   // V columns grp * 32 .. + 32 (one K block)
+            tc::wait_ld();
+#pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
-                const int j0 = grp * 32 + g8 * 8;
-                uint32_t v[8];
-                const uint32_t ta = tc::taddr(tm, warp, TM_D1 + j0);
-                tc::ld8(ta, v);
-                const uint32_t vb = vrow + (j0 >> 5) * 64 * 128;
-                const float4 v0 = at<float4>(sm, vb + (((((j0 & 31) >> 2)) ^ (r & 7)) << 4));
-                const float4 v1 = at<float4>(sm, vb + (((((j0 & 31) >> 2) + 1) ^ (r & 7)) << 4));
-                tc::wait_ld();
+                const float4 v0 = at<float4>(sm, vb + (((2 * g8) ^ (r & 7)) << 4));
+                const float4 v1 = at<float4>(sm, vb + (((2 * g8 + 1) ^ (r & 7)) << 4));
                 const float xs[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {   // row j = j0 + i of the operand (j & 7 = i)
+                for (int i = 0; i < 8; ++i) {   // row j = grp * 32 + 8 g8 + i of the operand (j & 7 = i)
                     at<uint32_t>(sm, kr + (g8 * 8 + i) * 128 + ((rch ^ i) << 4)) =
-                        tc::f2tf32(br * (xs[i] - __uint_as_float(v[i])));
-                    v[i] = 0u;
+                        tc::f2tf32(br * (xs[i] - __uint_as_float(v[g8 * 8 + i])));
+                    v[g8 * 8 + i] = 0u;
                 }
-                tc::st8(ta, v);
             }
+            tc::st32(ta, v);
         }
         publish();
         wtT.wait();   // MMA_T
         if (ci + 1 < nchunks) stage_v(ci + 1);     // the Minv^T region is free now
 
         // ---- DT -> tf32 in place (A operand of MMA2).
-#pragma unroll 1
-        for (int g8 = 0; g8 < 2; ++g8) {
-            uint32_t v[8];
-            const uint32_t ta = tc::taddr(tm, warp, TM_DT + grp * 16 + g8 * 8);
-            tc::ld8(ta, v);
+        {
+            uint32_t v[16];
+            const uint32_t ta = tc::taddr(tm, warp, TM_DT + grp * 16);
+            tc::ld16(ta, v);
             tc::wait_ld();
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = tc::f2tf32(__uint_as_float(v[i]));
-            tc::st8(ta, v);
+            for (int i = 0; i < 16; ++i) v[i] = tc::f2tf32(__uint_as_float(v[i]));
+            tc::st16(ta, v);
         }
         publish();
 
@@ -816,30 +818,26 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const int r = qrow;
             const uint32_t kr = (uint32_t)((r >> 5) * 128 * 128 + (r & 3) * 4);
             const int rch = (r >> 2) & 7;
-#pragma unroll 1
-            for (int g8 = 0; g8 < 4; ++g8) {
-                const int j0 = grp * 32 + g8 * 8;
-                uint32_t v[8];
-                tc::ld8(tc::taddr(tm, warp, TM_D1 + j0), v);
-                tc::wait_ld();
+            uint32_t v[32];
+            tc::ld32(tc::taddr(tm, warp, TM_D1 + grp * 32), v);
+            tc::wait_ld();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int j = j0 + i;
-                    at<uint32_t>(sm, OFF_R + kr + j * 128 + ((rch ^ (j & 7)) << 4)) =
-                        tc::f2tf32(__uint_as_float(v[i]));
-                }
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = grp * 32 + jj;
+                at<uint32_t>(sm, OFF_R + kr + j * 128 + ((rch ^ (j & 7)) << 4)) = tc::f2tf32(__uint_as_float(v[jj]));
             }
         } else {
             const int r = qrow - C;
-            float ss = 0.f;
-#pragma unroll 1
-            for (int g8 = 0; g8 < 4; ++g8) {
-                uint32_t v[8];
-                tc::ld8(tc::taddr(tm, warp, TM_D1 + grp * 32 + g8 * 8), v);
-                tc::wait_ld();
+            float ss = 0.f, ss2 = 0.f;
+            uint32_t v[32];
+            tc::ld32(tc::taddr(tm, warp, TM_D1 + grp * 32), v);
+            tc::wait_ld();
 #pragma unroll
-                for (int i = 0; i < 8; ++i) ss = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss);
+            for (int i = 0; i < 32; i += 2) {
+                ss = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss);
+                ss2 = fmaf(__uint_as_float(v[i + 1]), __uint_as_float(v[i + 1]), ss2);
             }
+            ss += ss2;
             s_part[grp * C + r] = ss;
         }
         publish();   // U operand visible; partial sums visible
@@ -863,14 +861,15 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
                                          (1.0f / D) + p.rms_eps);
             const uint32_t gbase = OFF_OG + grp * 16384 + r * 128;   // row r of box grp (SW128)
+            uint32_t w[32];
+            tc::ld32(tc::taddr(tm, warp, TM_D1 + grp * 32), w);
+            tc::wait_ld();
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
-                uint32_t v[8];
-                tc::ld8(tc::taddr(tm, warp, TM_D1 + grp * 32 + g8 * 8), v);
+                const uint32_t* v = w + g8 * 8;
                 const uint32_t oa_at = gbase + (((2 * g8) ^ (r & 7)) << 4);
                 const uint32_t ob_at = gbase + (((2 * g8 + 1) ^ (r & 7)) << 4);
                 const float4 ga = at<float4>(sm, oa_at), gb = at<float4>(sm, ob_at);
-                tc::wait_ld();
                 at<float4>(sm, oa_at) = make_float4(ga.x * __uint_as_float(v[0]) * inv, ga.y * __uint_as_float(v[1]) * inv,
                                                     ga.z * __uint_as_float(v[2]) * inv, ga.w * __uint_as_float(v[3]) * inv);
                 at<float4>(sm, ob_at) = make_float4(gb.x * __uint_as_float(v[4]) * inv, gb.y * __uint_as_float(v[5]) * inv,
