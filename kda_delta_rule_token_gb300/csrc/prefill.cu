@@ -28,13 +28,14 @@
 //   MMA0  D0 = L R^T                                  (N = 64,  K = 128)
 //   MMA_T DT = [I; P] Minv          A from TMEM       (N = 64,  K = 64)
 //   MMA1  D1 = L (Diag(e^rho) S0)                     (N = 128, K = 128)
-//   MMA2  D1 += DT (Diag(beta) X)   A from TMEM       (N = 128, K = 64)
+//   MMA2  D1 += DT (Diag(beta) X)   A from TMEM       (2 x N = 64, K = 64)
 //         with D1's top half cleared after X = V - K_g S0 was read, so D1 =
 //         [U; O_pre]
 //   MMA3  M  += R^T U               A from TMEM       (N = 128, K = 64)
 //         on the TMEM master M = Diag(e^rho) S0; S_new = e^{G_last-rho} M, that
 //         row scale being applied by the next chunk's pass over the master.
-// The unit-lower inverse is a forward substitution on CUDA cores.
+// The unit-lower inverse is a forward substitution on CUDA cores for the
+// diagonal 16 x 16 blocks and warp-level tf32 MMAs for the rest.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
