@@ -148,6 +148,34 @@ KDA_API kda_status kda_prefill(kda_ctx *ctx, int B, int T,
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Prefill of B packed sequences of different lengths: sequence b is tokens
+ * [cu_seqlens[b], cu_seqlens[b+1]) of one token axis of total_T tokens, and
+ * the result for it is that of kda_prefill on those tokens alone (same
+ * arithmetic, computed by the same kernel), continuing from its own
+ * conv_state[b] and S[b].  This is the recurrence of "Kimi K3 Metal Gap
+ * Analysis", section 2 "KDA Attention", row "Recurrence", run per sequence;
+ * the packed layout is this library's (the pages process one sequence).
+ *   cu_seqlens   [B+1] int32, DEVICE memory, non-decreasing, cu_seqlens[0] = 0
+ *                and cu_seqlens[B] = total_T.  Read by the kernel; each
+ *                range is clamped to [0, total_T] (a malformed array gives
+ *                wrong sequences, never an access outside the arrays).
+ *   q, k, v      [total_T][H][d] bf16 (raw bit patterns)  pre-conv inputs (in)
+ *   z            [total_T][H][d] fp32 (in)
+ *   beta_logit   [total_T][H]    fp32 (in)
+ *   gate_logit   [total_T][H][d] fp32 (in)
+ *   conv_state   [B][3][3*H*d] fp32 (in/out), as for kda_decode_step
+ *   S            [B][H][d][d] fp32 (in/out)
+ *   o            [total_T][H][d] fp32 (out)
+ * Alignment as for kda_prefill; cu_seqlens 4-byte aligned.  A sequence of
+ * length 0 leaves its state and window unchanged; B == 0 or total_T == 0 is a
+ * no-op returning KDA_OK.  Needs no workspace.
+ */
+KDA_API kda_status kda_prefill_varlen(kda_ctx *ctx, int B, const int32_t *cu_seqlens, int total_T,
+                       const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       const float *z, const float *beta_logit, const float *gate_logit,
+                       float *conv_state, float *S, float *o, void *stream);
+
+/*
  * Synchronise `stream` and report whether any kernel launched with this
  * context since the last call gave up on a bounded wait (KDA_ERR_TIMEOUT) or
  * raised a CUDA error (KDA_ERR_CUDA).  Clears the error word.

@@ -15,7 +15,7 @@ from . import build as _build_mod
 
 __all__ = [
     "KDAError", "load", "kda_create", "kda_destroy", "kda_strerror", "kda_last_error_detail",
-    "kda_decode_step", "kda_prefill", "kda_prefill_workspace_bytes", "kda_sync_status",
+    "kda_decode_step", "kda_prefill", "kda_prefill_varlen", "kda_prefill_workspace_bytes", "kda_sync_status",
     "kda_launch_count", "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_ALIGNMENT",
     "KDA_ERR_UNSUPPORTED", "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "HEAD_DIM", "CHUNK",
 ]
@@ -75,6 +75,8 @@ def load(path: str | None = None):
     lib.kda_prefill_workspace_bytes.restype = sz
     lib.kda_prefill.argtypes = [vp, i32, i32] + [vp] * 10 + [sz, vp]
     lib.kda_prefill.restype = i32
+    lib.kda_prefill_varlen.argtypes = [vp, i32, vp, i32] + [vp] * 10
+    lib.kda_prefill_varlen.restype = i32
     lib.kda_sync_status.argtypes = [vp, vp]
     lib.kda_sync_status.restype = i32
     lib.kda_launch_count.argtypes = []
@@ -151,6 +153,14 @@ def kda_prefill(ctx, B, T, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
     _check(load().kda_prefill(ctx, int(B), int(T), _p(q), _p(k), _p(v), _p(z), _p(beta_logit),
                               _p(gate_logit), _p(conv_state), _p(S), _p(o), _p(workspace),
                               int(workspace_bytes), _stream(stream)), "kda_prefill")
+
+
+def kda_prefill_varlen(ctx, B, cu_seqlens, total_T, q, k, v, z, beta_logit, gate_logit, conv_state,
+                       S, o, stream=None) -> None:
+    """Packed sequences: cu_seqlens is a device int32 tensor of B + 1 offsets."""
+    _check(load().kda_prefill_varlen(ctx, int(B), _p(cu_seqlens), int(total_T), _p(q), _p(k), _p(v),
+                                     _p(z), _p(beta_logit), _p(gate_logit), _p(conv_state), _p(S),
+                                     _p(o), _stream(stream)), "kda_prefill_varlen")
 
 
 def kda_sync_status(ctx, stream=None) -> int:

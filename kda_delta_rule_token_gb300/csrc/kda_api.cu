@@ -158,11 +158,32 @@ kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint
         if (!workspace || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
         if (!aligned16(workspace)) return KDA_ERR_ALIGNMENT;
     }
-    kda::PrefillIO io{B, T, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
+    kda::PrefillIO io{B, T, nullptr, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
                       workspace, workspace_bytes};
     cudaError_t e = kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word,
                                         static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) { kda::set_detail("prefill launch", e); return KDA_ERR_CUDA; }
+    return KDA_OK;
+}
+
+kda_status kda_prefill_varlen(kda_ctx* ctx, int B, const int32_t* cu_seqlens, int total_T,
+                              const uint16_t* q, const uint16_t* k, const uint16_t* v, const float* z,
+                              const float* beta_logit, const float* gate_logit, float* conv_state,
+                              float* S, float* o, void* stream) {
+    if (!ctx || B < 0 || total_T < 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0 || total_T == 0) return KDA_OK;   // every sequence empty: state and window unchanged
+    if (!cu_seqlens || !q || !k || !v || !z || !beta_logit || !gate_logit || !conv_state || !S || !o)
+        return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, z, gate_logit, conv_state, S, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (!aligned4(beta_logit) || !aligned4(cu_seqlens)) return KDA_ERR_ALIGNMENT;
+    if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    kda::PrefillIO io{B, total_T, cu_seqlens, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
+                      nullptr, 0};
+    cudaError_t e = kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word,
+                                        static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { kda::set_detail("prefill_varlen launch", e); return KDA_ERR_CUDA; }
     return KDA_OK;
 }
 

@@ -40,7 +40,8 @@ struct DecodeIO {
 
 struct PrefillIO {
     int B;
-    int T;
+    int T;              // tokens per sequence, or the total of packed sequences
+    const int* cu_seqlens;   // null, or [B + 1] device offsets of packed sequences
     const uint16_t* q;  // bf16 bits
     const uint16_t* k;
     const uint16_t* v;

@@ -239,7 +239,22 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh - b * p.H;
-    const int H = p.H, T = io.T;
+    const int H = p.H;
+    // This sequence's tokens: rows [rowbase, rowbase + T) of the token axis.
+    // Fixed length: T = io.T, the maps' axes are (d, H, T, B) and the copies
+    // address (t, b); packed sequences (cu_seqlens): the maps' axes are
+    // (d, H, total, 1), the copies address (tb0 + t, 0), and the range is
+    // clamped to [0, total].
+    int T = io.T, tb0 = 0, bmap = b;
+    size_t rowbase = (size_t)b * io.T;
+    if (io.cu_seqlens) {
+        const int lo = min(max(io.cu_seqlens[b], 0), io.T);
+        const int hi = min(max(io.cu_seqlens[b + 1], lo), io.T);
+        T = hi - lo;
+        tb0 = lo;
+        bmap = 0;
+        rowbase = (size_t)lo;
+    }
     const size_t HD = (size_t)H * D, HD3 = 3 * HD;
     const int nchunks = (T + C - 1) / C;
     const int qrow = (warp & 3) * 32 + lane;   // TMEM lane; channel of the per-channel passes
@@ -254,14 +269,14 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     auto stage_qkz = [&](int ci) {
         if (tid == kStager) {
             ptx::mbar_arrive_expect_tx(s_tbar, kStageBytes);
-            ptx::tma_load_4d(sm + STG_Q, &maps.q, 0, h, ci * C, b, s_tbar);
-            ptx::tma_load_4d(sm + STG_K, &maps.k, 0, h, ci * C, b, s_tbar);
-            ptx::tma_load_4d(sm + STG_Z, &maps.z, 0, h, ci * C, b, s_tbar);
-            ptx::tma_prefetch_4d(&maps.v, 0, h, ci * C, b);   // v lands later; have it in L2
+            ptx::tma_load_4d(sm + STG_Q, &maps.q, 0, h, tb0 + ci * C, bmap, s_tbar);
+            ptx::tma_load_4d(sm + STG_K, &maps.k, 0, h, tb0 + ci * C, bmap, s_tbar);
+            ptx::tma_load_4d(sm + STG_Z, &maps.z, 0, h, tb0 + ci * C, bmap, s_tbar);
+            ptx::tma_prefetch_4d(&maps.v, 0, h, tb0 + ci * C, bmap);   // v lands later; have it in L2
         }
     };
     auto stage_v = [&](int ci) {
-        if (tid == 0) ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, ci * C, b, s_tbar);
+        if (tid == 0) ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, tb0 + ci * C, bmap, s_tbar);
     };
     if (tid == 0) {
         ptx::mbar_init(s_bar, 1);
@@ -279,8 +294,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     Waiter wgate{s_gbar, s_dead, err, 0u};
     Waiter wtT{s_tbarT, s_dead, err, 0u};
     Waiter wt1{s_bar1, s_dead, err, 0u};
-    stage_qkz(0);
-    stage_v(0);
+    if (nchunks > 0) {
+        stage_qkz(0);
+        stage_v(0);
+    }
 
     // Initial state into the TMEM master (row qrow, columns of this group).
     {
@@ -339,7 +356,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         //      tiles); decay and its cumulative sum.  Loads of token group
         //      g + 1 are issued before the stores of group g.
         // beta logits of the chunk, consumed after the conv phase.
-        const float blog = tid < n ? io.beta_logit[((size_t)(b * T + t0 + tid)) * H + h] : 0.f;
+        const float blog = tid < n ? io.beta_logit[(rowbase + t0 + tid) * H + h] : 0.f;
         wtma.wait();
         if (grp < 3) {
             const uint32_t* src = reinterpret_cast<const uint32_t*>(
@@ -734,7 +751,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             ptx::mbar_arrive_expect_tx(s_gbar, C * D * 4);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                ptx::tma_load_4d(sm + OFF_OG + j * 16384, &maps.g, j * 32, h, t0, b, s_gbar);
+                ptx::tma_load_4d(sm + OFF_OG + j * 16384, &maps.g, j * 32, h, tb0 + t0, bmap, s_gbar);
         }
 
         // ---- E (lane quadrants 0, 1, under the levels): X = V - K_g S0 ->
@@ -856,7 +873,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         // O_pre -> RMSNorm x gamma sigmoid(gate) -> o (D1 rows 64..127 are not
         // touched by MMA3), written over the gate tile in shared memory and
-        // stored by TMA (rows past T are clipped by the copy).
+        // stored by TMA (rows past T are clipped by the copy).  The last,
+        // partial chunk of a packed sequence stores its rows < n directly: the
+        // rows after it belong to the next sequence.
+        const bool direct = io.cu_seqlens != nullptr && n < C;
         if ((warp & 3) >= 2) {
             const int r = qrow - C;
             const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
@@ -871,17 +891,25 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 const uint32_t oa_at = gbase + (((2 * g8) ^ (r & 7)) << 4);
                 const uint32_t ob_at = gbase + (((2 * g8 + 1) ^ (r & 7)) << 4);
                 const float4 ga = at<float4>(sm, oa_at), gb = at<float4>(sm, ob_at);
-                at<float4>(sm, oa_at) = make_float4(ga.x * __uint_as_float(v[0]) * inv, ga.y * __uint_as_float(v[1]) * inv,
-                                                    ga.z * __uint_as_float(v[2]) * inv, ga.w * __uint_as_float(v[3]) * inv);
-                at<float4>(sm, ob_at) = make_float4(gb.x * __uint_as_float(v[4]) * inv, gb.y * __uint_as_float(v[5]) * inv,
-                                                    gb.z * __uint_as_float(v[6]) * inv, gb.w * __uint_as_float(v[7]) * inv);
+                const float4 oa = make_float4(ga.x * __uint_as_float(v[0]) * inv, ga.y * __uint_as_float(v[1]) * inv,
+                                              ga.z * __uint_as_float(v[2]) * inv, ga.w * __uint_as_float(v[3]) * inv);
+                const float4 ob = make_float4(gb.x * __uint_as_float(v[4]) * inv, gb.y * __uint_as_float(v[5]) * inv,
+                                              gb.z * __uint_as_float(v[6]) * inv, gb.w * __uint_as_float(v[7]) * inv);
+                if (!direct) {
+                    at<float4>(sm, oa_at) = oa;
+                    at<float4>(sm, ob_at) = ob;
+                } else if (r < n) {
+                    float* orow = io.o + ((rowbase + t0 + r) * H + h) * D + grp * 32 + g8 * 8;
+                    *reinterpret_cast<float4*>(orow) = oa;
+                    *reinterpret_cast<float4*>(orow + 4) = ob;
+                }
             }
             ptx::fence_proxy_async_smem();
         }
         __syncthreads();
-        if (tid == kStager) {
+        if (tid == kStager && !direct) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) ptx::tma_store_4d(&maps.o, j * 32, h, t0, b, sm + OFF_OG + j * 16384);
+            for (int j = 0; j < 4; ++j) ptx::tma_store_4d(&maps.o, j * 32, h, tb0 + t0, bmap, sm + OFF_OG + j * 16384);
             ptx::bulk_commit();
         }
         wt.wait();
@@ -917,7 +945,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 const int t = T - 3 + j;
                 float2 w;
                 if (t >= 0) {
-                    const uint32_t u = *reinterpret_cast<const uint32_t*>(x + (((size_t)(b * T + t)) * H + h) * D + cp);
+                    const uint32_t u = *reinterpret_cast<const uint32_t*>(x + ((rowbase + t) * H + h) * D + cp);
                     w = make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
                 } else {   // an older tap of the initial window (not yet overwritten: j + T > j)
                     w = *reinterpret_cast<const float2*>(win + (j + T) * HD3 + gcp);
@@ -977,13 +1005,14 @@ cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const Devi
         if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device] = true;
     }
     Maps maps;
-    if (!make_map(&maps.q, io.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, io.B) ||
-        !make_map(&maps.k, io.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, io.B) ||
-        !make_map(&maps.v, io.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, io.B) ||
-        !make_map(&maps.z, io.z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, io.B) ||
-        !make_map(&maps.g, io.gate_logit, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, io.B, 32,
+    const int mB = io.cu_seqlens ? 1 : io.B;   // packed sequences: one token axis of length io.T
+    if (!make_map(&maps.q, io.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, mB) ||
+        !make_map(&maps.k, io.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, mB) ||
+        !make_map(&maps.v, io.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.H, io.T, mB) ||
+        !make_map(&maps.z, io.z, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, mB) ||
+        !make_map(&maps.g, io.gate_logit, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, mB, 32,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&maps.o, io.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, io.B, 32,
+        !make_map(&maps.o, io.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, mB, 32,
                   CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     kda_prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p, io, err_word, maps);

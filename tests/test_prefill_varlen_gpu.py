@@ -1,0 +1,152 @@
+"""Packed sequences of different lengths (kda_prefill_varlen) on the GPU.
+
+Each sequence is checked against the fp64 oracle run on that sequence alone
+(rel-L2 2e-3 over o and the final S; the conv window exactly), and the packed
+call must give exactly what one kda_prefill call per sequence gives: the
+same kernel runs the same arithmetic, only the addressing differs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_delta_rule_token_gb300 as kda
+from kda_delta_rule_token_gb300 import synth
+from harness import max_rel_err, np64, oracle_pairs, pair_window, rel_l2
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from kda_delta_rule_token_gb300 import build
+    build.build()
+    kda.load()
+
+
+def bits(x):
+    return x.view(torch.int16)
+
+
+def packed(tokens, lengths):
+    """[B, Tmax, ...] per-sequence tokens -> packed [total, ...] (first L_b of each)."""
+    out = {n: torch.cat([tokens[n][b, :L] for b, L in enumerate(lengths)], 0).contiguous()
+           for n in ("q", "k", "v", "z", "gate_logit", "beta_logit")}
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device=DEV)
+    return out, cu
+
+
+def run_varlen(H, params, pk, cu, S, conv):
+    total = int(cu[-1].item())
+    o = torch.full((total, H, 128), float("nan"), device=DEV)
+    ctx = kda.kda_create(H, params["conv_w"], params["dt_bias"], params["A_log"], params["gamma"])
+    try:
+        kda.kda_prefill_varlen(ctx, len(cu) - 1, cu, total, bits(pk["q"]), bits(pk["k"]), bits(pk["v"]),
+                               pk["z"], pk["beta_logit"], pk["gate_logit"], conv, S, o)
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+    finally:
+        kda.kda_destroy(ctx)
+    return o
+
+
+def run_separate(H, params, tokens, lengths, S, conv):
+    """One kda_prefill call per (non-empty) sequence, B = 1 each."""
+    outs = []
+    ctx = kda.kda_create(H, params["conv_w"], params["dt_bias"], params["A_log"], params["gamma"])
+    try:
+        for b, L in enumerate(lengths):
+            if L == 0:
+                continue
+            sl = {n: tokens[n][b:b + 1, :L].contiguous() for n in tokens}
+            o = torch.empty((1, L, H, 128), device=DEV)
+            Sb, cb = S[b:b + 1].clone(), conv[b:b + 1].clone()
+            kda.kda_prefill(ctx, 1, L, bits(sl["q"]), bits(sl["k"]), bits(sl["v"]), sl["z"],
+                            sl["beta_logit"], sl["gate_logit"], cb, Sb, o)
+            S[b:b + 1].copy_(Sb)
+            conv[b:b + 1].copy_(cb)
+            outs.append(o[0])
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+    finally:
+        kda.kda_destroy(ctx)
+    return torch.cat(outs, 0) if outs else torch.empty((0, H, 128), device=DEV)
+
+
+LENGTHS = [0, 1, 2, 63, 64, 65, 130, 5]
+
+
+def _setup(lengths, H=2):
+    wl = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], B=len(lengths), H=H, T=max(lengths),
+                      s0_std=0.05, win_std=1.0)
+    params = synth.make_params(wl, DEV)
+    tokens = synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    return wl, params, tokens, st["S"], st["conv_state"]
+
+
+def test_varlen_matches_oracle_per_sequence():
+    wl, params, tokens, S, conv = _setup(LENGTHS)
+    S0, c0 = S.clone(), conv.clone()
+    pk, cu = packed(tokens, LENGTHS)
+    o = run_varlen(wl.H, params, pk, cu, S, conv)
+    start = 0
+    for b, L in enumerate(LENGTHS):
+        if L == 0:
+            assert torch.equal(S[b], S0[b]) and torch.equal(conv[b], c0[b])
+            continue
+        tk = {n: tokens[n][b:b + 1, :L] for n in tokens}
+        ref = oracle_pairs(params, tk, S0[b:b + 1], c0[b:b + 1], [(0, h) for h in range(wl.H)],
+                           call_major=False)
+        for h in range(wl.H):
+            eo = rel_l2(np64(o[start:start + L, h]), ref[(0, h)].o[0, :, 0])
+            es = rel_l2(np64(S[b, h]), ref[(0, h)].S[0, 0])
+            assert eo <= TOL, f"seq {b} head {h}: o rel-L2 {eo:.3e}"
+            assert es <= TOL, f"seq {b} head {h}: S rel-L2 {es:.3e}"
+            assert max_rel_err(pair_window(conv, b, h), ref[(0, h)].conv_state) == 0.0
+        start += L
+
+
+def test_varlen_equals_separate_calls():
+    wl, params, tokens, S, conv = _setup(LENGTHS)
+    S2, c2 = S.clone(), conv.clone()
+    pk, cu = packed(tokens, LENGTHS)
+    o_v = run_varlen(wl.H, params, pk, cu, S, conv)
+    o_s = run_separate(wl.H, params, tokens, LENGTHS, S2, c2)
+    assert torch.equal(o_v, o_s)
+    assert torch.equal(S, S2)
+    assert torch.equal(conv, c2)
+
+
+def test_varlen_all_empty_or_zero_total_is_noop():
+    wl, params, tokens, S, conv = _setup([0, 0, 3])
+    S0, c0 = S.clone(), conv.clone()
+    cu = torch.zeros(4, dtype=torch.int32, device=DEV)
+    o = torch.empty((1, wl.H, 128), device=DEV)
+    ctx = kda.kda_create(wl.H, params["conv_w"], params["dt_bias"], params["A_log"], params["gamma"])
+    try:
+        t = tokens
+        kda.kda_prefill_varlen(ctx, 3, cu, 0, bits(t["q"]), bits(t["k"]), bits(t["v"]), t["z"],
+                               t["beta_logit"], t["gate_logit"], conv, S, o)
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+    finally:
+        kda.kda_destroy(ctx)
+    assert torch.equal(S, S0) and torch.equal(conv, c0)
+
+
+def test_varlen_long_sequences_sampled():
+    """Mixed long lengths (several chunks, ragged tails), sampled heads vs the oracle."""
+    lengths = [1000, 333, 0, 2049]
+    wl, params, tokens, S, conv = _setup(lengths, H=4)
+    S0, c0 = S.clone(), conv.clone()
+    pk, cu = packed(tokens, lengths)
+    o = run_varlen(wl.H, params, pk, cu, S, conv)
+    starts = np.concatenate([[0], np.cumsum(lengths)])
+    for b, h in [(0, 1), (1, 3), (3, 0)]:
+        L = lengths[b]
+        tk = {n: tokens[n][b:b + 1, :L] for n in tokens}
+        ref = oracle_pairs(params, tk, S0[b:b + 1], c0[b:b + 1], [(0, h)], call_major=False)[(0, h)]
+        s = starts[b]
+        assert rel_l2(np64(o[s:s + L, h]), ref.o[0, :, 0]) <= TOL
+        assert rel_l2(np64(S[b, h]), ref.S[0, 0]) <= TOL
+        assert max_rel_err(pair_window(conv, b, h), ref.conv_state) == 0.0
+    assert torch.equal(S[2], S0[2]) and torch.equal(conv[2], c0[2])
