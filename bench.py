@@ -351,6 +351,61 @@ class Ours:
         return res
 
 
+    # ------------------------------------------------------- packed-sequence prefill
+    def prefill_varlen(self):
+        """kda_prefill_varlen on 32 packed sequences of mixed lengths (64 heads):
+        lengths 2^U(8, 13) rounded (seed 5), q/k/v bf16 N(0, 1), the
+        prefill_b8_h64_t8192 parameter recipe, zero initial state."""
+        torch, kda, synth = self.torch, self.kda, self.synth
+        import numpy as np
+        rng = np.random.default_rng(5)
+        lengths = np.round(2.0 ** rng.uniform(8, 13, 32)).astype(np.int64)
+        total = int(lengths.sum())
+        base = synth.WORKLOADS[PREFILL_WL]
+        wl = synth.shrink(base, B=1, T=total)
+        p = synth.make_params(wl, self.dev)
+        tk = synth.make_tokens(wl, self.dev)
+        H = wl.H
+        Bs = len(lengths)
+        S = torch.zeros((Bs, H, D, D), device=self.dev)
+        cs = torch.zeros((Bs, 3, 3 * H * D), device=self.dev)
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device=self.dev)
+        q, k, v = (tk[n][0].view(torch.int16) for n in ("q", "k", "v"))
+        z, bl, g = tk["z"][0], tk["beta_logit"][0], tk["gate_logit"][0]
+        o = torch.empty((total, H, D), device=self.dev)
+        ctx = kda.kda_create(H, p["conv_w"], p["dt_bias"], p["A_log"], p["gamma"])
+        W = max(3, self.args.warmup)
+        K = max(3, min(self.args.steps, self.args.prefill_steps))
+        for _ in range(W):
+            S.zero_()
+            cs.zero_()
+            kda.kda_prefill_varlen(ctx, Bs, cu, total, q, k, v, z, bl, g, cs, S, o, self.stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        self.barrier_sync()
+        l0 = kda.kda_launch_count()
+        for i in range(K):
+            S.zero_()
+            cs.zero_()
+            ev[i][0].record(self.stream)
+            kda.kda_prefill_varlen(ctx, Bs, cu, total, q, k, v, z, bl, g, cs, S, o, self.stream)
+            ev[i][1].record(self.stream)
+        self.barrier_sync()
+        launches = kda.kda_launch_count() - l0
+        ms = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev))
+        assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
+        kda.kda_destroy(ctx)
+        th = total * H
+        io_bytes = th * (3 * D * 2 + 3 * D * 4 + 4) + Bs * H * (STATE_BYTES + 2 * 9 * D * 4) + H * 7680
+        res = {"sequences": Bs, "H": H, "total_tokens": total, "min_len": int(lengths.min()),
+               "max_len": int(lengths.max()), "ms": ms, "launches": launches,
+               "tokens_s": self.world * total / (ms * 1e-3), "alg_bytes": io_bytes,
+               "alg_gbs": io_bytes / (ms * 1e-3) / 1e9}
+        del tk, S, cs, o
+        torch.cuda.empty_cache()
+        return res
+
+
 # ----------------------------------------------------------------------------- oracle arm
 
 def oracle_decode(budget_s, calls_cap, threads=None):
@@ -468,6 +523,7 @@ def main():
     clocks.start()
     dec = None if args.no_decode else ours.decode()
     pre = None if args.no_prefill else ours.prefill()
+    pvl = None if (args.no_prefill or args.no_decode) else ours.prefill_varlen()
     clk = clocks.stop()
 
     if rank != 0:
@@ -535,6 +591,17 @@ def main():
             line["prefill"]["cpu_baseline"] = {
                 "value": round(cpu_pre["tokens_s"], 3), "unit": "tokens/s",
                 "cores": cpu_pre["threads"], "kind": "oracle", "sample": cpu_pre["sample"]}
+    if pvl is not None:
+        line["prefill_varlen"] = {
+            "workload": "32 packed sequences, lengths 2^U(8,13) (seed 5), H=64, chunk 64",
+            "sequences": pvl["sequences"], "H": pvl["H"], "total_tokens": pvl["total_tokens"],
+            "min_len": pvl["min_len"], "max_len": pvl["max_len"],
+            "value": round(pvl["tokens_s"], 1), "unit": "tokens/s", "ms_per_step": round(pvl["ms"], 4),
+            "gpu_launches": pvl["launches"],
+            "roofline": {"bound": "hbm", "achieved": round(pvl["alg_gbs"], 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(pvl["alg_gbs"] / peaks["hbm_gbs"], 4),
+                         "traffic": None, "alg_bytes_per_launch": pvl["alg_bytes"]},
+        }
     print(json.dumps(line), flush=True)
     if ours.dist is not None:
         ours.dist.destroy_process_group()
