@@ -355,6 +355,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // ---- A1: conv + SiLU per channel over the chunk (from the staged
         //      tiles); decay and its cumulative sum.  Loads of token group
         //      g + 1 are issued before the stores of group g.
+        bool big = false;
         // beta logits of the chunk, consumed after the conv phase.
         const float blog = tid < n ? io.beta_logit[(rowbase + t0 + tid) * H + h] : 0.f;
         wtma.wait();
@@ -448,8 +449,13 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 }
             }
             *reinterpret_cast<f32x2*>((th == 0 ? s_gh0 : s_gh1) + cp) = G;
+            float ga, gb;
+            upk(G, ga, gb);
+            big = -ga > 0.5f * kMaxSpan || -gb > 0.5f * kMaxSpan;   // a half beyond kMaxSpan / 2
         }
-        __syncthreads();
+        // The exact fallback when a chunk's decay may exceed kMaxSpan in some
+        // channel (decided per half of the chunk, so conservatively).
+        const bool fb = __syncthreads_or(big) != 0;
 
         // ---- A2: per-token norms of the conv outputs (4 threads per row, one
         //      per 32-channel block; the 8 lanes of a quarter warp take 8 rows of
@@ -468,8 +474,36 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             if (tid < C)
                 s_beta[tid] = tid < n ? sigmoidf_(blog) : 0.f;
         }
-        // G_last per channel; the exact fallback when a chunk decays by more than kMaxSpan.
-        const bool fb = __syncthreads_or(tid < D && -(s_gh0[tid] + s_gh1[tid]) > kMaxSpan) != 0;
+
+        // ---- D: state pass: S^T operand scaled by e^{rho_L}, master scaled by
+        //      e^{rho_R} (both also by the previous chunk's pending scale).
+        {
+            const float gl = s_gh0[qrow] + s_gh1[qrow];
+            const float eL = esc_prev * (fb ? 1.0f : __expf(0.5f * gl));
+            const float eR = esc_prev * __expf(fb ? gl : 0.5f * gl);
+            // S^T operand element (row j, K = qrow): K block and chunk are fixed per thread.
+            const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
+            const int kch = (qrow >> 2) & 7;
+            {
+                uint32_t v[32];
+                const int j0 = grp * 32;
+                const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
+                tc::ld32(ta, v);
+                tc::wait_ld();
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int j = j0 + g8 * 8 + i;
+                        const float sv = __uint_as_float(v[g8 * 8 + i]);
+                        at<uint32_t>(sm, OFF_ST + kq + j * 128 + ((kch ^ (j & 7)) << 4)) = tc::f2tf32(sv * eL);
+                        v[g8 * 8 + i] = __float_as_uint(sv * eR);
+                    }
+                }
+                tc::st32(ta, v);
+            }
+        }
+        publish();   // norms, beta; S^T operand and rescaled master
 
         // ---- A2b (rare): exact [A'; P] when the chunk decays by more than kMaxSpan.
         if (fb) {
@@ -542,48 +576,17 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         publish();
 
-        // ---- MMA0: [A'; P] = L R^T, issued by thread 0 a quarter (one K block)
-        //      per step of its state pass, so that the issue never waits long.
-        auto mma0_part = [&](int kb) {
+        // ---- MMA0: [A'; P] = L R^T.
+        if (!fb && tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
-#pragma unroll
-            for (int kin = 0; kin < 4; ++kin)
+#pragma unroll 1
+            for (int ks = 0; ks < D / 8; ++ks) {
+                const int kb = ks >> 2, kin = ks & 3;
                 tc::mma_ss(tm + TM_D0, tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)),
-                           tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 8192 + kin * 32)), id, (kb | kin) != 0);
-            if (kb == 3) tc::commit(s_bar);
-        };
-
-        // ---- D: state pass: S^T operand scaled by e^{rho_L}, master scaled by
-        //      e^{rho_R} (both also by the previous chunk's pending scale).
-        {
-            const float gl = s_gh0[qrow] + s_gh1[qrow];
-            const float eL = esc_prev * (fb ? 1.0f : __expf(0.5f * gl));
-            const float eR = esc_prev * __expf(fb ? gl : 0.5f * gl);
-            // S^T operand element (row j, K = qrow): K block and chunk are fixed per thread.
-            const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
-            const int kch = (qrow >> 2) & 7;
-            {
-                uint32_t v[32];
-                const int j0 = grp * 32;
-                const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
-                tc::ld32(ta, v);
-                tc::wait_ld();
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    if (!fb && tid == 0) mma0_part(g8);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int j = j0 + g8 * 8 + i;
-                        const float sv = __uint_as_float(v[g8 * 8 + i]);
-                        at<uint32_t>(sm, OFF_ST + kq + j * 128 + ((kch ^ (j & 7)) << 4)) = tc::f2tf32(sv * eL);
-                        v[g8 * 8 + i] = __float_as_uint(sv * eR);
-                    }
-                }
-                tc::st32(ta, v);
+                           tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 8192 + kin * 32)), id, ks > 0);
             }
+            tc::commit(s_bar);
         }
-        publish();
-        if (!fb) wt.wait();   // MMA0
 
         // ---- MMA1: D1 = L (Diag(e^rho_L) S0) = [K_g S0; Q_g S0] (runs under the
         //      inverse), issued by warp 10 in two halves: K blocks 0, 1 before
@@ -600,6 +603,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             if (half == 1) tc::commit(s_bar1);
         };
         if (tid == kIssuer1) mma1_part(0);
+        if (!fb) wt.wait();   // MMA0
 
         // ---- C1: N = Diag(beta) A' to shared memory as N^T (row b holds
         //      column b of N; 64-row SW128 layout), D0 -> [I; P] in TMEM (row
