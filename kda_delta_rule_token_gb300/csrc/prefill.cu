@@ -209,11 +209,11 @@ struct Maps {
 // Issuing threads.  Issuing a group of MMAs stalls the issuing warp for
 // about the group's execution time, so MMA1 comes from warp 10 (little work
 // in C1 and the inverse's first pass); MMA_T from warp 15 as soon as it has
-// written the last inverse block; the staging copies and the output store
-// from warp 12 (it waits for MMA1 anyway); MMA0 from thread 0 spread over its
-// state pass, MMA2 and MMA3 from thread 0 (warp 0 has no rows in the output
+// written the last inverse block; the staging copies from warp 12 (it waits
+// for MMA1 anyway); the output store from warp 3 (an output-epilogue warp);
+// MMA0, MMA2 and MMA3 from thread 0 (warp 0 has no rows in the output
 // epilogue and skips the gate pass).
-constexpr int kIssuerB = 480, kIssuer1 = 320, kStager = 384;
+constexpr int kIssuerB = 480, kIssuer1 = 320, kStager = 384, kOStore = 96;
 
 // 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and takes column group
 // w / 4 of every TMEM pass; in the thread-per-channel passes the same thread
@@ -834,8 +834,15 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         wt.wait();
 
-        // ---- F: U -> operand of MMA3 (rows 0..63); sum of squares of O_pre
-        //      (rows 64..127).
+        // ---- F and the output epilogue, as two independent groups of 8 warps
+        //      (named barriers): the U rows (lane quadrants 0, 1) write MMA3's
+        //      U operand and thread 0 issues MMA3 as soon as that group is done;
+        //      the O_pre rows (quadrants 2, 3) take their sums of squares, then
+        //      RMSNorm x gamma sigmoid(gate) -> o, written over the gate tile
+        //      and stored by TMA (rows past T clipped by the copy).  The last,
+        //      partial chunk of a packed sequence stores its rows < n directly:
+        //      the rows after it belong to the next sequence.
+        const bool direct = io.cu_seqlens != nullptr && n < C;
         if ((warp & 3) < 2) {
             const int r = qrow;
             const uint32_t kr = (uint32_t)((r >> 5) * 128 * 128 + (r & 3) * 4);
@@ -848,47 +855,37 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 const int j = grp * 32 + jj;
                 at<uint32_t>(sm, OFF_R + kr + j * 128 + ((rch ^ (j & 7)) << 4)) = tc::f2tf32(__uint_as_float(v[jj]));
             }
+            ptx::fence_proxy_async_smem();
+            tc::fence_before();
+            named_barrier_sync(2, 256);   // U operand complete
+            // ---- MMA3 (overlaps the output epilogue): M += R^T U.
+            if (tid == 0) {
+                tc::fence_after();
+                constexpr uint32_t id = tc::idesc_tf32(128, 128);
+#pragma unroll 1
+                for (int ks = 0; ks < C / 8; ++ks) {
+                    const int kb = ks >> 2, kin = ks & 3;
+                    tc::mma_ts(tm + TM_S, tm + TM_RT + ks * 8,
+                               tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 16384 + kin * 32)), id, 1u);
+                }
+                tc::commit(s_bar);
+            }
         } else {
             const int r = qrow - C;
             float ss = 0.f, ss2 = 0.f;
-            uint32_t v[32];
-            tc::ld32(tc::taddr(tm, warp, TM_D1 + grp * 32), v);
-            tc::wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                ss = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss);
-                ss2 = fmaf(__uint_as_float(v[i + 1]), __uint_as_float(v[i + 1]), ss2);
-            }
-            ss += ss2;
-            s_part[grp * C + r] = ss;
-        }
-        publish();   // U operand visible; partial sums visible
-
-        // ---- MMA3 (issued now, overlaps the output epilogue): M += R^T U.
-        if (tid == 0) {
-            constexpr uint32_t id = tc::idesc_tf32(128, 128);
-#pragma unroll 1
-            for (int ks = 0; ks < C / 8; ++ks) {
-                const int kb = ks >> 2, kin = ks & 3;
-                tc::mma_ts(tm + TM_S, tm + TM_RT + ks * 8,
-                           tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 16384 + kin * 32)), id, 1u);
-            }
-            tc::commit(s_bar);
-        }
-        // O_pre -> RMSNorm x gamma sigmoid(gate) -> o (D1 rows 64..127 are not
-        // touched by MMA3), written over the gate tile in shared memory and
-        // stored by TMA (rows past T are clipped by the copy).  The last,
-        // partial chunk of a packed sequence stores its rows < n directly: the
-        // rows after it belong to the next sequence.
-        const bool direct = io.cu_seqlens != nullptr && n < C;
-        if ((warp & 3) >= 2) {
-            const int r = qrow - C;
-            const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
-                                         (1.0f / D) + p.rms_eps);
-            const uint32_t gbase = OFF_OG + grp * 16384 + r * 128;   // row r of box grp (SW128)
             uint32_t w[32];
             tc::ld32(tc::taddr(tm, warp, TM_D1 + grp * 32), w);
             tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                ss = fmaf(__uint_as_float(w[i]), __uint_as_float(w[i]), ss);
+                ss2 = fmaf(__uint_as_float(w[i + 1]), __uint_as_float(w[i + 1]), ss2);
+            }
+            s_part[grp * C + r] = ss + ss2;
+            named_barrier_sync(3, 256);   // the four column groups' partial sums
+            const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
+                                         (1.0f / D) + p.rms_eps);
+            const uint32_t gbase = OFF_OG + grp * 16384 + r * 128;   // row r of box grp (SW128)
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 const uint32_t* v = w + g8 * 8;
@@ -909,16 +906,17 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 }
             }
             ptx::fence_proxy_async_smem();
-        }
-        __syncthreads();
-        if (tid == kStager && !direct) {
+            named_barrier_sync(3, 256);   // the o tile is complete
+            if (tid == kOStore && !direct) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) ptx::tma_store_4d(&maps.o, j * 32, h, tb0 + t0, bmap, sm + OFF_OG + j * 16384);
-            ptx::bulk_commit();
+                for (int j = 0; j < 4; ++j)
+                    ptx::tma_store_4d(&maps.o, j * 32, h, tb0 + t0, bmap, sm + OFF_OG + j * 16384);
+                ptx::bulk_commit();
+            }
         }
-        wt.wait();
+        wt.wait();   // MMA3
         // the next chunk's conv phase overwrites the tile: its reads must be done
-        if (tid == kStager) ptx::bulk_wait_read_all();
+        if (tid == kOStore) ptx::bulk_wait_read_all();
 
         // S_new = e^{G_last - rho_R} M: the scale is carried in a register and
         // applied by the next chunk's state pass (or the final write-back).
@@ -958,7 +956,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
         }
     }
-    if (tid == kStager) ptx::bulk_wait_all();
+    if (tid == kOStore) ptx::bulk_wait_all();
     sync_tc();
     if (warp == 0) tc::dealloc(tm, 512);
 }
