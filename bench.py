@@ -6,7 +6,8 @@ Headline: batched decode, 64 sequences x 32 heads x d=128, one token per call
 head and token, over the device time of one call).  L2 is flushed between
 timed calls (a 256 MiB write, then a 256 MiB read).  The line also carries
 the batched prefill (8 x 64 heads x 8192 tokens, chunk 64, bf16 q/k/v) as
-tokens/s, each with its roofline, an end-to-end figure through the C ABI with
+tokens/s, serving-scale decode (256 x 64 heads, 1 GiB of state) per call and
+replayed as one CUDA graph of 128 calls, each with its roofline, an end-to-end figure through the C ABI with
 host buffers, and the fp64 CPU oracle timed on this host's cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -34,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KDA decode state GB/s (% of HBM peak); prefill tokens/s (% tensor peak)"
 DECODE_WL = "decode_b64_h32_x256"
 PREFILL_WL = "prefill_b8_h64_t8192"
+SERVING_WL = "decode_b256_h64_x128"
 D = 128
 STATE_BYTES = 2 * D * D * 4          # read + write of one 128x128 fp32 state
 FLUSH_BYTES = 256 << 20
@@ -229,13 +231,26 @@ class Ours:
         assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
 
         # End to end through the C ABI with pinned host buffers: copy this
-        # call's inputs in, run, copy o out, all inside the timed region.
+        # call's inputs in, run, copy o out, all inside the timed region.  The
+        # six inputs of a call sit back to back in one pinned host buffer (each
+        # at a 16-byte multiple), so a call is one host-to-device copy, the
+        # decode call on views of the device copy, and one device-to-host copy.
         nh = min(8, wl.T)
-        host = [{n: tk[n][t].to("cpu").pin_memory() for n in
-                 ("q", "k", "v", "z", "beta_logit", "gate_logit")} for t in range(nh)]
-        dbuf = {n: torch.empty_like(tk[n][0]) for n in host[0]}
+        names = ("q", "k", "v", "z", "gate_logit", "beta_logit")
+        sizes = [tk[n][0].numel() for n in names]
+        offs = [0]
+        for n_el in sizes:
+            offs.append(offs[-1] + (n_el + 3) // 4 * 4)
+        host = []
+        for t in range(nh):
+            hb = torch.empty(offs[-1], dtype=torch.float32, pin_memory=True)
+            for n, a, n_el in zip(names, offs, sizes):
+                hb[a:a + n_el].copy_(tk[n][t].reshape(-1))
+            host.append(hb)
+        dpack = torch.empty(offs[-1], dtype=torch.float32, device=self.dev)
+        dv = {n: dpack[a:a + n_el].view(tk[n][0].shape) for n, a, n_el in zip(names, offs, sizes)}
         o_host = torch.empty((B, H, D), pin_memory=True)
-        h2d = sum(x.numel() * x.element_size() for x in host[0].values())
+        h2d = offs[-1] * 4
         d2h = o_host.numel() * 4
         Ke = max(3, min(K, 200))
         eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -244,11 +259,9 @@ class Ours:
             self.flush_l2()
             if i >= W:
                 eve[i - W][0].record(self.stream)
-            hb = host[i % nh]
-            for n in hb:
-                dbuf[n].copy_(hb[n], non_blocking=True)
-            kda.kda_decode_step(ctx, B, dbuf["q"], dbuf["k"], dbuf["v"], dbuf["z"],
-                                dbuf["beta_logit"], dbuf["gate_logit"], cs, S, o, None,
+            dpack.copy_(host[i % nh], non_blocking=True)
+            kda.kda_decode_step(ctx, B, dv["q"], dv["k"], dv["v"], dv["z"],
+                                dv["beta_logit"], dv["gate_logit"], cs, S, o, None,
                                 self.stream)
             o_host.copy_(o, non_blocking=True)
             if i >= W:
@@ -269,6 +282,83 @@ class Ours:
         del tk, S, cs
         torch.cuda.empty_cache()
         return res
+
+    # ---------------------------------------------------------------- serving decode
+    def decode_serving(self):
+        """256 sequences x 64 heads (1 GiB of state, larger than L2: no flush).
+
+        The state is the GPU's own after 32 warm-up tokens (the GPU tests check
+        that warm-up against the oracle).  Timed twice over the workload's 128
+        calls: one launch per call with events around each, and the 128 calls
+        captured once as a CUDA graph and replayed (per-call time = replay
+        time / 128), which removes the host launch path between calls.
+        """
+        torch, kda, synth = self.torch, self.kda, self.synth
+        wl = synth.WORKLOADS[SERVING_WL]
+        p = synth.make_params(wl, self.dev)
+        st = synth.make_state(wl, self.dev)
+        S, cs = st["S"], st["conv_state"]
+        B, H = wl.B, wl.H
+        o = torch.empty((B, H, D), device=self.dev)
+        ctx = kda.kda_create(H, p["conv_w"], p["dt_bias"], p["A_log"], p["gamma"])
+
+        def run(tk, t, stream=None):
+            kda.kda_decode_step(ctx, B, tk["q"][t], tk["k"][t], tk["v"][t], tk["z"][t],
+                                tk["beta_logit"][t], tk["gate_logit"][t], cs, S, o, None,
+                                self.stream if stream is None else stream)
+
+        warm = synth.make_tokens(wl, self.dev, T=wl.warmup_tokens, warm=True)
+        for t in range(wl.warmup_tokens):
+            run(warm, t)
+        del warm
+        tk = synth.make_tokens(wl, self.dev)
+        K, W = min(self.args.steps, 4 * wl.T), max(3, self.args.warmup)
+        for i in range(W):
+            run(tk, i % wl.T)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        self.barrier_sync()
+        l0 = kda.kda_launch_count()
+        for i in range(K):
+            ev[i][0].record(self.stream)
+            run(tk, (W + i) % wl.T)
+            ev[i][1].record(self.stream)
+        self.barrier_sync()
+        launches = kda.kda_launch_count() - l0
+        ms = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev))
+
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=self.dev)
+        side.wait_stream(self.stream)
+        with torch.cuda.graph(g, stream=side):
+            for t in range(wl.T):
+                run(tk, t, torch.cuda.current_stream())
+        self.stream.wait_stream(side)
+        R = 3
+        for _ in range(W):
+            g.replay()
+        evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(R)]
+        self.barrier_sync()
+        for i in range(R):
+            evg[i][0].record(self.stream)
+            g.replay()
+            evg[i][1].record(self.stream)
+        self.barrier_sync()
+        ms_graph = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in evg)) / wl.T
+        assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
+        kda.kda_destroy(ctx)
+        del g, tk, S, cs
+        torch.cuda.empty_cache()
+
+        units = B * H
+        alg_bytes = units * (STATE_BYTES + 5 * D * 4 + 4 + D * 4 + 2 * 9 * D * 4) + H * 7680
+        return {"wl": wl, "ms": ms, "launches": launches, "ms_graph": ms_graph,
+                "graph_launches": R * wl.T, "alg_bytes": alg_bytes,
+                "state_gbs": self.world * units * STATE_BYTES / (ms * 1e-3) / 1e9,
+                "alg_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+                "state_gbs_graph": self.world * units * STATE_BYTES / (ms_graph * 1e-3) / 1e9,
+                "alg_gbs_graph": alg_bytes / (ms_graph * 1e-3) / 1e9}
 
     # ---------------------------------------------------------------- prefill
     def prefill(self):
@@ -311,30 +401,46 @@ class Ours:
         ms = self.max_over_ranks(statistics.fmean(times))
         assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
 
-        # End to end with pinned host buffers (inputs in, o out, per call).
+        # End to end with pinned host buffers (inputs in, o out, per call),
+        # pipelined over groups of sequences: group j's inputs are copied in on
+        # one stream while group j - 1 runs (one kda_prefill call per group, on
+        # the group's slices of the same buffers) and group j - 2's output is
+        # copied out on a third stream.
         names = ("q", "k", "v", "z", "beta_logit", "gate_logit")
         host = {n: tk[n].to("cpu").pin_memory() for n in names}
         o_host = torch.empty((B, T, H, D), pin_memory=True)
         h2d = sum(x.numel() * x.element_size() for x in host.values())
         d2h = o_host.numel() * 4
         dbuf = tk                                       # reuse the device input buffers
+        groups = [(b, min(B, b + max(1, B // 4))) for b in range(0, B, max(1, B // 4))]
+        s_in = torch.cuda.Stream(device=self.dev)
+        s_out = torch.cuda.Stream(device=self.dev)
         Ke = 3
-        eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(Ke)]
+        eve = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+               for _ in range(1 + Ke)]
         for i in range(1 + Ke):
             S.zero_()
             cs.zero_()
-            if i >= 1:
-                eve[i - 1][0].record(self.stream)
-            for n in names:
-                dbuf[n].copy_(host[n], non_blocking=True)
-            kda.kda_prefill(ctx, B, T, dbuf["q"].view(torch.int16), dbuf["k"].view(torch.int16),
-                            dbuf["v"].view(torch.int16), dbuf["z"], dbuf["beta_logit"],
-                            dbuf["gate_logit"], cs, S, o, ws, nws, self.stream)
-            o_host.copy_(o, non_blocking=True)
-            if i >= 1:
-                eve[i - 1][1].record(self.stream)
+            t0 = eve[i][0]
+            t0.record(self.stream)
+            s_in.wait_event(t0)
+            s_out.wait_event(t0)
+            for (b0, b1) in groups:
+                with torch.cuda.stream(s_in):
+                    for n in names:
+                        dbuf[n][b0:b1].copy_(host[n][b0:b1], non_blocking=True)
+                self.stream.wait_stream(s_in)
+                kda.kda_prefill(ctx, b1 - b0, T, dbuf["q"][b0:b1].view(torch.int16),
+                                dbuf["k"][b0:b1].view(torch.int16), dbuf["v"][b0:b1].view(torch.int16),
+                                dbuf["z"][b0:b1], dbuf["beta_logit"][b0:b1], dbuf["gate_logit"][b0:b1],
+                                cs[b0:b1], S[b0:b1], o[b0:b1], ws, nws, self.stream)
+                s_out.wait_stream(self.stream)
+                with torch.cuda.stream(s_out):
+                    o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
+            self.stream.wait_stream(s_out)
+            eve[i][1].record(self.stream)
         self.barrier_sync()
+        eve = eve[1:]                                   # the first pass is the warm-up
         ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
         kda.kda_destroy(ctx)
         th = B * T * H
@@ -510,6 +616,8 @@ def main():
     ap.add_argument("--prefill-workload", default=PREFILL_WL,
                     help="prefill workload of the secondary line (default: the 8x64x8192 one)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-serving", action="store_true",
+                    help="skip the 256 x 64-head (1 GiB state) decode measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup()
@@ -524,6 +632,7 @@ def main():
     dec = None if args.no_decode else ours.decode()
     pre = None if args.no_prefill else ours.prefill()
     pvl = None if (args.no_prefill or args.no_decode) else ours.prefill_varlen()
+    srv = None if (args.no_decode or args.no_serving) else ours.decode_serving()
     clk = clocks.stop()
 
     if rank != 0:
@@ -601,6 +710,23 @@ def main():
             "roofline": {"bound": "hbm", "achieved": round(pvl["alg_gbs"], 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(pvl["alg_gbs"] / peaks["hbm_gbs"], 4),
                          "traffic": None, "alg_bytes_per_launch": pvl["alg_bytes"]},
+        }
+    if srv is not None:
+        sw = srv["wl"]
+        hb = peaks["hbm_gbs"]
+        line["decode_serving"] = {
+            "workload": sw.name, "B": sw.B, "H": sw.H, "d": D, "calls_cycled": sw.T,
+            "state_MiB": sw.B * sw.H * D * D * 4 / 2**20,
+            "l2": "state 1 GiB > L2, no flush", "initial_state": "after 32 warm-up tokens",
+            "ms_per_call": round(srv["ms"], 5), "state_gbs": round(srv["state_gbs"], 1),
+            "gpu_launches": srv["launches"],
+            "roofline": {"bound": "hbm", "achieved": round(srv["alg_gbs"], 1), "peak": hb,
+                         "unit": "GB/s", "frac": round(srv["alg_gbs"] / hb, 4), "traffic": None,
+                         "kernel": "kda_decode_kernel", "alg_bytes_per_launch": srv["alg_bytes"]},
+            "graph": {"calls_per_graph": sw.T, "ms_per_call": round(srv["ms_graph"], 5),
+                      "state_gbs": round(srv["state_gbs_graph"], 1),
+                      "frac": round(srv["alg_gbs_graph"] / hb, 4),
+                      "gpu_launches": srv["graph_launches"]},
         }
     print(json.dumps(line), flush=True)
     if ours.dist is not None:
