@@ -464,11 +464,9 @@ class Ours:
         prefill_b8_h64_t8192 parameter recipe, zero initial state."""
         torch, kda, synth = self.torch, self.kda, self.synth
         import numpy as np
-        rng = np.random.default_rng(5)
-        lengths = np.round(2.0 ** rng.uniform(8, 13, 32)).astype(np.int64)
+        lengths = synth.packed_lengths()
         total = int(lengths.sum())
-        base = synth.WORKLOADS[PREFILL_WL]
-        wl = synth.shrink(base, B=1, T=total)
+        wl = synth.packed_workload(lengths)
         p = synth.make_params(wl, self.dev)
         tk = synth.make_tokens(wl, self.dev)
         H = wl.H

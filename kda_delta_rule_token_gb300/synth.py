@@ -12,6 +12,8 @@ from __future__ import annotations
 
 from dataclasses import dataclass, replace
 
+import numpy as np
+
 import torch
 
 D = 128
@@ -65,6 +67,18 @@ WORKLOADS = {
                                      warmup_tokens=32),
 }
 TINY = WORKLOADS["tiny_decode_b1_h2_t16"]
+
+
+def packed_lengths(n: int = 32, seed: int = 5, lo: float = 8.0, hi: float = 13.0) -> np.ndarray:
+    """Sequence lengths of the packed-sequence prefill workload: round(2^U(lo, hi))."""
+    rng = np.random.default_rng(seed)
+    return np.round(2.0 ** rng.uniform(lo, hi, n)).astype(np.int64)
+
+
+def packed_workload(lengths) -> "Workload":
+    """One token axis of sum(lengths) tokens with the 8 x 64-head prefill recipe
+    (bf16 q/k/v, A_log U(-6, 0)); the caller packs sequences along it."""
+    return replace(WORKLOADS["prefill_b8_h64_t8192"], B=1, T=int(np.sum(lengths)))
 
 
 def shrink(wl: Workload, **kw) -> Workload:

@@ -150,3 +150,30 @@ def test_varlen_long_sequences_sampled():
         assert rel_l2(np64(S[b, h]), ref.S[0, 0]) <= TOL
         assert max_rel_err(pair_window(conv, b, h), ref.conv_state) == 0.0
     assert torch.equal(S[2], S0[2]) and torch.equal(conv[2], c0[2])
+
+
+def test_varlen_bench_workload_sampled():
+    """The packed workload the benchmark times (32 sequences, 80,371 tokens,
+    64 heads, one launch), sampled (sequence, head) pairs vs the oracle: the
+    shortest and the longest sequence, the first and the last."""
+    lengths = synth.packed_lengths()
+    wl = synth.packed_workload(lengths)
+    params = synth.make_params(wl, DEV)
+    tk = synth.make_tokens(wl, DEV)
+    Bs, H, total = len(lengths), wl.H, wl.T
+    S = torch.zeros((Bs, H, 128, 128), device=DEV)
+    conv = torch.zeros((Bs, 3, 3 * H * 128), device=DEV)
+    pk = {n: tk[n][0] for n in tk}
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device=DEV)
+    o = run_varlen(H, params, pk, cu, S, conv)
+    starts = np.concatenate([[0], np.cumsum(lengths)])
+    picks = [(int(np.argmin(lengths)), 5), (int(np.argmax(lengths)), 63), (0, 0), (Bs - 1, 31)]
+    zS = torch.zeros((1, H, 128, 128))
+    zc = torch.zeros((1, 3, 3 * H * 128))
+    for b, h in picks:
+        s, L = int(starts[b]), int(lengths[b])
+        seq = {n: tk[n][:, s:s + L] for n in tk}
+        ref = oracle_pairs(params, seq, zS, zc, [(0, h)], call_major=False)[(0, h)]
+        assert rel_l2(np64(o[s:s + L, h]), ref.o[0, :, 0]) <= TOL, f"seq {b} head {h}"
+        assert rel_l2(np64(S[b, h]), ref.S[0, 0]) <= TOL, f"seq {b} head {h}"
+        assert max_rel_err(pair_window(conv, b, h), ref.conv_state) == 0.0
