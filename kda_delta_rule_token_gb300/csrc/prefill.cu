@@ -66,8 +66,10 @@ constexpr uint32_t OFF_WIN = OFF_SMALL + 4096;   // conv window of a chunk's fir
 constexpr uint32_t kSmemBytes = OFF_WIN + 2 * 4608;
 constexpr uint32_t STG_Q = OFF_ST, STG_K = OFF_ST + 16384, STG_Z = OFF_ST + 32768, STG_V = OFF_MT;
 // Gate tile of the chunk, then its output tile: four 64-row x 32-channel SW128
-// boxes in the Q_g halves of the L operand (free once MMA1 has read them).
-constexpr uint32_t OFF_OG = OFF_L + 8192;
+// boxes in the upper half of the L region (free once MMA1 has read it; the
+// lower half then holds Diag(beta) X, the B operand of MMA2).
+constexpr uint32_t OFF_OG = OFF_L + 32768;
+constexpr uint32_t kOGBox = 8192;
 constexpr uint32_t kStageBytes = 3 * C * D * 2 + C * D * 4;   // 80 KiB per chunk
 
 // TMEM column map (512 columns allocated).
@@ -755,17 +757,17 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             ptx::mbar_arrive_expect_tx(s_gbar, C * D * 4);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                ptx::tma_load_4d(sm + OFF_OG + j * 16384, &maps.g, j * 32, h, tb0 + t0, bmap, s_gbar);
+                ptx::tma_load_4d(sm + OFF_OG + j * kOGBox, &maps.g, j * 32, h, tb0 + t0, bmap, s_gbar);
         }
 
         // ---- E (lane quadrants 0, 1, under the levels): X = V - K_g S0 ->
-        //      Diag(beta) X, the B operand of MMA2 as two N = 64 halves (value
-        //      channels) x 2 K blocks (tokens) in the K_g quarters of L (free
-        //      since MMA1); clear D1 top.
+        //      Diag(beta) X, the B operand of MMA2 (N = 128 value channels x
+        //      2 K blocks of 32 tokens, 16 KiB each) in the lower half of the L
+        //      region (free since MMA1); clear D1 top.
         if ((warp & 3) < 2) {
             const int r = qrow;   // token
             const float br = s_beta[r];
-            const uint32_t kr = OFF_L + (uint32_t)(((grp >> 1) * 2 + (r >> 5)) * 16384 + (grp & 1) * 32 * 128 + (r & 3) * 4);
+            const uint32_t kr = OFF_L + (uint32_t)((r >> 5) * 16384 + grp * 32 * 128 + (r & 3) * 4);
             const int rch = (r >> 2) & 7;
             const uint32_t vrow = OFF_V + r * 128;
             uint32_t v[32];
@@ -803,17 +805,15 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         publish();
 
-        // ---- MMA2: D1 += [Minv; P Minv] Diag(beta) X = [U; P U], as two N = 64 halves.
+        // ---- MMA2: D1 += [Minv; P Minv] Diag(beta) X = [U; P U] (N = 128: a
+        //      tf32 MMA costs about the same per instruction at N = 64 and 128).
         if (tid == 0) {
-            constexpr uint32_t id = tc::idesc_tf32(128, 64);
+            constexpr uint32_t id = tc::idesc_tf32(128, 128);
 #pragma unroll 1
-            for (int hv = 0; hv < 2; ++hv) {
-#pragma unroll 1
-                for (int ks = 0; ks < C / 8; ++ks) {
-                    const int kb = ks >> 2, kin = ks & 3;
-                    tc::mma_ts(tm + TM_D1 + hv * 64, tm + TM_DT + ks * 8,
-                               tc::desc_sw128(ptx::smem_u32(sm + OFF_L + (hv * 2 + kb) * 16384 + kin * 32)), id, 1u);
-                }
+            for (int ks = 0; ks < C / 8; ++ks) {
+                const int kb = ks >> 2, kin = ks & 3;
+                tc::mma_ts(tm + TM_D1, tm + TM_DT + ks * 8,
+                           tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)), id, 1u);
             }
             tc::commit(s_bar);
         }
@@ -826,7 +826,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             gm.x *= 0.5f; gm.y *= 0.5f; gm.z *= 0.5f; gm.w *= 0.5f;   // gamma sigmoid(g) = gm + gm tanh(g / 2)
 #pragma unroll 1
             for (int r = warp - 1; r < C; r += 15) {
-                const uint32_t o = OFF_OG + box * 16384 + r * 128 + ((ch ^ (r & 7)) << 4);
+                const uint32_t o = OFF_OG + box * kOGBox + r * 128 + ((ch ^ (r & 7)) << 4);
                 const float4 gv = at<float4>(sm, o);
                 at<float4>(sm, o) = make_float4(fmaf(gm.x, tanhf_(0.5f * gv.x), gm.x), fmaf(gm.y, tanhf_(0.5f * gv.y), gm.y),
                                                 fmaf(gm.z, tanhf_(0.5f * gv.z), gm.z), fmaf(gm.w, tanhf_(0.5f * gv.w), gm.w));
@@ -885,7 +885,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             named_barrier_sync(3, 256);   // the four column groups' partial sums
             const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
                                          (1.0f / D) + p.rms_eps);
-            const uint32_t gbase = OFF_OG + grp * 16384 + r * 128;   // row r of box grp (SW128)
+            const uint32_t gbase = OFF_OG + grp * kOGBox + r * 128;   // row r of box grp (SW128)
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 const uint32_t* v = w + g8 * 8;
@@ -910,7 +910,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             if (tid == kOStore && !direct) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    ptx::tma_store_4d(&maps.o, j * 32, h, tb0 + t0, bmap, sm + OFF_OG + j * 16384);
+                    ptx::tma_store_4d(&maps.o, j * 32, h, tb0 + t0, bmap, sm + OFF_OG + j * kOGBox);
                 ptx::bulk_commit();
             }
         }
