@@ -127,11 +127,11 @@ __device__ __forceinline__ float tanhf_(float x) {
     return y;
 }
 
-// SiLU of a pair: x sigmoid(x) = h + h tanh(h), h = x / 2 (one MUFU op per
-// element; measured on GB300, tanh.approx.f32 is within 7.8e-6 of tanh over
-// [-20, 20], so SiLU is within 1e-5 absolute).
-__device__ __forceinline__ f32x2 silu2(f32x2 x) {
-    const f32x2 hx = mul2(x, pk(0.5f, 0.5f));
+// SiLU of a pair given h = x / 2: x sigmoid(x) = h + h tanh(h) (one MUFU op
+// per element; measured on GB300, tanh.approx.f32 is within 7.8e-6 of tanh
+// over [-20, 20], so SiLU is within 1e-5 absolute).  The conv produces h
+// directly from halved taps (exact: a power-of-two scale).
+__device__ __forceinline__ f32x2 silu2_of_half(f32x2 hx) {
     float a, b;
     upk(hx, a, b);
     return fma2(hx, pk(tanhf_(a), tanhf_(b)), hx);
@@ -326,7 +326,9 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     if (grp < 3) {
         const float4 a = *reinterpret_cast<const float4*>(p.conv_w + gcp * 4);
         const float4 bq = *reinterpret_cast<const float4*>(p.conv_w + (gcp + 1) * 4);
-        W0 = pk(a.x, bq.x); W1 = pk(a.y, bq.y); W2 = pk(a.z, bq.z); W3 = pk(a.w, bq.w);
+        // taps halved: the conv then yields x / 2, the argument SiLU takes
+        W0 = pk(0.5f * a.x, 0.5f * bq.x); W1 = pk(0.5f * a.y, 0.5f * bq.y);
+        W2 = pk(0.5f * a.z, 0.5f * bq.z); W3 = pk(0.5f * a.w, 0.5f * bq.w);
         if (th == 0) {
 #pragma unroll
             for (int j = 0; j < 3; ++j)
@@ -394,7 +396,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                         pre = fma2(W1, M2, pre);
                         pre = fma2(W2, M1, pre);
                         pre = fma2(W3, x[i], pre);
-                        y[i] = silu2(pre);
+                        y[i] = silu2_of_half(pre);
                         M3 = M2; M2 = M1; M1 = x[i];
                     }
                 } else {
@@ -405,7 +407,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                         pre = fma2(W1, M2, pre);
                         pre = fma2(W2, M1, pre);
                         pre = fma2(W3, x[i], pre);
-                        y[i] = ok ? silu2(pre) : 0ull;
+                        y[i] = ok ? silu2_of_half(pre) : 0ull;
                         if (ok) { M3 = M2; M2 = M1; M1 = x[i]; }
                     }
                 }
