@@ -411,10 +411,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                         if (ok) { M3 = M2; M2 = M1; M1 = x[i]; }
                     }
                 }
+                // row r = r0 + 8 g + i (r & 7 = i): the swizzle only flips address
+                // bits 4..6, which the row base leaves clear, so it is one XOR
+                const uint32_t rb = dst + (uint32_t)(r0 + g * 8) * 128 + (pch << 4);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int r = r0 + g * 8 + i;
-                    at<f32x2>(sm, dst + r * 128 + ((pch ^ (r & 7)) << 4)) = y[i];
+                    at<f32x2>(sm, (rb ^ (uint32_t)(i << 4)) + i * 128) = y[i];
                 }
             }
             if (th == 1) {   // the next chunk's first half starts from this window
@@ -446,10 +448,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                     if (r0 + g * 8 + i < n) G = fma2(nEA, sp, G);
                     gg[i] = G;
                 }
+                const uint32_t rb = OFF_R + kpR + (uint32_t)(r0 + g * 8) * 128 + (pch << 4);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int r = r0 + g * 8 + i;
-                    at<f32x2>(sm, OFF_R + kpR + r * 128 + ((pch ^ (r & 7)) << 4)) = gg[i];
+                    at<f32x2>(sm, (rb ^ (uint32_t)(i << 4)) + i * 128) = gg[i];
                 }
             }
             *reinterpret_cast<f32x2*>((th == 0 ? s_gh0 : s_gh1) + cp) = G;
