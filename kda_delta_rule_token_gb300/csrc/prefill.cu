@@ -28,7 +28,7 @@
 //   MMA0  D0 = L R^T                                  (N = 64,  K = 128)
 //   MMA_T DT = [I; P] Minv          A from TMEM       (N = 64,  K = 64)
 //   MMA1  D1 = L (Diag(e^rho) S0)                     (N = 128, K = 128)
-//   MMA2  D1 += DT (Diag(beta) X)   A from TMEM       (2 x N = 64, K = 64)
+//   MMA2  D1 += DT (Diag(beta) X)   A from TMEM       (N = 128, K = 64)
 //         with D1's top half cleared after X = V - K_g S0 was read, so D1 =
 //         [U; O_pre]
 //   MMA3  M  += R^T U               A from TMEM       (N = 128, K = 64)
