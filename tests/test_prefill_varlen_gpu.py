@@ -177,3 +177,23 @@ def test_varlen_bench_workload_sampled():
         assert rel_l2(np64(o[s:s + L, h]), ref.o[0, :, 0]) <= TOL, f"seq {b} head {h}"
         assert rel_l2(np64(S[b, h]), ref.S[0, 0]) <= TOL, f"seq {b} head {h}"
         assert max_rel_err(pair_window(conv, b, h), ref.conv_state) == 0.0
+
+
+def test_varlen_nonfinite_next_sequence_does_not_leak():
+    """The last chunk of a packed sequence is partial and its tile rows past
+    the end hold the next sequence's tokens; NaN / Inf there must change
+    nothing of the earlier sequence (o, S and window bit for bit)."""
+    lengths = [70, 50]
+    wl, params, tokens, S, conv = _setup(lengths)
+    S2, c2 = S.clone(), conv.clone()
+    pk, cu = packed(tokens, lengths)
+    o_ref = run_varlen(wl.H, params, pk, cu, S, conv)
+    bad = {n: t.clone() for n, t in pk.items()}
+    for n in ("q", "k", "v", "gate_logit", "beta_logit"):
+        bad[n][lengths[0]:] = float("nan")
+    bad["z"][lengths[0]:] = float("inf")
+    o_bad = run_varlen(wl.H, params, bad, cu, S2, c2)
+    L = lengths[0]
+    assert torch.equal(o_bad[:L], o_ref[:L])
+    assert torch.equal(S2[0], S[0])
+    assert torch.equal(c2[0], conv[0])
