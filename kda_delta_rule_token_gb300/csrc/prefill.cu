@@ -757,7 +757,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         wt1.wait();   // MMA1
         if (tid == kStager) {
             if (ci + 1 < nchunks) stage_qkz(ci + 1);   // the S^T region is free now
-            // this chunk's gate tile into the Q_g half of L
+            // this chunk's gate tile into the upper half of the L region
             ptx::mbar_arrive_expect_tx(s_gbar, C * D * 4);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
