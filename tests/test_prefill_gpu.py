@@ -174,3 +174,36 @@ def test_prefill_b8_h64_t8192_sampled():
     pairs = synth.sample_heads(wl, 6)
     ref = oracle_pairs(params, tokens, S0, c0, pairs, call_major=False)
     check(ref, o, S, conv, pairs)
+
+
+def test_graph_replay_equals_launch():
+    """A prefill call captured in a CUDA graph and replayed gives bit for bit
+    what launching it gives (the entry point neither synchronises nor
+    allocates, so it can be captured)."""
+    params, tokens, S, conv = _setup(SMALL)
+    S2, c2 = S.clone(), conv.clone()
+    o_l = gpu_prefill(SMALL, params, tokens, S, conv)
+
+    B, T, H, d = tokens["q"].shape
+    q, k, v = (bits(tokens[n]) for n in ("q", "k", "v"))
+    o_g = torch.full((B, T, H, d), float("nan"), device=DEV)
+    ctx = kda.kda_create(H, params["conv_w"], params["dt_bias"], params["A_log"], params["gamma"])
+    try:
+        nws = kda.kda_prefill_workspace_bytes(ctx, B, T)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=DEV) if nws else None
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=side):
+            kda.kda_prefill(ctx, B, T, q, k, v, tokens["z"], tokens["beta_logit"],
+                            tokens["gate_logit"], c2, S2, o_g, ws, nws,
+                            stream=torch.cuda.current_stream())
+        torch.cuda.current_stream().wait_stream(side)
+        assert bool(torch.isnan(o_g).all())   # the capture itself ran nothing
+        g.replay()
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+    finally:
+        kda.kda_destroy(ctx)
+    assert torch.equal(o_g, o_l)
+    assert torch.equal(S2, S)
+    assert torch.equal(c2, conv)
