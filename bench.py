@@ -232,41 +232,71 @@ class Ours:
 
         # End to end through the C ABI with pinned host buffers: copy this
         # call's inputs in, run, copy o out, all inside the timed region.  The
-        # six inputs of a call sit back to back in one pinned host buffer (each
-        # at a 16-byte multiple), so a call is one host-to-device copy, the
-        # decode call on views of the device copy, and one device-to-host copy.
+        # batch is split into `--e2e-split` groups of sequences; a group's six
+        # inputs sit back to back in one pinned host buffer (each at a 16-byte
+        # multiple), so a group is one host-to-device copy, one decode call on
+        # views of the device copy and one device-to-host copy of its o, on
+        # three streams: group j's inputs arrive while group j - 1 decodes.
         nh = min(8, wl.T)
         names = ("q", "k", "v", "z", "gate_logit", "beta_logit")
-        sizes = [tk[n][0].numel() for n in names]
-        offs = [0]
-        for n_el in sizes:
-            offs.append(offs[-1] + (n_el + 3) // 4 * 4)
+        nsplit = max(1, min(self.args.e2e_split, B))
+        groups = [(B * j // nsplit, B * (j + 1) // nsplit) for j in range(nsplit)]
+        layout = []                                     # (group, name) -> (offset, shape)
+        off = 0
+        for (b0, b1) in groups:
+            ent = {}
+            for n in names:
+                shp = tk[n][0][b0:b1].shape
+                n_el = tk[n][0][b0:b1].numel()
+                ent[n] = (off, n_el, shp)
+                off += (n_el + 3) // 4 * 4
+            layout.append((off, ent))
+        total = off
         host = []
         for t in range(nh):
-            hb = torch.empty(offs[-1], dtype=torch.float32, pin_memory=True)
-            for n, a, n_el in zip(names, offs, sizes):
-                hb[a:a + n_el].copy_(tk[n][t].reshape(-1))
+            hb = torch.empty(total, dtype=torch.float32, pin_memory=True)
+            for (b0, b1), (_, ent) in zip(groups, layout):
+                for n, (a, n_el, _s) in ent.items():
+                    hb[a:a + n_el].copy_(tk[n][t][b0:b1].reshape(-1))
             host.append(hb)
-        dpack = torch.empty(offs[-1], dtype=torch.float32, device=self.dev)
-        dv = {n: dpack[a:a + n_el].view(tk[n][0].shape) for n, a, n_el in zip(names, offs, sizes)}
+        dpack = torch.empty(total, dtype=torch.float32, device=self.dev)
+        seg = []                                        # (start, end) of each group in the pack
+        dv = []
+        start = 0
+        for (end, ent) in layout:
+            seg.append((start, end))
+            dv.append({n: dpack[a:a + n_el].view(shp) for n, (a, n_el, shp) in ent.items()})
+            start = end
         o_host = torch.empty((B, H, D), pin_memory=True)
-        h2d = offs[-1] * 4
+        h2d = total * 4
         d2h = o_host.numel() * 4
+        s_in = torch.cuda.Stream(device=self.dev)
+        s_out = torch.cuda.Stream(device=self.dev)
         Ke = max(3, min(K, 200))
         eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(Ke)]
+               for _ in range(W + Ke)]
         for i in range(W + Ke):
             self.flush_l2()
-            if i >= W:
-                eve[i - W][0].record(self.stream)
-            dpack.copy_(host[i % nh], non_blocking=True)
-            kda.kda_decode_step(ctx, B, dv["q"], dv["k"], dv["v"], dv["z"],
-                                dv["beta_logit"], dv["gate_logit"], cs, S, o, None,
-                                self.stream)
-            o_host.copy_(o, non_blocking=True)
-            if i >= W:
-                eve[i - W][1].record(self.stream)
+            eve[i][0].record(self.stream)
+            s_in.wait_event(eve[i][0])
+            s_out.wait_event(eve[i][0])
+            hb = host[i % nh]
+            for j, (b0, b1) in enumerate(groups):
+                a0, a1 = seg[j]
+                with torch.cuda.stream(s_in):
+                    dpack[a0:a1].copy_(hb[a0:a1], non_blocking=True)
+                self.stream.wait_stream(s_in)
+                g = dv[j]
+                kda.kda_decode_step(ctx, b1 - b0, g["q"], g["k"], g["v"], g["z"],
+                                    g["beta_logit"], g["gate_logit"], cs[b0:b1], S[b0:b1],
+                                    o[b0:b1], None, self.stream)
+                s_out.wait_stream(self.stream)
+                with torch.cuda.stream(s_out):
+                    o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
+            self.stream.wait_stream(s_out)
+            eve[i][1].record(self.stream)
         self.barrier_sync()
+        eve = eve[W:]
         ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
         kda.kda_destroy(ctx)
 
@@ -614,6 +644,8 @@ def main():
     ap.add_argument("--prefill-workload", default=PREFILL_WL,
                     help="prefill workload of the secondary line (default: the 8x64x8192 one)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-split", type=int, default=2,
+                    help="groups of sequences the decode end-to-end step is pipelined over")
     ap.add_argument("--no-serving", action="store_true",
                     help="skip the 256 x 64-head (1 GiB state) decode measurement")
     args = ap.parse_args()
