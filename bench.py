@@ -108,25 +108,32 @@ class ClockSampler:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        text = self.file.read()
         os.unlink(self.file.name)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [x.strip() for x in r]
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, r[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return parse_clocks(text)
+
+
+def parse_clocks(text):
+    """Median SM clock, maximum SM clock and the throttle reasons seen in
+    `nvidia-smi --format=csv,noheader,nounits` lines of ClockSampler.Q
+    (malformed lines are skipped)."""
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.strip().splitlines():
+        r = [x.strip() for x in line.split(",")]
+        if len(r) < 9:
+            continue
+        try:
+            sm.append(float(r[1]))
+            smax.append(float(r[2]))
+        except ValueError:
+            continue
+        for name, val in zip(names, r[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+            "samples": len(sm)}
 
 
 def replica_aggregate(local_ms, units_per_rank, dist=None, device="cpu"):
