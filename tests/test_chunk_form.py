@@ -13,8 +13,10 @@ Per chunk of C tokens with state S0 and per-channel cumulative decay G_t:
     S   = e^{G_last} S0 + (k^ e^{G_last - G})^T U
 
 for any per-channel rho (the kernel takes G_last / 2, or 0 and G_last on its
-exact fallback).  Inputs are the oracle's own conv / norm / decay
-intermediates, so only the recurrence is restated here.
+exact fallback).  The same form split into a state-independent part for all
+chunks (W = Minv Diag(beta) K_g, U' = Minv Diag(beta) V) and a sequential
+state pass (U = U' - W e^{rho} S0) is checked too.  Inputs are the oracle's
+own conv / norm / decay intermediates, so only the recurrence is restated.
 """
 import numpy as np
 import pytest
@@ -57,6 +59,31 @@ def chunk_recurrence(qh, kh, v, gk, beta, S0, C, rho="half"):
     return o, S
 
 
+def chunk_recurrence_wu(qh, kh, v, gk, beta, S0, C):
+    """The same chunk form split into a state-independent part, computable for
+    every chunk at once (W = Minv Diag(beta) K_g, U' = Minv Diag(beta) V, P),
+    and the sequential state pass U = U' - W e^{rho} S0."""
+    T = qh.shape[0]
+    parts = []
+    for t0 in range(0, T, C):                          # independent of the state
+        n = min(C, T - t0)
+        k, q, vv, b = kh[t0:t0 + n], qh[t0:t0 + n], v[t0:t0 + n], beta[t0:t0 + n]
+        G = np.cumsum(gk[t0:t0 + n], axis=0)
+        rho = 0.5 * G[-1]
+        Kg, Qg, Rm = k * np.exp(G - rho), q * np.exp(G - rho), k * np.exp(rho - G)
+        Minv = np.linalg.inv(np.eye(n) + b[:, None] * np.tril(Kg @ Rm.T, -1))
+        parts.append((Minv @ (b[:, None] * Kg), Minv @ (b[:, None] * vv), Qg, np.tril(Qg @ Rm.T),
+                      Rm, G[-1], rho))
+    S = S0.copy()
+    o = np.zeros((T, D))
+    for c, (W, Up, Qg, P, Rm, Gl, rho) in enumerate(parts):   # sequential over chunks
+        S0s = np.exp(rho)[:, None] * S
+        U = Up - W @ S0s
+        o[c * C:c * C + Qg.shape[0]] = Qg @ S0s + P @ U
+        S = np.exp(Gl - rho)[:, None] * (S0s + Rm.T @ U)
+    return o, S
+
+
 def _oracle_case(T, s0_std=0.05, a_log_low=-4.0, seed=2):
     wl = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], B=1, H=2, T=T,
                       s0_std=s0_std, win_std=1.0, seed=seed, a_log_low=a_log_low)
@@ -96,3 +123,12 @@ def test_chunk_form_strong_decay():
             o, S = chunk_recurrence(qh, kh, vc, gk, beta, S0, 64, rho)
             assert np.max(np.abs(o - r.o_pre[0, :, 0])) <= 1e-10 * np.max(np.abs(r.o_pre[0, :, 0]))
             assert np.max(np.abs(S - r.S[0, 0])) <= 1e-10 * np.max(np.abs(r.S[0, 0]))
+
+
+def test_state_independent_split_equals_sequential():
+    """W and U' of every chunk first, the state pass after: same result."""
+    for h, (r, S0) in _oracle_case(T=150).items():
+        o, S = chunk_recurrence_wu(r.qhat[0, :, 0], r.khat[0, :, 0], r.vconv[0, :, 0],
+                                   r.gk[0, :, 0], r.beta[0, :, 0], S0, 64)
+        assert np.max(np.abs(o - r.o_pre[0, :, 0])) <= 1e-11 * np.max(np.abs(r.o_pre[0, :, 0]))
+        assert np.max(np.abs(S - r.S[0, 0])) <= 1e-11 * np.max(np.abs(r.S[0, 0]))
