@@ -82,7 +82,9 @@ typedef struct {
  *   A_log     [H][d]
  *   rms_gamma [H][d]
  * Allocates a few bytes of device memory for the kernel error word on the
- * current device; the context is tied to that device.
+ * current device; the context is tied to that device: a decode or prefill
+ * call made while another device is current returns KDA_ERR_INVALID_ARG
+ * (kda_last_error_detail names both devices) and launches nothing.
  * Returns KDA_OK and *out, or an error with *out left NULL.
  */
 KDA_API kda_status kda_create(const kda_config *cfg, const float *conv_w, const float *dt_bias,

@@ -31,6 +31,21 @@ void set_detail(const char* what, cudaError_t e) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+// A context is tied to the device current at kda_create: its kernels are
+// launched on the current device, with the context's error word, so the two
+// must agree.
+kda_status check_device(const kda_ctx* ctx) {
+    int cur = -1;
+    const cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) { set_detail("cudaGetDevice", e); return KDA_ERR_CUDA; }
+    if (cur != ctx->dev.device) {
+        std::snprintf(g_detail, sizeof(g_detail), "current device %d is not the context's device %d",
+                      cur, ctx->dev.device);
+        return KDA_ERR_INVALID_ARG;
+    }
+    return KDA_OK;
+}
+
 }  // namespace
 
 void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -39,6 +54,7 @@ void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_rela
 
 using kda::aligned16;
 using kda::aligned4;
+using kda::check_device;
 
 extern "C" {
 
@@ -89,7 +105,10 @@ kda_status kda_create(const kda_config* cfg, const float* conv_w, const float* d
         return KDA_ERR_UNSUPPORTED;
     }
     kda_ctx* c = new (std::nothrow) kda_ctx{};
-    if (!c) return KDA_ERR_INVALID_ARG;
+    if (!c) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail), "host allocation of the context failed");
+        return KDA_ERR_INVALID_ARG;
+    }
     c->params = kda::LayerParams{cfg->num_heads, cfg->l2_eps, cfg->rms_eps,
                                  conv_w, dt_bias, A_log, rms_gamma};
     c->chunk = cfg->chunk_size;
@@ -128,6 +147,7 @@ kda_status kda_decode_step(kda_ctx* ctx, int B, const float* q, const float* k, 
     if (!aligned4(beta_logit)) return KDA_ERR_ALIGNMENT;
     if (o_pre && !aligned16(o_pre)) return KDA_ERR_ALIGNMENT;
     if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::DecodeIO io{B, q, k, v, z, beta_logit, gate_logit, conv_state, S, o, o_pre};
     cudaError_t e = kda::launch_decode(ctx->params, io, ctx->dev, ctx->err_word,
                                        static_cast<cudaStream_t>(stream));
@@ -158,6 +178,7 @@ kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint
         if (!workspace || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
         if (!aligned16(workspace)) return KDA_ERR_ALIGNMENT;
     }
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::PrefillIO io{B, T, nullptr, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
                       workspace, workspace_bytes};
     cudaError_t e = kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word,
@@ -179,6 +200,7 @@ kda_status kda_prefill_varlen(kda_ctx* ctx, int B, const int32_t* cu_seqlens, in
         if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
     if (!aligned4(beta_logit) || !aligned4(cu_seqlens)) return KDA_ERR_ALIGNMENT;
     if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::PrefillIO io{B, total_T, cu_seqlens, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
                       nullptr, 0};
     cudaError_t e = kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word,
