@@ -1,14 +1,18 @@
 #!/usr/bin/env python
 """Benchmark of the KDA token step on GB300 (one JSON line on stdout).
 
-Headline: batched decode, 64 sequences x 32 heads x d=128, one token per call
-(fp32 state, 128 MiB), metric = state GB/s (2 * d * d * 4 bytes per sequence,
-head and token, over the device time of one call).  L2 is flushed between
-timed calls (a 256 MiB write, then a 256 MiB read).  The line also carries
-the batched prefill (8 x 64 heads x 8192 tokens, chunk 64, bf16 q/k/v) as
-tokens/s, serving-scale decode (256 x 64 heads, 1 GiB of state) per call and
-replayed as one CUDA graph of 128 calls, each with its roofline, an end-to-end figure through the C ABI with
-host buffers, and the fp64 CPU oracle timed on this host's cores.
+Headline: serving-scale decode, 256 sequences x 64 heads x d=128, one token
+per call (fp32 state, 1 GiB, larger than L2, so calls run back to back),
+starting from the state 32 warm-up tokens leave; metric = state GB/s (2 * d
+* d * 4 bytes per sequence, head and token, over the device time of one
+call).  The same line carries: that workload's 128 calls replayed as one
+CUDA graph; its end-to-end figure through the C ABI with host buffers; the
+batched decode (64 x 32 heads, 128 MiB of state, L2 flushed between timed
+calls by a 256 MiB write and a 256 MiB read); the batched prefill (8 x 64
+heads x 8192 tokens) and the single-sequence prefill (1 x 32 heads x 4096
+tokens), chunk 64, bf16 q/k/v, as tokens/s; the packed variable-length
+prefill; each with its roofline; and the fp64 CPU oracle timed on this
+host's cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -33,9 +37,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "KDA decode state GB/s (% of HBM peak); prefill tokens/s (% tensor peak)"
-DECODE_WL = "decode_b64_h32_x256"
-PREFILL_WL = "prefill_b8_h64_t8192"
-SERVING_WL = "decode_b256_h64_x128"
+HEADLINE_WL = "decode_b256_h64_x128"     # serving-scale decode, 1 GiB of state
+DECODE_WL = "decode_b64_h32_x256"       # batched decode, 128 MiB of state (L2 flushed)
+PREFILL_WL = "prefill_b8_h64_t8192"     # batched prefill
+PREFILL1_WL = "prefill_b1_h32_t4096"    # single-sequence prefill
 D = 128
 STATE_BYTES = 2 * D * D * 4          # read + write of one 128x128 fp32 state
 FLUSH_BYTES = 256 << 20
@@ -199,11 +204,21 @@ class Ours:
         self.torch.sum(self.flush_r, 0, out=self.sink)
 
     # ---------------------------------------------------------------- decode
-    def decode(self):
+    def decode(self, wl_name, flush, graph=False, e2e=True):
+        """Decode calls of one workload, one launch per call, device-timed.
+
+        flush: write and read 256 MiB between timed calls (for workloads whose
+        state fits in L2); otherwise calls run back to back.  Workloads with
+        warm-up tokens start from the state the decode kernel reaches after
+        them (the GPU tests check that warm-up against the oracle).  graph:
+        also time the workload's calls captured once as a CUDA graph and
+        replayed (per-call time = replay time / calls).  e2e: the same calls
+        through the C ABI with the inputs copied in from pinned host memory
+        and o copied out, inside the timed region.
+        """
         torch, kda, synth = self.torch, self.kda, self.synth
-        wl = synth.WORKLOADS[DECODE_WL]
+        wl = synth.WORKLOADS[wl_name]
         p = synth.make_params(wl, self.dev)
-        tk = synth.make_tokens(wl, self.dev)
         st = synth.make_state(wl, self.dev)
         S, cs = st["S"], st["conv_state"]
         B, H = wl.B, wl.H
@@ -211,24 +226,31 @@ class Ours:
         ctx = kda.kda_create(H, p["conv_w"], p["dt_bias"], p["A_log"], p["gamma"])
         K, W = self.args.steps, self.args.warmup
 
-        def step(i, out=o):
-            t = i % wl.T
+        def run(tk, t, out=o, stream=None):
             kda.kda_decode_step(ctx, B, tk["q"][t], tk["k"][t], tk["v"][t], tk["z"][t],
-                                tk["beta_logit"][t], tk["gate_logit"][t], cs, S, out,
-                                None, self.stream)
+                                tk["beta_logit"][t], tk["gate_logit"][t], cs, S, out, None,
+                                self.stream if stream is None else stream)
 
+        if wl.warmup_tokens:
+            warm = synth.make_tokens(wl, self.dev, T=wl.warmup_tokens, warm=True)
+            for t in range(wl.warmup_tokens):
+                run(warm, t)
+            del warm
+        tk = synth.make_tokens(wl, self.dev)
         for i in range(W):
-            self.flush_l2()
-            step(i)
+            if flush:
+                self.flush_l2()
+            run(tk, i % wl.T)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(K)]
         self.barrier_sync()
         l0 = kda.kda_launch_count()
         t_wall = time.perf_counter()
         for i in range(K):
-            self.flush_l2()
+            if flush:
+                self.flush_l2()
             ev[i][0].record(self.stream)
-            step(W + i)
+            run(tk, (W + i) % wl.T)
             ev[i][1].record(self.stream)
         self.barrier_sync()
         t_wall = time.perf_counter() - t_wall
@@ -237,6 +259,31 @@ class Ours:
         ms = self.max_over_ranks(statistics.fmean(times))
         assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
 
+        ms_graph, graph_launches = None, 0
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(device=self.dev)
+            side.wait_stream(self.stream)
+            with torch.cuda.graph(g, stream=side):
+                for t in range(wl.T):
+                    run(tk, t, stream=torch.cuda.current_stream())
+            self.stream.wait_stream(side)
+            R = 3
+            for _ in range(W):
+                g.replay()
+            evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(R)]
+            self.barrier_sync()
+            for i in range(R):
+                evg[i][0].record(self.stream)
+                g.replay()
+                evg[i][1].record(self.stream)
+            self.barrier_sync()
+            ms_graph = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in evg)) / wl.T
+            graph_launches = R * wl.T
+            assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
+            del g
+
         # End to end through the C ABI with pinned host buffers: copy this
         # call's inputs in, run, copy o out, all inside the timed region.  The
         # batch is split into `--e2e-split` groups of sequences; a group's six
@@ -244,67 +291,72 @@ class Ours:
         # multiple), so a group is one host-to-device copy, one decode call on
         # views of the device copy and one device-to-host copy of its o, on
         # three streams: group j's inputs arrive while group j - 1 decodes.
-        nh = min(8, wl.T)
-        names = ("q", "k", "v", "z", "gate_logit", "beta_logit")
-        nsplit = max(1, min(self.args.e2e_split, B))
-        groups = [(B * j // nsplit, B * (j + 1) // nsplit) for j in range(nsplit)]
-        layout = []                                     # (group, name) -> (offset, shape)
-        off = 0
-        for (b0, b1) in groups:
-            ent = {}
-            for n in names:
-                shp = tk[n][0][b0:b1].shape
-                n_el = tk[n][0][b0:b1].numel()
-                ent[n] = (off, n_el, shp)
-                off += (n_el + 3) // 4 * 4
-            layout.append((off, ent))
-        total = off
-        host = []
-        for t in range(nh):
-            hb = torch.empty(total, dtype=torch.float32, pin_memory=True)
-            for (b0, b1), (_, ent) in zip(groups, layout):
-                for n, (a, n_el, _s) in ent.items():
-                    hb[a:a + n_el].copy_(tk[n][t][b0:b1].reshape(-1))
-            host.append(hb)
-        dpack = torch.empty(total, dtype=torch.float32, device=self.dev)
-        seg = []                                        # (start, end) of each group in the pack
-        dv = []
-        start = 0
-        for (end, ent) in layout:
-            seg.append((start, end))
-            dv.append({n: dpack[a:a + n_el].view(shp) for n, (a, n_el, shp) in ent.items()})
-            start = end
-        o_host = torch.empty((B, H, D), pin_memory=True)
-        h2d = total * 4
-        d2h = o_host.numel() * 4
-        s_in = torch.cuda.Stream(device=self.dev)
-        s_out = torch.cuda.Stream(device=self.dev)
-        Ke = max(3, min(K, 200))
-        eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(W + Ke)]
-        for i in range(W + Ke):
-            self.flush_l2()
-            eve[i][0].record(self.stream)
-            s_in.wait_event(eve[i][0])
-            s_out.wait_event(eve[i][0])
-            hb = host[i % nh]
-            for j, (b0, b1) in enumerate(groups):
-                a0, a1 = seg[j]
-                with torch.cuda.stream(s_in):
-                    dpack[a0:a1].copy_(hb[a0:a1], non_blocking=True)
-                self.stream.wait_stream(s_in)
-                g = dv[j]
-                kda.kda_decode_step(ctx, b1 - b0, g["q"], g["k"], g["v"], g["z"],
-                                    g["beta_logit"], g["gate_logit"], cs[b0:b1], S[b0:b1],
-                                    o[b0:b1], None, self.stream)
-                s_out.wait_stream(self.stream)
-                with torch.cuda.stream(s_out):
-                    o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
-            self.stream.wait_stream(s_out)
-            eve[i][1].record(self.stream)
-        self.barrier_sync()
-        eve = eve[W:]
-        ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
+        ms_e2e, h2d, d2h = None, 0, 0
+        if e2e:
+            nh = min(8, wl.T)
+            names = ("q", "k", "v", "z", "gate_logit", "beta_logit")
+            nsplit = max(1, min(self.args.e2e_split, B))
+            groups = [(B * j // nsplit, B * (j + 1) // nsplit) for j in range(nsplit)]
+            layout = []                                     # (group, name) -> (offset, shape)
+            off = 0
+            for (b0, b1) in groups:
+                ent = {}
+                for n in names:
+                    shp = tk[n][0][b0:b1].shape
+                    n_el = tk[n][0][b0:b1].numel()
+                    ent[n] = (off, n_el, shp)
+                    off += (n_el + 3) // 4 * 4
+                layout.append((off, ent))
+            total = off
+            host = []
+            for t in range(nh):
+                hb = torch.empty(total, dtype=torch.float32, pin_memory=True)
+                for (b0, b1), (_, ent) in zip(groups, layout):
+                    for n, (a, n_el, _s) in ent.items():
+                        hb[a:a + n_el].copy_(tk[n][t][b0:b1].reshape(-1))
+                host.append(hb)
+            dpack = torch.empty(total, dtype=torch.float32, device=self.dev)
+            seg = []                                        # (start, end) of each group in the pack
+            dv = []
+            start = 0
+            for (end, ent) in layout:
+                seg.append((start, end))
+                dv.append({n: dpack[a:a + n_el].view(shp) for n, (a, n_el, shp) in ent.items()})
+                start = end
+            o_host = torch.empty((B, H, D), pin_memory=True)
+            h2d = total * 4
+            d2h = o_host.numel() * 4
+            s_in = torch.cuda.Stream(device=self.dev)
+            s_out = torch.cuda.Stream(device=self.dev)
+            Ke = max(3, min(K, 200))
+            eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(W + Ke)]
+            for i in range(W + Ke):
+                if flush:
+                    self.flush_l2()
+                eve[i][0].record(self.stream)
+                s_in.wait_event(eve[i][0])
+                s_out.wait_event(eve[i][0])
+                hb = host[i % nh]
+                for j, (b0, b1) in enumerate(groups):
+                    a0, a1 = seg[j]
+                    with torch.cuda.stream(s_in):
+                        dpack[a0:a1].copy_(hb[a0:a1], non_blocking=True)
+                    self.stream.wait_stream(s_in)
+                    g_ = dv[j]
+                    kda.kda_decode_step(ctx, b1 - b0, g_["q"], g_["k"], g_["v"], g_["z"],
+                                        g_["beta_logit"], g_["gate_logit"], cs[b0:b1], S[b0:b1],
+                                        o[b0:b1], None, self.stream)
+                    s_out.wait_stream(self.stream)
+                    with torch.cuda.stream(s_out):
+                        o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
+                self.stream.wait_stream(s_out)
+                eve[i][1].record(self.stream)
+            self.barrier_sync()
+            eve = eve[W:]
+            ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
+            assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
+            del host, dpack, dv, o_host
         kda.kda_destroy(ctx)
 
         units = B * H                                   # (sequence, head) pairs per call
@@ -313,94 +365,22 @@ class Ours:
             "wl": wl, "ms": ms, "times": times, "launches": launches, "wall": t_wall,
             "state_gbs": self.world * units * STATE_BYTES / (ms * 1e-3) / 1e9,
             "alg_gbs": alg_bytes / (ms * 1e-3) / 1e9, "alg_bytes": alg_bytes,
-            "e2e_gbs": self.world * units * STATE_BYTES / (ms_e2e * 1e-3) / 1e9,
-            "ms_e2e": ms_e2e, "h2d": h2d, "d2h": d2h,
+            "ms_graph": ms_graph, "graph_launches": graph_launches,
         }
+        if ms_graph is not None:
+            res["state_gbs_graph"] = self.world * units * STATE_BYTES / (ms_graph * 1e-3) / 1e9
+            res["alg_gbs_graph"] = alg_bytes / (ms_graph * 1e-3) / 1e9
+        if ms_e2e is not None:
+            res.update({"e2e_gbs": self.world * units * STATE_BYTES / (ms_e2e * 1e-3) / 1e9,
+                        "ms_e2e": ms_e2e, "h2d": h2d, "d2h": d2h})
         del tk, S, cs
         torch.cuda.empty_cache()
         return res
 
-    # ---------------------------------------------------------------- serving decode
-    def decode_serving(self):
-        """256 sequences x 64 heads (1 GiB of state, larger than L2: no flush).
-
-        The state is the GPU's own after 32 warm-up tokens (the GPU tests check
-        that warm-up against the oracle).  Timed twice over the workload's 128
-        calls: one launch per call with events around each, and the 128 calls
-        captured once as a CUDA graph and replayed (per-call time = replay
-        time / 128), which removes the host launch path between calls.
-        """
-        torch, kda, synth = self.torch, self.kda, self.synth
-        wl = synth.WORKLOADS[SERVING_WL]
-        p = synth.make_params(wl, self.dev)
-        st = synth.make_state(wl, self.dev)
-        S, cs = st["S"], st["conv_state"]
-        B, H = wl.B, wl.H
-        o = torch.empty((B, H, D), device=self.dev)
-        ctx = kda.kda_create(H, p["conv_w"], p["dt_bias"], p["A_log"], p["gamma"])
-
-        def run(tk, t, stream=None):
-            kda.kda_decode_step(ctx, B, tk["q"][t], tk["k"][t], tk["v"][t], tk["z"][t],
-                                tk["beta_logit"][t], tk["gate_logit"][t], cs, S, o, None,
-                                self.stream if stream is None else stream)
-
-        warm = synth.make_tokens(wl, self.dev, T=wl.warmup_tokens, warm=True)
-        for t in range(wl.warmup_tokens):
-            run(warm, t)
-        del warm
-        tk = synth.make_tokens(wl, self.dev)
-        K, W = min(self.args.steps, 4 * wl.T), max(3, self.args.warmup)
-        for i in range(W):
-            run(tk, i % wl.T)
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K)]
-        self.barrier_sync()
-        l0 = kda.kda_launch_count()
-        for i in range(K):
-            ev[i][0].record(self.stream)
-            run(tk, (W + i) % wl.T)
-            ev[i][1].record(self.stream)
-        self.barrier_sync()
-        launches = kda.kda_launch_count() - l0
-        ms = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev))
-
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream(device=self.dev)
-        side.wait_stream(self.stream)
-        with torch.cuda.graph(g, stream=side):
-            for t in range(wl.T):
-                run(tk, t, torch.cuda.current_stream())
-        self.stream.wait_stream(side)
-        R = 3
-        for _ in range(W):
-            g.replay()
-        evg = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(R)]
-        self.barrier_sync()
-        for i in range(R):
-            evg[i][0].record(self.stream)
-            g.replay()
-            evg[i][1].record(self.stream)
-        self.barrier_sync()
-        ms_graph = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in evg)) / wl.T
-        assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
-        kda.kda_destroy(ctx)
-        del g, tk, S, cs
-        torch.cuda.empty_cache()
-
-        units = B * H
-        alg_bytes = units * (STATE_BYTES + 5 * D * 4 + 4 + D * 4 + 2 * 9 * D * 4) + H * 7680
-        return {"wl": wl, "ms": ms, "launches": launches, "ms_graph": ms_graph,
-                "graph_launches": R * wl.T, "alg_bytes": alg_bytes,
-                "state_gbs": self.world * units * STATE_BYTES / (ms * 1e-3) / 1e9,
-                "alg_gbs": alg_bytes / (ms * 1e-3) / 1e9,
-                "state_gbs_graph": self.world * units * STATE_BYTES / (ms_graph * 1e-3) / 1e9,
-                "alg_gbs_graph": alg_bytes / (ms_graph * 1e-3) / 1e9}
-
     # ---------------------------------------------------------------- prefill
-    def prefill(self):
+    def prefill(self, wl_name, e2e=True):
         torch, kda, synth = self.torch, self.kda, self.synth
-        wl = synth.WORKLOADS[self.args.prefill_workload]
+        wl = synth.WORKLOADS[wl_name]
         p = synth.make_params(wl, self.dev)
         tk = synth.make_tokens(wl, self.dev)
         st = synth.make_state(wl, self.dev)
@@ -438,58 +418,60 @@ class Ours:
         ms = self.max_over_ranks(statistics.fmean(times))
         assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
 
-        # End to end with pinned host buffers (inputs in, o out, per call),
-        # pipelined over groups of sequences: group j's inputs are copied in on
-        # one stream while group j - 1 runs (one kda_prefill call per group, on
-        # the group's slices of the same buffers) and group j - 2's output is
-        # copied out on a third stream.
-        names = ("q", "k", "v", "z", "beta_logit", "gate_logit")
-        host = {n: tk[n].to("cpu").pin_memory() for n in names}
-        o_host = torch.empty((B, T, H, D), pin_memory=True)
-        h2d = sum(x.numel() * x.element_size() for x in host.values())
-        d2h = o_host.numel() * 4
-        dbuf = tk                                       # reuse the device input buffers
-        groups = [(b, min(B, b + max(1, B // 4))) for b in range(0, B, max(1, B // 4))]
-        s_in = torch.cuda.Stream(device=self.dev)
-        s_out = torch.cuda.Stream(device=self.dev)
-        Ke = 3
-        eve = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-               for _ in range(1 + Ke)]
-        for i in range(1 + Ke):
-            S.zero_()
-            cs.zero_()
-            t0 = eve[i][0]
-            t0.record(self.stream)
-            s_in.wait_event(t0)
-            s_out.wait_event(t0)
-            for (b0, b1) in groups:
-                with torch.cuda.stream(s_in):
-                    for n in names:
-                        dbuf[n][b0:b1].copy_(host[n][b0:b1], non_blocking=True)
-                self.stream.wait_stream(s_in)
-                kda.kda_prefill(ctx, b1 - b0, T, dbuf["q"][b0:b1].view(torch.int16),
-                                dbuf["k"][b0:b1].view(torch.int16), dbuf["v"][b0:b1].view(torch.int16),
-                                dbuf["z"][b0:b1], dbuf["beta_logit"][b0:b1], dbuf["gate_logit"][b0:b1],
-                                cs[b0:b1], S[b0:b1], o[b0:b1], ws, nws, self.stream)
-                s_out.wait_stream(self.stream)
-                with torch.cuda.stream(s_out):
-                    o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
-            self.stream.wait_stream(s_out)
-            eve[i][1].record(self.stream)
-        self.barrier_sync()
-        eve = eve[1:]                                   # the first pass is the warm-up
-        ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
+        ms_e2e, h2d, d2h = None, 0, 0
+        if e2e:
+            # End to end with pinned host buffers (inputs in, o out, per call),
+            # pipelined over groups of sequences: group j's inputs are copied in on
+            # one stream while group j - 1 runs (one kda_prefill call per group, on
+            # the group's slices of the same buffers) and group j - 2's output is
+            # copied out on a third stream.
+            names = ("q", "k", "v", "z", "beta_logit", "gate_logit")
+            host = {n: tk[n].to("cpu").pin_memory() for n in names}
+            o_host = torch.empty((B, T, H, D), pin_memory=True)
+            h2d = sum(x.numel() * x.element_size() for x in host.values())
+            d2h = o_host.numel() * 4
+            dbuf = tk                                       # reuse the device input buffers
+            groups = [(b, min(B, b + max(1, B // 4))) for b in range(0, B, max(1, B // 4))]
+            s_in = torch.cuda.Stream(device=self.dev)
+            s_out = torch.cuda.Stream(device=self.dev)
+            Ke = 3
+            eve = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                   for _ in range(1 + Ke)]
+            for i in range(1 + Ke):
+                S.zero_()
+                cs.zero_()
+                t0 = eve[i][0]
+                t0.record(self.stream)
+                s_in.wait_event(t0)
+                s_out.wait_event(t0)
+                for (b0, b1) in groups:
+                    with torch.cuda.stream(s_in):
+                        for n in names:
+                            dbuf[n][b0:b1].copy_(host[n][b0:b1], non_blocking=True)
+                    self.stream.wait_stream(s_in)
+                    kda.kda_prefill(ctx, b1 - b0, T, dbuf["q"][b0:b1].view(torch.int16),
+                                    dbuf["k"][b0:b1].view(torch.int16), dbuf["v"][b0:b1].view(torch.int16),
+                                    dbuf["z"][b0:b1], dbuf["beta_logit"][b0:b1], dbuf["gate_logit"][b0:b1],
+                                    cs[b0:b1], S[b0:b1], o[b0:b1], ws, nws, self.stream)
+                    s_out.wait_stream(self.stream)
+                    with torch.cuda.stream(s_out):
+                        o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
+                self.stream.wait_stream(s_out)
+                eve[i][1].record(self.stream)
+            self.barrier_sync()
+            eve = eve[1:]                                   # the first pass is the warm-up
+            ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
         kda.kda_destroy(ctx)
         th = B * T * H
         io_bytes = th * (3 * D * 2 + 3 * D * 4 + 4) + B * H * (STATE_BYTES + 2 * 9 * D * 4) \
             + H * 7680
         res = {"wl": wl, "ms": ms, "launches": launches,
                "tokens_s": self.world * B * T / (ms * 1e-3),
-               "e2e_tokens_s": self.world * B * T / (ms_e2e * 1e-3), "ms_e2e": ms_e2e,
-               "h2d": h2d, "d2h": d2h, "alg_bytes": io_bytes,
+               "e2e_tokens_s": None if ms_e2e is None else self.world * B * T / (ms_e2e * 1e-3),
+               "ms_e2e": ms_e2e, "h2d": h2d, "d2h": d2h, "alg_bytes": io_bytes,
                "alg_gbs": io_bytes / (ms * 1e-3) / 1e9,
                "alg_tflops": th * PREFILL_FLOP_PER_TOKEN_HEAD / (ms * 1e-3) / 1e12}
-        del tk, S, cs, o, host, o_host
+        del tk, S, cs, o
         torch.cuda.empty_cache()
         return res
 
@@ -549,18 +531,24 @@ class Ours:
 
 # ----------------------------------------------------------------------------- oracle arm
 
-def oracle_decode(budget_s, calls_cap, threads=None):
-    """Time the fp64 oracle on whole decode calls of the headline workload."""
+def oracle_decode(wl_name, budget_s, calls_cap, pairs=None, threads=None):
+    """Time the fp64 oracle on decode calls of a workload.
+
+    Each call covers the first ``pairs`` (sequence, head) pairs in (b, h)
+    order (all of them when None), so a call is a bounded sample of the
+    workload's call; the inputs of the first calls are cycled.
+    """
     import numpy as np
-    import torch
     from kda_delta_rule_token_gb300 import synth
     import oracle
-    wl = synth.WORKLOADS[DECODE_WL]
+    wl = synth.WORKLOADS[wl_name]
     nthreads = threads or oracle.cpu_count()
-    p = {k: v.numpy().astype(np.float64) for k, v in synth.make_params(wl, "cpu").items()}
-    st = {k: v.numpy().astype(np.float64) for k, v in synth.make_state(wl, "cpu").items()}
-    ncalls = max(1, min(wl.T, calls_cap))
-    tk = synth.make_tokens(wl, "cpu", T=ncalls)
+    Bs = wl.B if pairs is None else max(1, min(wl.B, pairs // wl.H))
+    small = synth.shrink(wl, B=Bs)
+    p = {k: v.numpy().astype(np.float64) for k, v in synth.make_params(small, "cpu").items()}
+    st = {k: v.numpy().astype(np.float64) for k, v in synth.make_state(small, "cpu").items()}
+    ncalls = max(1, min(wl.T, calls_cap, 16))
+    tk = synth.make_tokens(small, "cpu", T=ncalls)
     S, cs = st["S"], st["conv_state"]
     done, elapsed = 0, 0.0
     per_call = []
@@ -576,20 +564,25 @@ def oracle_decode(budget_s, calls_cap, threads=None):
         per_call.append(dt)
         elapsed += dt
         done += 1
-    units = wl.B * wl.H
+    units = Bs * wl.H
     return {"gbs": done * units * STATE_BYTES / elapsed / 1e9, "calls": done,
-            "per_call": per_call, "threads": nthreads,
-            "sample": f"{done} whole decode calls of {wl.B}x{wl.H} heads (all units; the "
-                      f"first {ncalls} calls' inputs, cycled), fp64, {nthreads} threads"}
+            "per_call": per_call, "threads": nthreads, "units": units,
+            "sample": f"{done} decode calls over {Bs} of the {wl.B} sequences x {wl.H} heads "
+                      f"({units} pairs per call; the first {ncalls} calls' inputs cycled), fp64, "
+                      f"{nthreads} threads, state GB/s of the pairs processed"}
 
 
-def oracle_prefill(budget_tokens, heads):
+def oracle_prefill(wl_name, tokens, heads=None):
+    """Time the fp64 oracle on one sequence of ``tokens`` tokens over ``heads``
+    heads of a prefill workload's shape (heads = this host's cores by default,
+    one head per thread); tokens/s is scaled to the workload's head count."""
     import numpy as np
     from kda_delta_rule_token_gb300 import synth
     import oracle
-    wl = synth.WORKLOADS[PREFILL_WL]
+    wl = synth.WORKLOADS[wl_name]
     nthreads = oracle.cpu_count()
-    small = synth.shrink(wl, B=1, H=heads, T=budget_tokens)
+    heads = heads or max(nthreads, 1)
+    small = synth.shrink(wl, B=1, H=heads, T=tokens)
     p = {k: v.numpy().astype(np.float64) for k, v in synth.make_params(small, "cpu").items()}
     tk = {k: v.float().numpy().astype(np.float64) for k, v in
           synth.make_tokens(small, "cpu").items()}
@@ -598,15 +591,20 @@ def oracle_prefill(budget_tokens, heads):
     oracle.run(**tk, conv_w=p["conv_w"], dt_bias=p["dt_bias"], A_log=p["A_log"],
                gamma=p["gamma"], conv_state=st["conv_state"], S=st["S"], nthreads=nthreads)
     dt = time.perf_counter() - t0
-    token_heads = heads * budget_tokens
-    return {"tokens_s": token_heads / wl.H / dt, "threads": min(nthreads, heads),
-            "sample": f"1 sequence x {heads} heads x {budget_tokens} tokens of the "
-                      f"{wl.B}x{wl.H}x{wl.T} prefill shape (fp64 sequential, tokens/s "
-                      f"scaled by {heads}/{wl.H} heads)"}
+    token_heads = heads * tokens
+    return {"tokens_s": token_heads / wl.H / dt, "threads": min(nthreads, heads), "seconds": dt,
+            "sample": f"1 sequence x {heads} heads x {tokens} tokens of the "
+                      f"{wl.B}x{wl.H}x{wl.T} prefill shape (fp64 sequential per head, "
+                      f"{min(nthreads, heads)} threads; tokens/s scaled by {heads}/{wl.H} heads)"}
+
+
+REF_PAIRS = 2048   # (sequence, head) pairs per reference-arm step: a bounded sample of a call
 
 
 def run_reference(args, world, rank):
-    """--impl reference: the fp64 oracle as it stands, on this host's cores."""
+    """--impl reference: the fp64 oracle as it stands, on this host's cores,
+    on the headline workload's decode calls (each step one call over a
+    bounded sample of its (sequence, head) pairs)."""
     if rank != 0:
         return
     import oracle
@@ -614,20 +612,20 @@ def run_reference(args, world, rank):
     W, K = args.warmup, args.steps
     calls = W + K
     from kda_delta_rule_token_gb300 import synth
-    wl = synth.WORKLOADS[DECODE_WL]
-    r = oracle_decode(budget_s=float("inf"), calls_cap=calls)
+    wl = synth.WORKLOADS[HEADLINE_WL]
+    r = oracle_decode(HEADLINE_WL, budget_s=float("inf"), calls_cap=calls, pairs=REF_PAIRS)
     timed = r["per_call"][W:]
     ms = statistics.fmean(timed) * 1e3
-    units = wl.B * wl.H
-    value = units * STATE_BYTES / (ms * 1e-3) / 1e9
+    value = r["units"] * STATE_BYTES / (ms * 1e-3) / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": DECODE_WL, "B": wl.B, "H": wl.H, "d": D,
+        "config": {"workload": HEADLINE_WL, "B": wl.B, "H": wl.H, "d": D,
                    "calls_cycled": wl.T, "state_MiB": wl.B * wl.H * D * D * 4 / 2**20,
-                   "l2": "n/a (CPU)", "parallelism": "rank 0 only"},
+                   "l2": "n/a (CPU)", "parallelism": "rank 0 only",
+                   "pairs_per_step": r["units"]},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": r["threads"],
                          "kind": "oracle", "sample": r["sample"]},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -639,6 +637,65 @@ def run_reference(args, world, rank):
 
 # ----------------------------------------------------------------------------- main
 
+def decode_block(res, peaks, md_name, sha, flush_note):
+    wl = res["wl"]
+    hb = peaks["hbm_gbs"]
+    out = {
+        "workload": wl.name, "B": wl.B, "H": wl.H, "d": D, "calls_cycled": wl.T,
+        "state_MiB": wl.B * wl.H * D * D * 4 / 2**20, "l2": flush_note,
+        "initial_state": f"after {wl.warmup_tokens} warm-up tokens" if wl.warmup_tokens else
+                         "N(0, 0.01) state, N(0, 1) window",
+        "ms_per_call": round(res["ms"], 5), "state_gbs": round(res["state_gbs"], 1),
+        "gpu_launches": res["launches"],
+        "roofline": {"bound": "hbm", "achieved": round(res["alg_gbs"], 1), "peak": hb,
+                     "unit": "GB/s", "frac": round(res["alg_gbs"] / hb, 4),
+                     "traffic": profile_traffic(md_name, sha),
+                     "kernel": "kda_decode_kernel", "peak_src": peaks["src"] + " hbm_gbs",
+                     "alg_bytes_per_launch": res["alg_bytes"]},
+    }
+    if res.get("ms_graph") is not None:
+        out["graph"] = {"calls_per_graph": wl.T, "ms_per_call": round(res["ms_graph"], 5),
+                        "state_gbs": round(res["state_gbs_graph"], 1),
+                        "frac": round(res["alg_gbs_graph"] / hb, 4),
+                        "gpu_launches": res["graph_launches"]}
+    if res.get("ms_e2e") is not None:
+        out["e2e"] = {"value": round(res["e2e_gbs"], 2), "unit": "GB/s",
+                      "ms_per_step": round(res["ms_e2e"], 5),
+                      "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]}
+    return out
+
+
+def prefill_block(pre, peaks, steps, md_name, sha, cpu=None):
+    pw = pre["wl"]
+    tf32_peak = peaks["bf16_tflops"] * 0.5
+    blk = {
+        "workload": pw.name, "B": pw.B, "H": pw.H, "T": pw.T, "chunk": pw.chunk,
+        "value": round(pre["tokens_s"], 1), "unit": "tokens/s",
+        "ms_per_step": round(pre["ms"], 4), "steps": steps,
+        "dtype": "bf16 in, f32 compute/state/out",
+        "l2": f"inputs and output {pre['alg_bytes'] / 1e9:.2f} GB > L2",
+        "gpu_launches": pre["launches"],
+        "roofline": {"bound": "hbm", "achieved": round(pre["alg_gbs"], 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(pre["alg_gbs"] / peaks["hbm_gbs"], 4),
+                     "traffic": profile_traffic(md_name, sha),
+                     "kernel": "kda_prefill_kernel", "peak_src": peaks["src"] + " hbm_gbs",
+                     "alg_bytes_per_launch": pre["alg_bytes"]},
+        "tensor": {"achieved_tflops": round(pre["alg_tflops"], 2),
+                   "pct_of_bf16_peak": round(100 * pre["alg_tflops"] / peaks["bf16_tflops"], 2),
+                   "pct_of_tf32_peak": round(100 * pre["alg_tflops"] / tf32_peak, 2),
+                   "flop_per_token_head": PREFILL_FLOP_PER_TOKEN_HEAD},
+    }
+    if pre.get("ms_e2e") is not None:
+        blk["e2e"] = {"value": round(pre["e2e_tokens_s"], 1), "unit": "tokens/s",
+                      "ms_per_step": round(pre["ms_e2e"], 3),
+                      "h2d_bytes_per_step": pre["h2d"], "d2h_bytes_per_step": pre["d2h"]}
+    if cpu is not None:
+        blk["cpu_baseline"] = {"value": round(cpu["tokens_s"], 3), "unit": "tokens/s",
+                               "cores": cpu["threads"], "kind": "oracle", "sample": cpu["sample"]}
+    return blk
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -647,14 +704,14 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--no-decode", action="store_true", help="skip the decode headline (profiling only)")
-    ap.add_argument("--prefill-workload", default=PREFILL_WL,
-                    help="prefill workload of the secondary line (default: the 8x64x8192 one)")
+    ap.add_argument("--no-decode", action="store_true", help="skip every decode line (profiling only)")
+    ap.add_argument("--prefill-workload", default=None,
+                    help="profiling only: time this prefill workload alone")
+    ap.add_argument("--decode-workload", default=None,
+                    help="profiling only: time this decode workload alone (no e2e, no graph)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-split", type=int, default=2,
                     help="groups of sequences the decode end-to-end step is pipelined over")
-    ap.add_argument("--no-serving", action="store_true",
-                    help="skip the 256 x 64-head (1 GiB state) decode measurement")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup()
@@ -664,79 +721,72 @@ def main():
 
     ours = Ours(args, world, rank, local)
     peaks = load_peaks()
+    if args.prefill_workload or args.decode_workload:   # profiling runs: one workload alone
+        out = {"profiling_only": True}
+        if args.prefill_workload:
+            r = ours.prefill(args.prefill_workload, e2e=False)
+            out.update(prefill_workload=args.prefill_workload, prefill_ms=round(r["ms"], 4))
+        if args.decode_workload:
+            r = ours.decode(args.decode_workload, flush=False, e2e=False)
+            out.update(decode_workload=args.decode_workload, decode_ms=round(r["ms"], 5))
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return
+
     clocks = ClockSampler(local)
     clocks.start()
-    dec = None if args.no_decode else ours.decode()
-    pre = None if args.no_prefill else ours.prefill()
-    pvl = None if (args.no_prefill or args.no_decode) else ours.prefill_varlen()
-    srv = None if (args.no_decode or args.no_serving) else ours.decode_serving()
+    head = None if args.no_decode else ours.decode(HEADLINE_WL, flush=False, graph=True)
+    dec = None if args.no_decode else ours.decode(DECODE_WL, flush=True)
+    psteps = max(3, min(args.steps, args.prefill_steps))
+    pre = None if args.no_prefill else ours.prefill(PREFILL_WL)
+    pre1 = None if args.no_prefill else ours.prefill(PREFILL1_WL, e2e=False)
+    pvl = None if args.no_prefill else ours.prefill_varlen()
     clk = clocks.stop()
 
     if rank != 0:
         return
-    if dec is None:   # profiling run: report the prefill alone
-        print(json.dumps({"profiling_only": True, "prefill_ms": pre and round(pre["ms"], 4),
-                          "prefill_workload": args.prefill_workload}), flush=True)
-        return
-    cpu_dec = None if args.no_cpu_baseline else oracle_decode(budget_s=10.0, calls_cap=100000)
-    cpu_pre = None if (args.no_cpu_baseline or pre is None) else oracle_prefill(256, 4)
+    cpu_head = None if (args.no_cpu_baseline or head is None) else \
+        oracle_decode(HEADLINE_WL, budget_s=10.0, calls_cap=100000, pairs=None)
+    cpu_pre = None if (args.no_cpu_baseline or pre is None) else oracle_prefill(PREFILL_WL, 8192)
+    cpu_pre1 = None if (args.no_cpu_baseline or pre1 is None) else oracle_prefill(PREFILL1_WL, 4096)
 
-    wl = dec["wl"]
     dsha = source_sha("decode.cu")
-    frac = dec["alg_gbs"] / peaks["hbm_gbs"]
-    line = {
-        "metric": METRIC,
-        "value": round(dec["state_gbs"], 2), "unit": "GB/s",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(dec["ms"], 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": DECODE_WL, "B": wl.B, "H": wl.H, "d": D,
-                   "calls_cycled": wl.T, "state_MiB": wl.B * wl.H * D * D * 4 / 2**20,
-                   "l2": "flushed between timed calls (256 MiB write + 256 MiB read)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "state_pct_of_hbm_peak": round(100 * dec["state_gbs"] / world / peaks["hbm_gbs"], 2),
-        "roofline": {"bound": "hbm", "achieved": round(dec["alg_gbs"], 1),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(frac, 4),
-                     "traffic": profile_traffic("decode_b64_h32_kda_decode_kernel.md", dsha),
-                     "kernel": "kda_decode_kernel", "peak_src": peaks["src"] + " hbm_gbs",
-                     "alg_bytes_per_launch": dec["alg_bytes"]},
-        "e2e": {"value": round(dec["e2e_gbs"], 2), "unit": "GB/s",
-                "ms_per_step": round(dec["ms_e2e"], 5),
-                "h2d_bytes_per_step": dec["h2d"], "d2h_bytes_per_step": dec["d2h"]},
-        "gpu_launches": dec["launches"],
-        "clocks": clk,
-    }
-    if cpu_dec is not None:
-        line["cpu_baseline"] = {"value": round(cpu_dec["gbs"], 4), "unit": "GB/s",
-                                "cores": cpu_dec["threads"], "kind": "oracle",
-                                "sample": cpu_dec["sample"]}
+    psha = source_sha("prefill.cu", "ptx.cuh", "tc.cuh")
+    line = {"metric": METRIC}
+    if head is not None:
+        wl = head["wl"]
+        hb = decode_block(head, peaks, "decode_b256_h64_kda_decode_kernel.md", dsha,
+                          "state 1 GiB > L2, calls back to back")
+        line.update({
+            "value": round(head["state_gbs"], 2), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(head["ms"], 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": HEADLINE_WL, "B": wl.B, "H": wl.H, "d": D,
+                       "calls_cycled": wl.T, "state_MiB": wl.B * wl.H * D * D * 4 / 2**20,
+                       "initial_state": hb["initial_state"],
+                       "l2": "inputs larger than L2 (1 GiB of state read and written per call)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "state_pct_of_hbm_peak": round(100 * head["state_gbs"] / world / peaks["hbm_gbs"], 2),
+            "roofline": hb["roofline"],
+            "e2e": hb["e2e"],
+            "gpu_launches": head["launches"],
+            "graph": hb["graph"],
+        })
+    line["clocks"] = clk
+    if cpu_head is not None:
+        line["cpu_baseline"] = {"value": round(cpu_head["gbs"], 4), "unit": "GB/s",
+                                "cores": cpu_head["threads"], "kind": "oracle",
+                                "sample": cpu_head["sample"]}
+    if dec is not None:
+        line["decode_b64_h32"] = decode_block(
+            dec, peaks, "decode_b64_h32_kda_decode_kernel.md", dsha,
+            "state 128 MiB < L2: flushed between timed calls (256 MiB write + 256 MiB read)")
     if pre is not None:
-        pw = pre["wl"]
-        tf32_peak = peaks["bf16_tflops"] * 0.5
-        psha = source_sha("prefill.cu", "ptx.cuh", "tc.cuh")
-        line["prefill"] = {
-            "workload": pw.name, "B": pw.B, "H": pw.H, "T": pw.T, "chunk": pw.chunk,
-            "value": round(pre["tokens_s"], 1), "unit": "tokens/s",
-            "ms_per_step": round(pre["ms"], 4), "steps": max(3, min(args.steps, args.prefill_steps)),
-            "dtype": "bf16 in, f32 compute/state/out", "l2": "inputs 9.7 GB > L2",
-            "gpu_launches": pre["launches"],
-            "roofline": {"bound": "hbm", "achieved": round(pre["alg_gbs"], 1),
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(pre["alg_gbs"] / peaks["hbm_gbs"], 4),
-                         "traffic": profile_traffic("prefill_b8_h64_kernel.md", psha),
-                         "alg_bytes_per_launch": pre["alg_bytes"]},
-            "tensor": {"achieved_tflops": round(pre["alg_tflops"], 2),
-                       "pct_of_bf16_peak": round(100 * pre["alg_tflops"] / peaks["bf16_tflops"], 2),
-                       "pct_of_tf32_peak": round(100 * pre["alg_tflops"] / tf32_peak, 2),
-                       "flop_per_token_head": PREFILL_FLOP_PER_TOKEN_HEAD},
-            "e2e": {"value": round(pre["e2e_tokens_s"], 1), "unit": "tokens/s",
-                    "ms_per_step": round(pre["ms_e2e"], 3),
-                    "h2d_bytes_per_step": pre["h2d"], "d2h_bytes_per_step": pre["d2h"]},
-        }
-        if cpu_pre is not None:
-            line["prefill"]["cpu_baseline"] = {
-                "value": round(cpu_pre["tokens_s"], 3), "unit": "tokens/s",
-                "cores": cpu_pre["threads"], "kind": "oracle", "sample": cpu_pre["sample"]}
+        line["prefill"] = prefill_block(pre, peaks, psteps, "prefill_b8_h64_kernel.md", psha, cpu_pre)
+    if pre1 is not None:
+        line["prefill_single"] = prefill_block(pre1, peaks, psteps, "prefill_b1_h32_kernel.md", psha,
+                                               cpu_pre1)
     if pvl is not None:
         line["prefill_varlen"] = {
             "workload": "32 packed sequences, lengths 2^U(8,13) (seed 5), H=64, chunk 64",
@@ -746,24 +796,8 @@ def main():
             "gpu_launches": pvl["launches"],
             "roofline": {"bound": "hbm", "achieved": round(pvl["alg_gbs"], 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(pvl["alg_gbs"] / peaks["hbm_gbs"], 4),
-                         "traffic": None, "alg_bytes_per_launch": pvl["alg_bytes"]},
-        }
-    if srv is not None:
-        sw = srv["wl"]
-        hb = peaks["hbm_gbs"]
-        line["decode_serving"] = {
-            "workload": sw.name, "B": sw.B, "H": sw.H, "d": D, "calls_cycled": sw.T,
-            "state_MiB": sw.B * sw.H * D * D * 4 / 2**20,
-            "l2": "state 1 GiB > L2, no flush", "initial_state": "after 32 warm-up tokens",
-            "ms_per_call": round(srv["ms"], 5), "state_gbs": round(srv["state_gbs"], 1),
-            "gpu_launches": srv["launches"],
-            "roofline": {"bound": "hbm", "achieved": round(srv["alg_gbs"], 1), "peak": hb,
-                         "unit": "GB/s", "frac": round(srv["alg_gbs"] / hb, 4), "traffic": None,
-                         "kernel": "kda_decode_kernel", "alg_bytes_per_launch": srv["alg_bytes"]},
-            "graph": {"calls_per_graph": sw.T, "ms_per_call": round(srv["ms_graph"], 5),
-                      "state_gbs": round(srv["state_gbs_graph"], 1),
-                      "frac": round(srv["alg_gbs_graph"] / hb, 4),
-                      "gpu_launches": srv["graph_launches"]},
+                         "traffic": None, "kernel": "kda_prefill_kernel",
+                         "alg_bytes_per_launch": pvl["alg_bytes"]},
         }
     print(json.dumps(line), flush=True)
     if ours.dist is not None:

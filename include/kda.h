@@ -36,6 +36,19 @@
  *  - Errors come back as a kda_status; there is no CPU fallback.  Argument
  *    errors are detected on the host before any launch.
  *  - One kda_ctx may be used from one host thread at a time.
+ *  - Every wait inside a kernel is bounded (1 s of wall time).  A kernel that
+ *    gives up stops issuing copies and tensor-core operations, waits (again
+ *    bounded) for the ones it already issued, records the failure in the
+ *    context's error word and returns; kda_sync_status then reports
+ *    KDA_ERR_TIMEOUT.  What the affected (sequence, head) pairs hold afterwards
+ *    is stated per call below.  A wait that gives up means the device did not
+ *    complete a copy within a second, so later results on that device deserve
+ *    the same suspicion.
+ *  - Host-side fault injection for tests: the environment variable
+ *    KDA_FAULT_INJECT, read by kda_create, names entry points ("decode",
+ *    "prefill", "prefill_varlen", "all"; comma-separated) whose launches that
+ *    context replaces by cudaErrorLaunchFailure: nothing is launched, no
+ *    buffer changes, and the call returns KDA_ERR_CUDA.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -114,6 +127,9 @@ KDA_API const char *kda_last_error_detail(void);
  *   o            [B][H][d] fp32  gated, normalised output (out)
  *   o_pre        [B][H][d] fp32  S^T q^ before RMSNorm (out), or NULL
  * B == 0 is a no-op returning KDA_OK.  Outputs must not alias inputs.
+ * After a give-up (KDA_ERR_TIMEOUT from kda_sync_status) the affected pairs
+ * keep their old S and window and their o / o_pre are not written; the other
+ * pairs of the call are computed normally.
  */
 KDA_API kda_status kda_decode_step(kda_ctx *ctx, int B,
                            const float *q, const float *k, const float *v,
@@ -142,6 +158,10 @@ KDA_API size_t kda_prefill_workspace_bytes(const kda_ctx *ctx, int B, int T);
  *   workspace    device buffer of at least kda_prefill_workspace_bytes(ctx,B,T)
  *                bytes (may be NULL when that is 0); workspace_bytes is its size
  * B == 0 or T == 0 is a no-op returning KDA_OK.
+ * After a give-up (KDA_ERR_TIMEOUT from kda_sync_status) an affected pair
+ * stops at the end of a chunk and keeps its old S and window; the o rows of
+ * its chunks from the one that gave up onwards are not written (earlier rows
+ * hold their results), so its o is incomplete.
  */
 KDA_API kda_status kda_prefill(kda_ctx *ctx, int B, int T,
                        const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -172,7 +192,7 @@ KDA_API kda_status kda_prefill(kda_ctx *ctx, int B, int T,
  * length 0 leaves its state and window unchanged; B == 0 or total_T == 0 is a
  * no-op returning KDA_OK.  Needs no workspace.  Sequences are isolated: no
  * value of one sequence's inputs, not even a NaN or an infinity, changes
- * another sequence's o, S or window.
+ * another sequence's o, S or window.  Give-ups behave as for kda_prefill.
  */
 KDA_API kda_status kda_prefill_varlen(kda_ctx *ctx, int B, const int32_t *cu_seqlens, int total_T,
                        const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -182,7 +202,8 @@ KDA_API kda_status kda_prefill_varlen(kda_ctx *ctx, int B, const int32_t *cu_seq
 /*
  * Synchronise `stream` and report whether any kernel launched with this
  * context since the last call gave up on a bounded wait (KDA_ERR_TIMEOUT) or
- * raised a CUDA error (KDA_ERR_CUDA).  Clears the error word.
+ * raised a CUDA error (KDA_ERR_CUDA).  Clears the error word, so the next
+ * call reports only what happened after this one.
  */
 KDA_API kda_status kda_sync_status(kda_ctx *ctx, void *stream);
 

@@ -81,6 +81,8 @@ def load(path: str | None = None):
     lib.kda_sync_status.restype = i32
     lib.kda_launch_count.argtypes = []
     lib.kda_launch_count.restype = u64
+    lib.kda_testing_bounded_wait.argtypes = [vp, ctypes.c_uint, vp]
+    lib.kda_testing_bounded_wait.restype = i32
     _lib = lib
     return lib
 
@@ -166,3 +168,11 @@ def kda_prefill_varlen(ctx, B, cu_seqlens, total_T, q, k, v, z, beta_logit, gate
 def kda_sync_status(ctx, stream=None) -> int:
     """Synchronise and return the status code (does not raise)."""
     return int(load().kda_sync_status(ctx, _stream(stream)))
+
+
+def kda_testing_bounded_wait(ctx, limit_us, stream=None) -> None:
+    """Test hook (not part of the public API): launch a kernel whose bounded
+    wait runs out after ``limit_us`` microseconds; the next kda_sync_status
+    reports KDA_ERR_TIMEOUT."""
+    _check(load().kda_testing_bounded_wait(ctx, int(limit_us), _stream(stream)),
+           "kda_testing_bounded_wait")

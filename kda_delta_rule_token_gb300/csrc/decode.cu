@@ -20,6 +20,8 @@
 //    in-thread adds plus one 8-way shared-memory reduction;
 //  * o_pre = S_new^T q = p + (q^.k^) delta with delta = beta (v - u): the
 //    read-out needs no extra pass over the state.
+#include <atomic>
+
 #include "kda_internal.cuh"
 #include "ptx.cuh"
 
@@ -77,12 +79,17 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     }
 
     // 2. While it is in flight: conv4 + SiLU on the 3*d channels of q, k, v
-    //    (shifting the window) and the per-channel decay a = exp(gk),
-    //    gk = -exp(A_log) softplus(z + dt_bias).
+    //    and the per-channel decay a = exp(gk), gk = -exp(A_log) softplus(z +
+    //    dt_bias).  The shifted window is held in registers and written back
+    //    only once the state load is known to have landed (step 5).
     const size_t HD = (size_t)p.H * D;
     const size_t HD3 = 3 * HD;
     float* win = io.conv_state + (size_t)b * 3 * HD3;
-    for (int ch = tid; ch < 4 * D; ch += kThreads) {
+    float wnew[2][3];          // (m2, m1, x_t) of this thread's conv channels
+    size_t wgc[2] = {0, 0};
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int ch = tid + it * kThreads;
         if (ch < 3 * D) {
             const int tensor = ch >> 7;
             const int c = ch & (D - 1);
@@ -94,9 +101,8 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
             const float m2 = win[HD3 + gc];
             const float m1 = win[2 * HD3 + gc];
             const float pre = fmaf(w.w, xt, fmaf(w.z, m1, fmaf(w.y, m2, w.x * m3)));
-            win[gc] = m2;
-            win[HD3 + gc] = m1;
-            win[2 * HD3 + gc] = xt;
+            wgc[it] = gc;
+            wnew[it][0] = m2; wnew[it][1] = m1; wnew[it][2] = xt;
             (tensor == 0 ? s_q : (tensor == 1 ? s_k : s_v))[c] = pre / (1.0f + expf(-pre));
         } else {
             const int c = ch - 3 * D;
@@ -124,6 +130,9 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     const float qk = s_scal[2] * rq * rk;
     const float beta = s_scal[3];
 
+    // Every thread waits (bounded) for the state load; a thread that gives up
+    // records the error bit.  Whether the whole CTA saw the load land is
+    // decided at the next barrier (all_ok).
     const bool ok = ptx::mbar_wait(&s_bar, 0, err, ptx::kErrDecodeLoadWait);
 
     // 4. Pass 1: partial u = S'^T k and p = S'^T q over this warp's rows
@@ -143,7 +152,23 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     }
     reinterpret_cast<float4*>(s_red_u[warp])[lane] = u;
     reinterpret_cast<float4*>(s_red_p[warp])[lane] = pr;
-    __syncthreads();
+    const bool all_ok = __syncthreads_and(ok) != 0;
+    if (!all_ok) {
+        // Give-up path: nothing of this (sequence, head) is written (window,
+        // o, o_pre and S keep their old contents); wait once more, bounded,
+        // for the state load so that no copy into this CTA's shared memory is
+        // left in flight when it exits.
+        if (tid == 0) ptx::mbar_wait_timed(&s_bar, 0);
+        return;
+    }
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        if (tid + it * kThreads < 3 * D) {
+            win[wgc[it]] = wnew[it][0];
+            win[HD3 + wgc[it]] = wnew[it][1];
+            win[2 * HD3 + wgc[it]] = wnew[it][2];
+        }
+    }
 
     // 5. Column totals, delta = beta (v - u), o_pre = p + (q^.k^) delta.
     float opre = 0.0f;
@@ -177,7 +202,7 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     }
     ptx::fence_proxy_async_smem();
     __syncthreads();
-    if (tid == 0 && ok) {
+    if (tid == 0) {
         ptx::bulk_s2g(Sg, sS, kStateBytes);
         ptx::bulk_commit();
     }
@@ -191,10 +216,12 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
         io.o[(size_t)bh * D + j] = p.gamma[h * D + j] * opre * inv * g;
     }
     // The CTA's shared memory must outlive the bulk store's reads of it.
-    if (tid == 0 && ok) ptx::bulk_wait_read_all();
+    if (tid == 0) ptx::bulk_wait_read_all();
 }
 
-bool g_attr_done[64] = {};
+// Per-device flag: the kernel's attributes are set (the calls are
+// idempotent, so two host threads setting them at once is harmless).
+std::atomic<bool> g_attr_done[64];
 
 }  // namespace
 
@@ -202,14 +229,14 @@ cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const Device
                           int* err_word, cudaStream_t stream) {
     const long long grid = (long long)io.B * p.H;
     if (grid <= 0) return cudaSuccess;
-    if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device]) {
+    if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kda_decode_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kda_decode_kernel,
                                  cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
-        if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device] = true;
+        if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device].store(true, std::memory_order_release);
     }
     kda_decode_kernel<<<(unsigned)grid, kThreads, kDynSmem, stream>>>(p, io, err_word);
     count_launches(1);

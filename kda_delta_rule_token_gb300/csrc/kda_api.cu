@@ -1,6 +1,13 @@
 // Host side of the C ABI declared in include/kda.h: argument validation,
 // device checks, launch and error reporting.  No allocation happens on the
 // per-call path; kda_create allocates the 16-byte kernel error word.
+//
+// Host-side fault injection: KDA_FAULT_INJECT, read once by kda_create, is a
+// comma-separated list of entry points ("decode", "prefill",
+// "prefill_varlen", or "all") whose launches that context replaces by the
+// error cudaErrorLaunchFailure: nothing is launched, no buffer is touched and
+// the call returns KDA_ERR_CUDA (kda_last_error_detail names the error and
+// says it was injected).  Unset or empty: no injection.
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -9,12 +16,14 @@
 #include <new>
 
 #include "kda_internal.cuh"
+#include "kda_testing.h"
 
 struct kda_ctx {
     kda::LayerParams params;
     int chunk;
     kda::DeviceInfo dev;
-    int* err_word;  // device int: nonzero after a kernel gave up on a bounded wait
+    int* err_word;    // device int: nonzero after a kernel gave up on a bounded wait
+    unsigned inject;  // launches replaced by an injected failure (KDA_FAULT_INJECT)
 };
 
 namespace kda {
@@ -44,6 +53,43 @@ kda_status check_device(const kda_ctx* ctx) {
         return KDA_ERR_INVALID_ARG;
     }
     return KDA_OK;
+}
+
+constexpr unsigned kInjectDecode = 1u, kInjectPrefill = 2u, kInjectVarlen = 4u;
+
+// Parse KDA_FAULT_INJECT (see the top of this file).
+unsigned parse_inject(const char* v) {
+    if (!v) return 0u;
+    unsigned m = 0u;
+    const char* p = v;
+    while (*p) {
+        const char* e = p;
+        while (*e && *e != ',') ++e;
+        const size_t n = (size_t)(e - p);
+        auto is = [&](const char* w) { return std::strlen(w) == n && std::strncmp(p, w, n) == 0; };
+        if (is("decode")) m |= kInjectDecode;
+        else if (is("prefill")) m |= kInjectPrefill;
+        else if (is("prefill_varlen")) m |= kInjectVarlen;
+        else if (is("all")) m |= kInjectDecode | kInjectPrefill | kInjectVarlen;
+        p = *e ? e + 1 : e;
+    }
+    return m;
+}
+
+// The launch itself, or the injected failure in its place.
+template <typename F>
+cudaError_t launch_or_inject(const kda_ctx* ctx, unsigned what, F&& launch) {
+    if (ctx->inject & what) return cudaErrorLaunchFailure;
+    return launch();
+}
+
+void set_launch_detail(const kda_ctx* ctx, unsigned what, const char* name, cudaError_t e) {
+    if (ctx->inject & what) {
+        std::snprintf(g_detail, sizeof(g_detail), "%s: %s (injected by KDA_FAULT_INJECT; nothing launched)",
+                      name, cudaGetErrorName(e));
+    } else {
+        set_detail(name, e);
+    }
 }
 
 }  // namespace
@@ -113,6 +159,7 @@ kda_status kda_create(const kda_config* cfg, const float* conv_w, const float* d
                                  conv_w, dt_bias, A_log, rms_gamma};
     c->chunk = cfg->chunk_size;
     c->dev = dev;
+    c->inject = kda::parse_inject(std::getenv("KDA_FAULT_INJECT"));
     if ((e = cudaMalloc(&c->err_word, 16)) != cudaSuccess) {
         kda::set_detail("cudaMalloc(error word)", e);
         delete c;
@@ -149,9 +196,10 @@ kda_status kda_decode_step(kda_ctx* ctx, int B, const float* q, const float* k, 
     if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::DecodeIO io{B, q, k, v, z, beta_logit, gate_logit, conv_state, S, o, o_pre};
-    cudaError_t e = kda::launch_decode(ctx->params, io, ctx->dev, ctx->err_word,
-                                       static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) { kda::set_detail("decode launch", e); return KDA_ERR_CUDA; }
+    cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectDecode, [&] {
+        return kda::launch_decode(ctx->params, io, ctx->dev, ctx->err_word, static_cast<cudaStream_t>(stream));
+    });
+    if (e != cudaSuccess) { kda::set_launch_detail(ctx, kda::kInjectDecode, "decode launch", e); return KDA_ERR_CUDA; }
     return KDA_OK;
 }
 
@@ -181,9 +229,10 @@ kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint
     if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::PrefillIO io{B, T, nullptr, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
                       workspace, workspace_bytes};
-    cudaError_t e = kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word,
-                                        static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) { kda::set_detail("prefill launch", e); return KDA_ERR_CUDA; }
+    cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectPrefill, [&] {
+        return kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word, static_cast<cudaStream_t>(stream));
+    });
+    if (e != cudaSuccess) { kda::set_launch_detail(ctx, kda::kInjectPrefill, "prefill launch", e); return KDA_ERR_CUDA; }
     return KDA_OK;
 }
 
@@ -203,9 +252,10 @@ kda_status kda_prefill_varlen(kda_ctx* ctx, int B, const int32_t* cu_seqlens, in
     if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::PrefillIO io{B, total_T, cu_seqlens, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
                       nullptr, 0};
-    cudaError_t e = kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word,
-                                        static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) { kda::set_detail("prefill_varlen launch", e); return KDA_ERR_CUDA; }
+    cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectVarlen, [&] {
+        return kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word, static_cast<cudaStream_t>(stream));
+    });
+    if (e != cudaSuccess) { kda::set_launch_detail(ctx, kda::kInjectVarlen, "prefill_varlen launch", e); return KDA_ERR_CUDA; }
     return KDA_OK;
 }
 
@@ -227,6 +277,14 @@ kda_status kda_sync_status(kda_ctx* ctx, void* stream) {
         }
         return KDA_ERR_TIMEOUT;
     }
+    return KDA_OK;
+}
+
+kda_status kda_testing_bounded_wait(kda_ctx* ctx, unsigned limit_us, void* stream) {
+    if (!ctx || limit_us < 1 || limit_us > 1000000) return KDA_ERR_INVALID_ARG;
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
+    cudaError_t e = kda::launch_testing_wait(ctx->err_word, 1000ull * limit_us, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { kda::set_detail("testing wait launch", e); return KDA_ERR_CUDA; }
     return KDA_OK;
 }
 

@@ -70,6 +70,9 @@ size_t prefill_workspace_bytes(int H, int B, int T);
 cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const DeviceInfo& dev,
                            int* err_word, cudaStream_t stream);
 
+// Test hook (csrc/testing.cu): a kernel whose bounded wait runs out.
+cudaError_t launch_testing_wait(int* err_word, unsigned long long limit_ns, cudaStream_t stream);
+
 // Counts kernel launches made by the library (for benchmark accounting).
 void count_launches(uint64_t n);
 

@@ -39,6 +39,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "kda_internal.cuh"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -235,8 +237,11 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     uint64_t* s_gbar = s_bar + 2;                                 // gate tile landed
     uint64_t* s_tbarT = s_bar + 3;                                // MMA_T done
     uint64_t* s_bar1 = s_bar + 4;                                 // MMA1 done
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 5);
+    uint64_t* s_drain = s_bar + 5;                                // give-up path: MMA issuers drained
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 6);
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
+    int* s_nt = s_dead + 1;                                       // input-tile phases issued
+    int* s_ng = s_dead + 2;                                       // gate-tile phases issued
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x;
@@ -268,8 +273,11 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     // back as zeros).  q, k, z land in the S^T operand region and may be
     // issued once MMA1 has read it; v lands in the Minv^T region and may be
     // issued once MMA_T has read it.  One barrier phase covers all four.
+    // After a bounded wait gave up (*s_dead), no new copy or MMA is issued.
+    auto alive = [&]() { return *(volatile int*)s_dead == 0; };
     auto stage_qkz = [&](int ci) {
-        if (tid == kStager) {
+        if (tid == kStager && alive()) {
+            ++*s_nt;
             ptx::mbar_arrive_expect_tx(s_tbar, kStageBytes);
             ptx::tma_load_4d(sm + STG_Q, &maps.q, 0, h, tb0 + ci * C, bmap, s_tbar);
             ptx::tma_load_4d(sm + STG_K, &maps.k, 0, h, tb0 + ci * C, bmap, s_tbar);
@@ -277,8 +285,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             ptx::tma_prefetch_4d(&maps.v, 0, h, tb0 + ci * C, bmap);   // v lands later; have it in L2
         }
     };
+    // v joins the phase stage_qkz opened for the same chunk, and only if that
+    // phase was opened (for ci > 0 a block barrier separates the two issues,
+    // so the count written by the stager is visible here).
     auto stage_v = [&](int ci) {
-        if (tid == 0) ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, tb0 + ci * C, bmap, s_tbar);
+        if (tid == 0 && alive() && (ci == 0 || *(volatile int*)s_nt == ci + 1))
+            ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, tb0 + ci * C, bmap, s_tbar);
     };
     if (tid == 0) {
         ptx::mbar_init(s_bar, 1);
@@ -286,8 +298,11 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         ptx::mbar_init(s_gbar, 1);
         ptx::mbar_init(s_tbarT, 1);
         ptx::mbar_init(s_bar1, 1);
+        ptx::mbar_init(s_drain, 3);
         ptx::fence_mbar_init();
         *s_dead = 0;
+        *s_nt = 0;
+        *s_ng = 0;
     }
     sync_tc();
     const uint32_t tm = *s_tmem;
@@ -583,7 +598,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         publish();
 
         // ---- MMA0: [A'; P] = L R^T.
-        if (!fb && tid == 0) {
+        if (!fb && tid == 0 && alive()) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll 1
             for (int ks = 0; ks < D / 8; ++ks) {
@@ -608,7 +623,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             if (half == 1) tc::commit(s_bar1);
         };
-        if (tid == kIssuer1) mma1_part(0);
+        if (tid == kIssuer1 && alive()) mma1_part(0);
         if (!fb) wt.wait();   // MMA0
 
         // ---- C1: N = Diag(beta) A' to shared memory as N^T (row b holds
@@ -638,7 +653,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         tc::wait_st();
         sync_tc();
 
-        if (tid == kIssuer1) mma1_part(1);
+        if (tid == kIssuer1 && alive()) mma1_part(1);
 
         // ---- C2: Minv = (I + N)^{-1} (N strictly lower) by 16 x 16 blocks.
         //      Pass 1: forward substitution with the diagonal block I + N_II
@@ -741,7 +756,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 }
                 // ---- MMA_T: [Minv; P Minv] = [I; P] Minv, issued by the warp that
                 //      wrote the last block (runs under the rest of the X epilogue).
-                if (tid == kIssuerB) {
+                if (tid == kIssuerB && alive()) {
                     tc::fence_after();
                     constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll 1
@@ -757,7 +772,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         wt1.wait();   // MMA1
         if (tid == kStager) {
             if (ci + 1 < nchunks) stage_qkz(ci + 1);   // the S^T region is free now
+        }
+        if (tid == kStager && alive()) {
             // this chunk's gate tile into the upper half of the L region
+            ++*s_ng;
             ptx::mbar_arrive_expect_tx(s_gbar, C * D * 4);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -811,7 +829,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
 
         // ---- MMA2: D1 += [Minv; P Minv] Diag(beta) X = [U; P U] (N = 128: a
         //      tf32 MMA costs about the same per instruction at N = 64 and 128).
-        if (tid == 0) {
+        if (tid == 0 && alive()) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
 #pragma unroll 1
             for (int ks = 0; ks < C / 8; ++ks) {
@@ -821,16 +839,20 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             tc::commit(s_bar);
         }
-        // Under MMA2: the gate tile becomes gamma * sigmoid(gate) in place
-        // (warp 0, which issues MMA2, sits this out).
-        wgate.wait();
-        if (warp > 0) {   // lane = (box, 16-byte chunk) of a row: channels 4 lane .. 4 lane + 3
-            const int box = lane >> 3, ch = lane & 7;
-            float4 gm = *reinterpret_cast<const float4*>(p.gamma + h * D + lane * 4);
-            gm.x *= 0.5f; gm.y *= 0.5f; gm.z *= 0.5f; gm.w *= 0.5f;   // gamma sigmoid(g) = gm + gm tanh(g / 2)
-#pragma unroll 1
-            for (int r = warp - 1; r < C; r += 15) {
-                const uint32_t o = OFF_OG + box * kOGBox + r * 128 + ((ch ^ (r & 7)) << 4);
+        // Under MMA2: each output-epilogue thread (lane quadrants 2, 3) turns
+        // the 32 gate values it reads later (token row r, box grp) into
+        // gamma * sigmoid(gate) in place; no other thread touches them, so
+        // this pass and the epilogue need no barrier between them.
+        if ((warp & 3) >= 2) {
+            wgate.wait();
+            const int r = qrow - C;
+            const uint32_t gbase = OFF_OG + grp * kOGBox + r * 128;
+            const float* gam = p.gamma + h * D + grp * 32;
+#pragma unroll 4
+            for (int cc = 0; cc < 8; ++cc) {   // 16-byte chunk cc of the row: channels 4 cc .. 4 cc + 3
+                float4 gm = *reinterpret_cast<const float4*>(gam + cc * 4);
+                gm.x *= 0.5f; gm.y *= 0.5f; gm.z *= 0.5f; gm.w *= 0.5f;   // gamma sigmoid(g) = gm + gm tanh(g / 2)
+                const uint32_t o = gbase + ((cc ^ (r & 7)) << 4);
                 const float4 gv = at<float4>(sm, o);
                 at<float4>(sm, o) = make_float4(fmaf(gm.x, tanhf_(0.5f * gv.x), gm.x), fmaf(gm.y, tanhf_(0.5f * gv.y), gm.y),
                                                 fmaf(gm.z, tanhf_(0.5f * gv.z), gm.z), fmaf(gm.w, tanhf_(0.5f * gv.w), gm.w));
@@ -863,7 +885,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             tc::fence_before();
             named_barrier_sync(2, 256);   // U operand complete
             // ---- MMA3 (overlaps the output epilogue): M += R^T U.
-            if (tid == 0) {
+            if (tid == 0 && alive()) {
                 tc::fence_after();
                 constexpr uint32_t id = tc::idesc_tf32(128, 128);
 #pragma unroll 1
@@ -911,7 +933,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             ptx::fence_proxy_async_smem();
             named_barrier_sync(3, 256);   // the o tile is complete
-            if (tid == kOStore && !direct) {
+            if (tid == kOStore && !direct && alive()) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     ptx::tma_store_4d(&maps.o, j * 32, h, tb0 + t0, bmap, sm + OFF_OG + j * kOGBox);
@@ -928,11 +950,18 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const float gl = s_gh0[qrow] + s_gh1[qrow];
             esc_prev = __expf(fb ? 0.f : 0.5f * gl);   // e^{G_last - rho_R}
         }
-        sync_tc();
+        // A bounded wait that gave up anywhere in the CTA ends the walk for
+        // every thread at once (the vote is uniform).
+        tc::fence_before();
+        const bool stop = __syncthreads_or(*(volatile int*)s_dead) != 0;
+        tc::fence_after();
+        if (stop) break;
     }
+    const bool dead = __syncthreads_or(*(volatile int*)s_dead) != 0;
 
-    // Final state and conv window back to global memory.
-    {
+    // Final state and conv window back to global memory (not after a give-up:
+    // S and the window then keep their old contents).
+    if (!dead) {
         float* dst = io.S + ((size_t)bh * D + qrow) * D + grp * 32;
         uint32_t s[32];
         tc::ld32(tc::taddr(tm, warp, TM_S + grp * 32), s);
@@ -961,11 +990,25 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
     }
     if (tid == kOStore) ptx::bulk_wait_all();
+    if (dead) {
+        // Give-up path: let everything this CTA issued finish (each wait
+        // bounded) before its TMEM and shared memory are released.  The three
+        // MMA issuers commit their MMAs to one barrier; the last input-tile and
+        // gate-tile phases that were issued are waited for as well.
+        if (tid == 0 || tid == kIssuer1 || tid == kIssuerB) tc::commit(s_drain);
+        if (tid == kStager) {
+            if (*s_nt > 0) ptx::mbar_wait_timed(s_tbar, (uint32_t)((*s_nt - 1) & 1));
+            if (*s_ng > 0) ptx::mbar_wait_timed(s_gbar, (uint32_t)((*s_ng - 1) & 1));
+        }
+        if (tid == 0) ptx::mbar_wait_timed(s_drain, 0);
+    }
     sync_tc();
     if (warp == 0) tc::dealloc(tm, 512);
 }
 
-bool g_attr_done[64] = {};
+// Per-device flag: the kernel's attributes are set (the call is idempotent,
+// so two host threads setting it at once is harmless).
+std::atomic<bool> g_attr_done[64];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1004,11 +1047,11 @@ cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const Devi
                            int* err_word, cudaStream_t stream) {
     const long long grid = (long long)io.B * p.H;
     if (grid <= 0 || io.T <= 0) return cudaSuccess;
-    if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device]) {
+    if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kda_prefill_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device] = true;
+        if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device].store(true, std::memory_order_release);
     }
     Maps maps;
     const int mB = io.cu_seqlens ? 1 : io.B;   // packed sequences: one token axis of length io.T

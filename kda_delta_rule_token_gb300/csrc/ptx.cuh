@@ -13,6 +13,7 @@ namespace ptx {
 // Bits of the per-context error word (read back by kda_sync_status).
 constexpr int kErrDecodeLoadWait = 1 << 0;
 constexpr int kErrPrefillWait = 1 << 1;
+constexpr int kErrTestingWait = 1 << 2;
 
 // Longest a kernel waits on one barrier phase before it reports an error.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
@@ -58,16 +59,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* m, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Bounded in wall
-// time (kWaitLimitNs) and, when `abort` is given, cut short as soon as
-// another thread of the CTA has set *abort.  Returns false if it gave up.
-__device__ __forceinline__ bool mbar_wait_timed(uint64_t* m, uint32_t parity, const int* abort = nullptr) {
+// time (limit_ns) and, when `abort` is given, cut short as soon as another
+// thread of the CTA has set *abort.  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t* m, uint32_t parity, const int* abort = nullptr,
+                                                unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(m, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (unsigned i = 1;; ++i) {
         if (mbar_try_wait(m, parity)) return true;
         if ((i & 63) == 0) {
             if (abort && *(volatile const int*)abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
 }

@@ -91,3 +91,31 @@ def oracle_pairs(params, tokens, S0, conv0, pairs, *, call_major, l2_eps=1e-6, r
 
     with cf.ThreadPoolExecutor(workers) as ex:
         return dict(ex.map(one, pairs))
+
+
+POISON = 0x7FADBEEF          # a quiet NaN with a payload no computation produces
+GUARD_BYTES = 4096
+
+
+class Guarded:
+    """A float32 tensor placed inside a larger device buffer whose margins
+    (GUARD_BYTES before and after) hold the NaN pattern POISON.
+
+    ``t`` is the interior view (contiguous, 16-byte aligned: torch buffers
+    are 256-byte aligned and the margin is a multiple of 16 bytes);
+    ``intact()`` says whether every margin word still holds the pattern bit
+    for bit, i.e. no kernel wrote outside the tensor it was given.
+    """
+
+    def __init__(self, like: torch.Tensor):
+        assert like.dtype == torch.float32 and like.is_contiguous()
+        n, m = like.numel(), GUARD_BYTES // 4
+        self.m = m
+        self.buf = torch.empty(n + 2 * m, dtype=torch.float32, device=like.device)
+        self.buf.view(torch.int32).fill_(POISON)
+        self.t = self.buf[m:m + n].view(like.shape)
+        self.t.copy_(like)
+
+    def intact(self) -> bool:
+        w = self.buf.view(torch.int32)
+        return bool((w[:self.m] == POISON).all()) and bool((w[-self.m:] == POISON).all())

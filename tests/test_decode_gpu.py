@@ -10,7 +10,7 @@ import torch
 
 import kda_delta_rule_token_gb300 as kda
 from kda_delta_rule_token_gb300 import synth
-from harness import (max_rel_err, np64, oracle_pairs, pair_window, set_pair_window)
+from harness import (Guarded, max_rel_err, np64, oracle_pairs, pair_window, set_pair_window)
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-4
@@ -25,8 +25,15 @@ def _lib():
 
 
 def gpu_decode(wl, params, tokens, S, conv, *, o_pre=True, stream=None):
-    """Run the calls of ``tokens`` (call-major) in place on S / conv."""
+    """Run the calls of ``tokens`` (call-major) in place on S / conv.
+
+    o, o_pre, S and the window live inside poisoned guard regions during the
+    calls; the guards are checked bit for bit after every call.
+    """
     T, B, H, d = tokens["q"].shape
+    go = Guarded(torch.zeros((B, H, d), device=DEV))
+    gp = Guarded(torch.zeros((B, H, d), device=DEV)) if o_pre else None
+    gS, gc = Guarded(S), Guarded(conv)
     o = torch.empty((T, B, H, d), device=DEV)
     op = torch.empty((T, B, H, d), device=DEV) if o_pre else None
     ctx = kda.kda_create(H, params["conv_w"], params["dt_bias"], params["A_log"],
@@ -35,11 +42,22 @@ def gpu_decode(wl, params, tokens, S, conv, *, o_pre=True, stream=None):
         for t in range(T):
             kda.kda_decode_step(ctx, B, tokens["q"][t], tokens["k"][t], tokens["v"][t],
                                 tokens["z"][t], tokens["beta_logit"][t],
-                                tokens["gate_logit"][t], conv, S, o[t],
-                                op[t] if o_pre else None, stream=stream)
+                                tokens["gate_logit"][t], gc.t, gS.t, go.t,
+                                gp.t if o_pre else None, stream=stream)
+            o[t].copy_(go.t)
+            if o_pre:
+                op[t].copy_(gp.t)
+            if t == 0 or t == T - 1 or T <= 32:
+                torch.cuda.synchronize()
+                for g in (go, gp, gS, gc):
+                    assert g is None or g.intact(), f"a guard region was written at call {t}"
         assert kda.kda_sync_status(ctx, stream) == kda.KDA_OK
     finally:
         kda.kda_destroy(ctx)
+    S.copy_(gS.t)
+    conv.copy_(gc.t)
+    for g in (go, gp, gS, gc):
+        assert g is None or g.intact()
     return o, op
 
 

@@ -1,0 +1,153 @@
+"""Failure paths on the GPU, made to happen without faulting anything.
+
+* A bounded wait that runs out: a test-only kernel waits on an mbarrier that
+  nothing arrives on (no copy or MMA pending) for one millisecond and gives
+  up; kda_sync_status must report KDA_ERR_TIMEOUT once, then KDA_OK, and the
+  context must keep working.
+* An injected launch failure: with KDA_FAULT_INJECT naming an entry point,
+  the context's launches of it are replaced on the host by
+  cudaErrorLaunchFailure; the call must return KDA_ERR_CUDA, launch nothing
+  and leave every buffer as it was.
+"""
+import os
+
+import pytest
+import torch
+
+import kda_delta_rule_token_gb300 as kda
+from kda_delta_rule_token_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from kda_delta_rule_token_gb300 import build
+    build.build()
+    kda.load()
+
+
+def _create(wl, params):
+    return kda.kda_create(wl.H, params["conv_w"], params["dt_bias"], params["A_log"], params["gamma"])
+
+
+def _decode_once(ctx, wl, tokens, S, conv, o):
+    kda.kda_decode_step(ctx, wl.B, tokens["q"][0], tokens["k"][0], tokens["v"][0], tokens["z"][0],
+                        tokens["beta_logit"][0], tokens["gate_logit"][0], conv, S, o)
+
+
+def test_bounded_wait_gives_up_and_is_reported_once():
+    wl = synth.shrink(synth.WORKLOADS["decode_b64_h32_x256"], B=2, H=2, T=1)
+    params, tokens = synth.make_params(wl, DEV), synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    S, conv = st["S"], st["conv_state"]
+    ctx = _create(wl, params)
+    try:
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+        kda.kda_testing_bounded_wait(ctx, 1000)          # gives up after 1 ms
+        assert kda.kda_sync_status(ctx) == kda.KDA_ERR_TIMEOUT
+        assert "error word" in kda.kda_last_error_detail()
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK    # the word was cleared
+        # the context and the device keep working
+        o = torch.empty((wl.B, wl.H, 128), device=DEV)
+        _decode_once(ctx, wl, tokens, S, conv, o)
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+        assert bool(torch.isfinite(o).all())
+    finally:
+        kda.kda_destroy(ctx)
+
+
+def test_bounded_wait_limit_is_validated():
+    wl = synth.TINY
+    params = synth.make_params(wl, DEV)
+    ctx = _create(wl, params)
+    try:
+        for bad in (0, 1000001):
+            with pytest.raises(kda.KDAError) as ei:
+                kda.kda_testing_bounded_wait(ctx, bad)
+            assert ei.value.status == kda.KDA_ERR_INVALID_ARG
+    finally:
+        kda.kda_destroy(ctx)
+
+
+@pytest.fixture
+def inject(monkeypatch):
+    def set_(what):
+        monkeypatch.setenv("KDA_FAULT_INJECT", what)
+    return set_
+
+
+@pytest.mark.parametrize("what", ["decode", "all", "prefill,decode"])
+def test_injected_decode_launch_failure(inject, what):
+    wl = synth.shrink(synth.WORKLOADS["decode_b64_h32_x256"], B=2, H=3, T=1)
+    params, tokens = synth.make_params(wl, DEV), synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    S, conv = st["S"], st["conv_state"]
+    S0, c0 = S.clone(), conv.clone()
+    o = torch.full((wl.B, wl.H, 128), 3.0, device=DEV)
+    inject(what)
+    ctx = _create(wl, params)
+    try:
+        n0 = kda.kda_launch_count()
+        with pytest.raises(kda.KDAError) as ei:
+            _decode_once(ctx, wl, tokens, S, conv, o)
+        assert ei.value.status == kda.KDA_ERR_CUDA
+        detail = kda.kda_last_error_detail()
+        assert "cudaErrorLaunchFailure" in detail and "KDA_FAULT_INJECT" in detail
+        assert kda.kda_launch_count() == n0                 # nothing was launched
+        torch.cuda.synchronize()
+        assert torch.equal(S, S0) and torch.equal(conv, c0) and bool((o == 3.0).all())
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK       # no kernel reported anything
+    finally:
+        kda.kda_destroy(ctx)
+
+
+def test_injected_prefill_launch_failures(inject):
+    wl = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], B=2, H=2, T=70)
+    params, tokens = synth.make_params(wl, DEV), synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    S, conv = st["S"], st["conv_state"]
+    S0, c0 = S.clone(), conv.clone()
+    q, k, v = (tokens[n].view(torch.int16) for n in ("q", "k", "v"))
+    o = torch.full((wl.B, wl.T, wl.H, 128), 3.0, device=DEV)
+    cu = torch.tensor([0, wl.T], dtype=torch.int32, device=DEV)
+    inject("prefill,prefill_varlen")
+    ctx = _create(wl, params)
+    try:
+        n0 = kda.kda_launch_count()
+        with pytest.raises(kda.KDAError) as ei:
+            kda.kda_prefill(ctx, wl.B, wl.T, q, k, v, tokens["z"], tokens["beta_logit"],
+                            tokens["gate_logit"], conv, S, o)
+        assert ei.value.status == kda.KDA_ERR_CUDA
+        with pytest.raises(kda.KDAError) as ei:
+            kda.kda_prefill_varlen(ctx, 1, cu, wl.T, q[0], k[0], v[0], tokens["z"][0],
+                                   tokens["beta_logit"][0], tokens["gate_logit"][0], conv[:1], S[:1], o[0])
+        assert ei.value.status == kda.KDA_ERR_CUDA
+        assert "KDA_FAULT_INJECT" in kda.kda_last_error_detail()
+        assert kda.kda_launch_count() == n0
+        torch.cuda.synchronize()
+        assert torch.equal(S, S0) and torch.equal(conv, c0) and bool((o == 3.0).all())
+        # decode is not named: it still runs
+        od = torch.empty((wl.B, wl.H, 128), device=DEV)
+        f32 = {n: tokens[n][:, 0].float().contiguous() for n in ("q", "k", "v", "z", "gate_logit")}
+        kda.kda_decode_step(ctx, wl.B, f32["q"], f32["k"], f32["v"], f32["z"],
+                            tokens["beta_logit"][:, 0].contiguous(), f32["gate_logit"], conv, S, od)
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+        assert kda.kda_launch_count() == n0 + 1
+    finally:
+        kda.kda_destroy(ctx)
+
+
+def test_injection_is_off_when_unset(monkeypatch):
+    monkeypatch.delenv("KDA_FAULT_INJECT", raising=False)
+    wl = synth.shrink(synth.WORKLOADS["decode_b64_h32_x256"], B=1, H=1, T=1)
+    params, tokens = synth.make_params(wl, DEV), synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    ctx = _create(wl, params)
+    try:
+        o = torch.empty((1, 1, 128), device=DEV)
+        _decode_once(ctx, wl, tokens, st["S"], st["conv_state"], o)
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+    finally:
+        kda.kda_destroy(ctx)

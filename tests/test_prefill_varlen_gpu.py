@@ -3,7 +3,8 @@
 Each sequence is checked against the fp64 oracle run on that sequence alone
 (rel-L2 2e-3 over o and the final S; the conv window exactly), and the packed
 call must give exactly what one kda_prefill call per sequence gives: the
-same kernel runs the same arithmetic, only the addressing differs.
+same kernel runs the same arithmetic, only the addressing differs.  o, S and
+the windows sit inside poisoned guard regions during each packed call.
 """
 import numpy as np
 import pytest
@@ -11,7 +12,7 @@ import torch
 
 import kda_delta_rule_token_gb300 as kda
 from kda_delta_rule_token_gb300 import synth
-from harness import max_rel_err, np64, oracle_pairs, pair_window, rel_l2
+from harness import Guarded, max_rel_err, np64, oracle_pairs, pair_window, rel_l2
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-3
@@ -39,15 +40,19 @@ def packed(tokens, lengths):
 
 def run_varlen(H, params, pk, cu, S, conv):
     total = int(cu[-1].item())
-    o = torch.full((total, H, 128), float("nan"), device=DEV)
+    go = Guarded(torch.full((total, H, 128), float("nan"), device=DEV))
+    gS, gc = Guarded(S), Guarded(conv)
     ctx = kda.kda_create(H, params["conv_w"], params["dt_bias"], params["A_log"], params["gamma"])
     try:
         kda.kda_prefill_varlen(ctx, len(cu) - 1, cu, total, bits(pk["q"]), bits(pk["k"]), bits(pk["v"]),
-                               pk["z"], pk["beta_logit"], pk["gate_logit"], conv, S, o)
+                               pk["z"], pk["beta_logit"], pk["gate_logit"], gc.t, gS.t, go.t)
         assert kda.kda_sync_status(ctx) == kda.KDA_OK
     finally:
         kda.kda_destroy(ctx)
-    return o
+    assert go.intact() and gS.intact() and gc.intact(), "a guard region was written"
+    S.copy_(gS.t)
+    conv.copy_(gc.t)
+    return go.t.clone()
 
 
 def run_separate(H, params, tokens, lengths, S, conv):
