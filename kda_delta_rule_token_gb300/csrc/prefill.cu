@@ -232,13 +232,18 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     float* s_gh0 = s_part + 256;                                  // [128] decay sum over tokens 0..31
     float* s_gh1 = s_gh0 + 128;                                   // [128] decay sum over tokens 32..63
     float* s_win = reinterpret_cast<float*>(sm + OFF_WIN);        // [2][3][3][128], by chunk parity
-    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_gh1 + 128);
+    // mbarriers.  Each completes at most one phase per chunk and every thread
+    // that waits on one waits on it once per chunk, so no waiter can fall two
+    // phases behind (a parity wait would then alias onto a later phase).
+    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_gh1 + 128);   // MMA0 done
     uint64_t* s_tbar = s_bar + 1;                                 // input tiles landed
     uint64_t* s_gbar = s_bar + 2;                                 // gate tile landed
     uint64_t* s_tbarT = s_bar + 3;                                // MMA_T done
     uint64_t* s_bar1 = s_bar + 4;                                 // MMA1 done
     uint64_t* s_drain = s_bar + 5;                                // give-up path: MMA issuers drained
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 6);
+    uint64_t* s_bar2 = s_bar + 6;                                 // MMA2 done
+    uint64_t* s_bar3 = s_bar + 7;                                 // MMA3 done
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 8);
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
     int* s_nt = s_dead + 1;                                       // input-tile phases issued
     int* s_ng = s_dead + 2;                                       // gate-tile phases issued
@@ -299,6 +304,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         ptx::mbar_init(s_tbarT, 1);
         ptx::mbar_init(s_bar1, 1);
         ptx::mbar_init(s_drain, 3);
+        ptx::mbar_init(s_bar2, 1);
+        ptx::mbar_init(s_bar3, 1);
         ptx::fence_mbar_init();
         *s_dead = 0;
         *s_nt = 0;
@@ -307,6 +314,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     sync_tc();
     const uint32_t tm = *s_tmem;
     Waiter wt{s_bar, s_dead, err, 0u};
+    Waiter wt2{s_bar2, s_dead, err, 0u};
+    Waiter wt3{s_bar3, s_dead, err, 0u};
     Waiter wtma{s_tbar, s_dead, err, 0u};
     Waiter wgate{s_gbar, s_dead, err, 0u};
     Waiter wtT{s_tbarT, s_dead, err, 0u};
@@ -837,7 +846,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 tc::mma_ts(tm + TM_D1, tm + TM_DT + ks * 8,
                            tc::desc_sw128(ptx::smem_u32(sm + OFF_L + kb * 16384 + kin * 32)), id, 1u);
             }
-            tc::commit(s_bar);
+            tc::commit(s_bar2);
         }
         // Under MMA2: each output-epilogue thread (lane quadrants 2, 3) turns
         // the 32 gate values it reads later (token row r, box grp) into
@@ -858,7 +867,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                                                 fmaf(gm.z, tanhf_(0.5f * gv.z), gm.z), fmaf(gm.w, tanhf_(0.5f * gv.w), gm.w));
             }
         }
-        wt.wait();
+        wt2.wait();   // MMA2
 
         // ---- F and the output epilogue, as two independent groups of 8 warps
         //      (named barriers): the U rows (lane quadrants 0, 1) write MMA3's
@@ -894,7 +903,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                     tc::mma_ts(tm + TM_S, tm + TM_RT + ks * 8,
                                tc::desc_sw128(ptx::smem_u32(sm + OFF_R + kb * 16384 + kin * 32)), id, 1u);
                 }
-                tc::commit(s_bar);
+                tc::commit(s_bar3);
             }
         } else {
             const int r = qrow - C;
@@ -940,7 +949,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 ptx::bulk_commit();
             }
         }
-        wt.wait();   // MMA3
+        wt3.wait();   // MMA3
         // the next chunk's conv phase overwrites the tile: its reads must be done
         if (tid == kOStore) ptx::bulk_wait_read_all();
 
