@@ -69,6 +69,8 @@ def _load(lib_path: str | None = None):
             [ctypes.c_int] * 4 + [dp] * 10 + [ctypes.c_double] * 2 + [dp] * 9 + [ctypes.c_int])
         lib.kda_oracle_cpu_count.restype = ctypes.c_int
         lib.kda_oracle_cpu_count.argtypes = []
+        lib.kda_oracle_lowrank.restype = ctypes.c_int
+        lib.kda_oracle_lowrank.argtypes = [ctypes.c_int] * 5 + [dp] * 6
         _libs[path] = lib
     return _libs[path]
 
@@ -137,3 +139,26 @@ def run(q, k, v, z, beta_logit, gate_logit, conv_w, dt_bias, A_log, gamma,
     if rc != 0:
         raise ValueError(f"kda_oracle_run rejected its arguments (rc={rc})")
     return OracleOut(o, o_pre, St, cs, *extra)
+
+
+def lowrank(x, W_fa, W_fb, W_bp, H, d=128, *, lib_path: str | None = None):
+    """Low-rank front-end: z = W_fb (W_fa x), beta_logit = W_bp x per token.
+
+    x: [..., hidden]; W_fa: [rank, hidden]; W_fb: [H*d, rank]; W_bp: [H, hidden].
+    Returns (z [..., H, d], beta_logit [..., H]) as float64.
+    """
+    x = _f64(x)
+    lead = x.shape[:-1]
+    hidden = x.shape[-1]
+    W_fa, W_fb, W_bp = _f64(W_fa), _f64(W_fb), _f64(W_bp)
+    rank = W_fa.shape[0]
+    assert W_fa.shape == (rank, hidden) and W_fb.shape == (H * d, rank) and W_bp.shape == (H, hidden)
+    N = int(np.prod(lead)) if lead else 1
+    xf = np.ascontiguousarray(x.reshape(N, hidden))
+    z = np.zeros((N, H * d))
+    bl = np.zeros((N, H))
+    rc = _load(lib_path).kda_oracle_lowrank(N, hidden, rank, H, d, _ptr(xf), _ptr(W_fa), _ptr(W_fb),
+                                            _ptr(W_bp), _ptr(z), _ptr(bl))
+    if rc != 0:
+        raise ValueError(f"kda_oracle_lowrank rejected its arguments (rc={rc})")
+    return z.reshape(*lead, H, d), bl.reshape(*lead, H)

@@ -176,6 +176,42 @@ static void *worker(void *arg)
     return NULL;
 }
 
+/*
+ * Low-rank front-end ("What runs where (per layer)", row "KDA low-rank
+ * (fa,fb,bp)"; "Decay compute" row: z = W_fb W_fa x).  Each product is a
+ * plain sum over its inner index, one token at a time.
+ */
+int kda_oracle_lowrank(int N, int hidden, int rank, int H, int d,
+                       const double *x, const double *W_fa, const double *W_fb,
+                       const double *W_bp, double *z, double *beta_logit)
+{
+    if (N < 0 || hidden <= 0 || rank <= 0 || H <= 0 || d <= 0) return -1;
+    if (N == 0) return 0;
+    if (!x || !W_fa || !W_fb || !W_bp || !z || !beta_logit) return -1;
+    const size_t HD = (size_t)H * d;
+    double *u = malloc(sizeof(double) * rank);
+    for (int n = 0; n < N; ++n) {
+        const double *xn = x + (size_t)n * hidden;
+        for (int r = 0; r < rank; ++r) {
+            double s = 0.0;
+            for (int j = 0; j < hidden; ++j) s += W_fa[(size_t)r * hidden + j] * xn[j];
+            u[r] = s;
+        }
+        for (size_t m = 0; m < HD; ++m) {
+            double s = 0.0;
+            for (int r = 0; r < rank; ++r) s += W_fb[m * rank + r] * u[r];
+            z[(size_t)n * HD + m] = s;
+        }
+        for (int h = 0; h < H; ++h) {
+            double s = 0.0;
+            for (int j = 0; j < hidden; ++j) s += W_bp[(size_t)h * hidden + j] * xn[j];
+            beta_logit[(size_t)n * H + h] = s;
+        }
+    }
+    free(u);
+    return 0;
+}
+
 int kda_oracle_cpu_count(void)
 {
 #ifdef __linux__

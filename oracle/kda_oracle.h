@@ -48,6 +48,22 @@ int kda_oracle_run(int B, int T, int H, int d,
                    double *gk, double *beta,
                    int nthreads);
 
+/*
+ * Low-rank front-end of the decay and beta inputs ("Metal (Apple GPU) backend
+ * for Kimi K3", table "What runs where (per layer)", row "KDA low-rank
+ * (fa,fb,bp)"; "Kimi K3 Metal Gap Analysis", section 2, row "Decay compute",
+ * whose z is W_fb W_fa x).  For each of N tokens with hidden input x:
+ *   u          = W_fa x           u: [rank]
+ *   z          = W_fb u           z: [H*d]   (head h, channel c at h*d + c)
+ *   beta_logit = W_bp x           beta_logit: [H]
+ * Shapes: x [N][hidden], W_fa [rank][hidden], W_fb [H*d][rank],
+ * W_bp [H][hidden]; z [N][H*d] and beta_logit [N][H] are written.
+ * Returns 0 on success, -1 on a bad argument.
+ */
+int kda_oracle_lowrank(int N, int hidden, int rank, int H, int d,
+                       const double *x, const double *W_fa, const double *W_fb,
+                       const double *W_bp, double *z, double *beta_logit);
+
 /* Number of hardware threads this process may run on (sched affinity). */
 int kda_oracle_cpu_count(void);
 

@@ -9,7 +9,8 @@ operand) is caught by at least one of them.
 Sources: "Kimi K3 Metal Gap Analysis" section 2 "KDA Attention" (rows Conv4 +
 SiLU, L2 normalize q/k, Decay compute, Recurrence, O projection) and "Metal
 (Apple GPU) backend for Kimi K3" section "Correctness" (token-0 zero-state
-identity o / (v * beta) = q_hat . k_hat).
+identity o / (v * beta) = q_hat . k_hat) and table "What runs where (per
+layer)" (the low-rank fa, fb, bp matmuls feeding the decay and beta).
 """
 from __future__ import annotations
 
@@ -249,7 +250,60 @@ def pin_decay_values(lib_path=None):
     np.testing.assert_allclose(out.beta[0, :, 0], [0.5, 0.75, 0.25], rtol=1e-14)
 
 
+def _lowrank_inputs(seed, N=5, hidden=40, rank=6, H=3):
+    rng = np.random.default_rng(seed)
+    n = rng.standard_normal
+    return dict(x=n((N, hidden)), W_fa=n((rank, hidden)) / math.sqrt(hidden),
+                W_fb=n((H * D, rank)) / math.sqrt(rank), W_bp=n((H, hidden)) / math.sqrt(hidden))
+
+
+def pin_lowrank_one_hot(lib_path=None):
+    """Low-rank front-end ("What runs where (per layer)", row "KDA low-rank
+    (fa,fb,bp)"; "Decay compute" row, z = W_fb W_fa x): a single nonzero
+    weight in each matrix routes one input value to one output.  With
+    W_fa = e_2 e_17^T, W_fb = 3 e_(1*d+5) e_2^T and W_bp = -2 e_2 e_9^T, the
+    only nonzero outputs are z[head 1, channel 5] = 3 x_17 and
+    beta_logit[head 2] = -2 x_9, exactly."""
+    inp = _lowrank_inputs(301)
+    N, hidden = inp["x"].shape
+    W_fa = np.zeros_like(inp["W_fa"]); W_fa[2, 17] = 1.0
+    W_fb = np.zeros_like(inp["W_fb"]); W_fb[1 * D + 5, 2] = 3.0
+    W_bp = np.zeros_like(inp["W_bp"]); W_bp[2, 9] = -2.0
+    z, bl = oracle.lowrank(inp["x"], W_fa, W_fb, W_bp, H=3, lib_path=lib_path)
+    ez = np.zeros((N, 3, D)); ez[:, 1, 5] = 3.0 * inp["x"][:, 17]
+    eb = np.zeros((N, 3)); eb[:, 2] = -2.0 * inp["x"][:, 9]
+    assert np.array_equal(z, ez) and np.array_equal(bl, eb)
+
+
+def pin_lowrank_zero_fa(lib_path=None):
+    """W_fa = 0 makes z = 0 whatever W_fb and x are; beta_logit does not
+    depend on W_fa (the same with W_fa random)."""
+    inp = _lowrank_inputs(302)
+    z0, b0 = oracle.lowrank(inp["x"], np.zeros_like(inp["W_fa"]), inp["W_fb"], inp["W_bp"], H=3,
+                            lib_path=lib_path)
+    z1, b1 = oracle.lowrank(inp["x"], inp["W_fa"], inp["W_fb"], inp["W_bp"], H=3, lib_path=lib_path)
+    assert np.array_equal(z0, np.zeros_like(z0))
+    assert np.array_equal(b0, b1) and np.abs(z1).max() > 0
+
+
+def pin_lowrank_rank_and_linearity(lib_path=None):
+    """z is a linear map of x of rank at most `rank`: z(a x1 + b x2) =
+    a z(x1) + b z(x2) to rounding, and the z of 40 tokens span exactly `rank`
+    dimensions (W_fb W_fa has rank `rank` for generic weights); beta_logit is
+    linear in x too."""
+    inp = _lowrank_inputs(303, N=40)
+    rank = inp["W_fa"].shape[0]
+    x1, x2 = inp["x"][:20], inp["x"][20:]
+    f = lambda x: oracle.lowrank(x, inp["W_fa"], inp["W_fb"], inp["W_bp"], H=3, lib_path=lib_path)
+    (z1, b1), (z2, b2), (z3, b3) = f(x1), f(x2), f(0.5 * x1 - 2.0 * x2)
+    np.testing.assert_allclose(z3, 0.5 * z1 - 2.0 * z2, rtol=0, atol=1e-12 * np.abs(z1).max())
+    np.testing.assert_allclose(b3, 0.5 * b1 - 2.0 * b2, rtol=0, atol=1e-12 * np.abs(b1).max())
+    zs, _ = f(inp["x"])
+    sv = np.linalg.svd(zs.reshape(40, -1), compute_uv=False)
+    assert sv[rank - 1] > 1e-6 * sv[0] and sv[rank] < 1e-10 * sv[0]
+
+
 PINS = [pin_token0_identity, pin_identity_when_no_write_no_decay, pin_decay_only_closed_form,
         pin_delta_rule_write, pin_bruteforce_products, pin_conv_one_hot_tap, pin_conv_impulse,
         pin_window_continuity, pin_l2_norm, pin_rmsnorm_gate_gamma, pin_contraction_bound,
-        pin_decay_values]
+        pin_decay_values, pin_lowrank_one_hot, pin_lowrank_zero_fa, pin_lowrank_rank_and_linearity]

@@ -30,6 +30,13 @@ MUTANTS = [
     ("l2_eps_dropped", "1.0 / sqrt(ss + eps)", "1.0 / sqrt(ss)"),
     ("rms_eps_dropped", "sqrt(ms + J->rms_eps)", "sqrt(ms)"),
     ("exp_alog_dropped", "-exp(J->A_log[(size_t)h * d + c])", "-(J->A_log[(size_t)h * d + c])"),
+    # low-rank front-end
+    ("lowrank_fa_transposed", "W_fa[(size_t)r * hidden + j] * xn[j]", "W_fa[(size_t)j * rank + r] * xn[j]"),
+    ("lowrank_fb_transposed", "W_fb[m * rank + r] * u[r]", "W_fb[(size_t)r * HD + m] * u[r]"),
+    ("lowrank_skips_fa", "W_fb[m * rank + r] * u[r]", "W_fb[m * rank + r] * xn[r]"),
+    ("lowrank_beta_from_fa", "W_bp[(size_t)h * hidden + j] * xn[j]", "W_fa[(size_t)h * hidden + j] * xn[j]"),
+    ("lowrank_token_stride", "const double *xn = x + (size_t)n * hidden;", "const double *xn = x + (size_t)n * rank;"),
+    ("lowrank_head_offset", "z[(size_t)n * HD + m] = s;", "z[(size_t)n * HD + (m + d) % HD] = s;"),
 ]
 
 
