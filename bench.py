@@ -377,6 +377,67 @@ class Ours:
         torch.cuda.empty_cache()
         return res
 
+    # ---------------------------------------------------------- low-rank decode
+    def decode_lowrank(self, wl_name):
+        """kda_decode_step_lowrank (front-end GEMMs + decode kernel) per call,
+        and the front-end alone (kda_lowrank), on a decode workload with the
+        default low-rank widths; L2 flushed between timed calls."""
+        torch, kda, synth = self.torch, self.kda, self.synth
+        wl = synth.WORKLOADS[wl_name]
+        p = synth.make_params(wl, self.dev)
+        st = synth.make_state(wl, self.dev)
+        S, cs = st["S"], st["conv_state"]
+        tk = synth.make_tokens(wl, self.dev)
+        lr = synth.make_lowrank(wl, self.dev)
+        B, H = wl.B, wl.H
+        o = torch.empty((B, H, D), device=self.dev)
+        ctx = kda.kda_create(H, p["conv_w"], p["dt_bias"], p["A_log"], p["gamma"])
+        kda.kda_bind_lowrank(ctx, lr["hidden"], lr["rank"], lr["W_fa"], lr["W_fb"], lr["W_bp"])
+        ws = torch.empty(kda.kda_decode_lowrank_workspace_bytes(ctx, B), dtype=torch.uint8, device=self.dev)
+        wsf = torch.empty(kda.kda_lowrank_workspace_bytes(ctx, B), dtype=torch.uint8, device=self.dev)
+        z = torch.empty((B, H, D), device=self.dev)
+        bl = torch.empty((B, H), device=self.dev)
+        K, W = min(self.args.steps, 500), self.args.warmup
+
+        def step(i):
+            t = i % wl.T
+            kda.kda_decode_step_lowrank(ctx, B, lr["x"][t], tk["q"][t], tk["k"][t], tk["v"][t],
+                                        tk["gate_logit"][t], cs, S, o, None, ws, 0, self.stream)
+
+        def front(i):
+            kda.kda_lowrank(ctx, B, lr["x"][i % wl.T], z, bl, wsf, 0, self.stream)
+
+        out = {}
+        for name, fn in (("step", step), ("frontend", front)):
+            for i in range(W):
+                self.flush_l2()
+                fn(i)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)]
+            self.barrier_sync()
+            l0 = kda.kda_launch_count()
+            for i in range(K):
+                self.flush_l2()
+                ev[i][0].record(self.stream)
+                fn(W + i)
+                ev[i][1].record(self.stream)
+            self.barrier_sync()
+            out[name] = (self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev)),
+                         kda.kda_launch_count() - l0)
+        assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
+        kda.kda_destroy(ctx)
+        hid, rank = lr["hidden"], lr["rank"]
+        fe_bytes = 4 * ((rank + H) * hid + H * D * rank + B * hid + B * H * D + B * H)
+        fe_flop = 2 * B * ((rank + H) * hid + H * D * rank)
+        units = B * H
+        res = {"wl": wl, "hidden": hid, "rank": rank, "ms_step": out["step"][0], "launches_step": out["step"][1],
+               "ms_frontend": out["frontend"][0], "launches_frontend": out["frontend"][1],
+               "fe_bytes": fe_bytes, "fe_flop": fe_flop,
+               "state_gbs": self.world * units * STATE_BYTES / (out["step"][0] * 1e-3) / 1e9}
+        del tk, S, cs, lr
+        torch.cuda.empty_cache()
+        return res
+
     # ---------------------------------------------------------------- prefill
     def prefill(self, wl_name, e2e=True):
         torch, kda, synth = self.torch, self.kda, self.synth
@@ -737,6 +798,7 @@ def main():
     clocks.start()
     head = None if args.no_decode else ours.decode(HEADLINE_WL, flush=False, graph=True)
     dec = None if args.no_decode else ours.decode(DECODE_WL, flush=True)
+    dlr = None if args.no_decode else ours.decode_lowrank(DECODE_WL)
     psteps = max(3, min(args.steps, args.prefill_steps))
     pre = None if args.no_prefill else ours.prefill(PREFILL_WL)
     pre1 = None if args.no_prefill else ours.prefill(PREFILL1_WL, e2e=False)
@@ -782,6 +844,23 @@ def main():
         line["decode_b64_h32"] = decode_block(
             dec, peaks, "decode_b64_h32_kda_decode_kernel.md", dsha,
             "state 128 MiB < L2: flushed between timed calls (256 MiB write + 256 MiB read)")
+    if dlr is not None:
+        w = dlr["wl"]
+        fe_gbs = dlr["fe_bytes"] / (dlr["ms_frontend"] * 1e-3) / 1e9
+        line["decode_lowrank"] = {
+            "workload": w.name + f" through the low-rank front-end (hidden {dlr['hidden']}, rank {dlr['rank']})",
+            "B": w.B, "H": w.H, "l2": "flushed between timed calls",
+            "ms_per_call": round(dlr["ms_step"], 5), "state_gbs": round(dlr["state_gbs"], 1),
+            "gpu_launches": dlr["launches_step"],
+            "frontend": {
+                "ms_per_call": round(dlr["ms_frontend"], 5), "gpu_launches": dlr["launches_frontend"],
+                "tflops_algorithmic": round(dlr["fe_flop"] / (dlr["ms_frontend"] * 1e-3) / 1e12, 3),
+                "roofline": {"bound": "hbm", "achieved": round(fe_gbs, 1), "peak": peaks["hbm_gbs"],
+                             "unit": "GB/s", "frac": round(fe_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                             "kernel": "kda_lowrank_gemm_kernel + kda_lowrank_reduce_kernel",
+                             "alg_bytes_per_call": dlr["fe_bytes"]},
+            },
+        }
     if pre is not None:
         line["prefill"] = prefill_block(pre, peaks, psteps, "prefill_b8_h64_kernel.md", psha, cpu_pre)
     if pre1 is not None:

@@ -46,7 +46,8 @@
  *    the same suspicion.
  *  - Host-side fault injection for tests: the environment variable
  *    KDA_FAULT_INJECT, read by kda_create, names entry points ("decode",
- *    "prefill", "prefill_varlen", "all"; comma-separated) whose launches that
+ *    "prefill", "prefill_varlen", "lowrank", "all"; comma-separated; the
+ *    low-rank decode step counts as "decode" and "lowrank") whose launches that
  *    context replaces by cudaErrorLaunchFailure: nothing is launched, no
  *    buffer changes, and the call returns KDA_ERR_CUDA.
  */
@@ -198,6 +199,61 @@ KDA_API kda_status kda_prefill_varlen(kda_ctx *ctx, int B, const int32_t *cu_seq
                        const uint16_t *q, const uint16_t *k, const uint16_t *v,
                        const float *z, const float *beta_logit, const float *gate_logit,
                        float *conv_state, float *S, float *o, void *stream);
+
+/*
+ * Bind the low-rank front-end weights of the layer to the context ("Metal
+ * (Apple GPU) backend for Kimi K3", table "What runs where (per layer)", row
+ * "KDA low-rank (fa,fb,bp)"; "Kimi K3 Metal Gap Analysis", section 2, row
+ * "Decay compute", whose decay input is z = W_fb W_fa x).  Per token with
+ * hidden input x:  u = W_fa x,  z = W_fb u,  beta_logit = W_bp x.
+ *   hidden   width of x; a multiple of 4
+ *   rank     inner width of W_fb W_fa; a multiple of 4, at most 512
+ *   W_fa     [rank][hidden]  fp32 device pointer, 16-byte aligned, borrowed
+ *   W_fb     [H*d][rank]     fp32, row h*d + c feeds head h, channel c
+ *   W_bp     [H][hidden]     fp32
+ * The pages give neither width; both are the caller's.  Rebinding replaces
+ * the previous weights.  Launches nothing.
+ */
+KDA_API kda_status kda_bind_lowrank(kda_ctx *ctx, int hidden, int rank, const float *W_fa,
+                                    const float *W_fb, const float *W_bp);
+
+/* Bytes of device workspace kda_lowrank needs for N tokens (0 if no weights
+ * are bound or N <= 0). */
+KDA_API size_t kda_lowrank_workspace_bytes(const kda_ctx *ctx, int N);
+
+/*
+ * The low-rank front-end for N tokens, on tensor cores (two tf32 GEMMs with
+ * fp32 accumulation and a fixed-order reduction):
+ *   x            [N][hidden] fp32 (in), 16-byte aligned
+ *   z            [N][H][d]   fp32 (out): the decay input of kda_decode_step /
+ *                kda_prefill (N = B, or N = B*T with the [B][T][H][d] layout)
+ *   beta_logit   [N][H]      fp32 (out), 4-byte aligned
+ *   workspace    at least kda_lowrank_workspace_bytes(ctx, N) bytes, 16-byte
+ *                aligned, owned by the caller; its contents are scratch
+ * N == 0 is a no-op.  KDA_ERR_INVALID_ARG if no weights are bound.
+ */
+KDA_API kda_status kda_lowrank(kda_ctx *ctx, int N, const float *x, float *z, float *beta_logit,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of device workspace kda_decode_step_lowrank needs for B sequences. */
+KDA_API size_t kda_decode_lowrank_workspace_bytes(const kda_ctx *ctx, int B);
+
+/*
+ * One decode token whose decay input and beta logits come from the hidden
+ * input through the bound low-rank weights: kda_lowrank on the B tokens (z
+ * and beta_logit kept in the workspace), then the kda_decode_step kernel on
+ * them, both on `stream`.
+ *   x            [B][hidden] fp32 (in)
+ *   q, k, v, gate_logit, conv_state, S, o, o_pre   as for kda_decode_step
+ *   workspace    at least kda_decode_lowrank_workspace_bytes(ctx, B) bytes,
+ *                16-byte aligned, owned by the caller
+ * B == 0 is a no-op.  Give-ups behave as for kda_decode_step.
+ */
+KDA_API kda_status kda_decode_step_lowrank(kda_ctx *ctx, int B, const float *x,
+                                           const float *q, const float *k, const float *v,
+                                           const float *gate_logit, float *conv_state, float *S,
+                                           float *o, float *o_pre, void *workspace,
+                                           size_t workspace_bytes, void *stream);
 
 /*
  * Synchronise `stream` and report whether any kernel launched with this

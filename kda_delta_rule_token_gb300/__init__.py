@@ -16,7 +16,8 @@ from . import build as _build_mod
 __all__ = [
     "KDAError", "load", "kda_create", "kda_destroy", "kda_strerror", "kda_last_error_detail",
     "kda_decode_step", "kda_prefill", "kda_prefill_varlen", "kda_prefill_workspace_bytes", "kda_sync_status",
-    "kda_launch_count", "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_ALIGNMENT",
+    "kda_launch_count", "kda_bind_lowrank", "kda_lowrank", "kda_lowrank_workspace_bytes",
+    "kda_decode_step_lowrank", "kda_decode_lowrank_workspace_bytes", "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_ALIGNMENT",
     "KDA_ERR_UNSUPPORTED", "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "HEAD_DIM", "CHUNK",
 ]
 
@@ -81,6 +82,16 @@ def load(path: str | None = None):
     lib.kda_sync_status.restype = i32
     lib.kda_launch_count.argtypes = []
     lib.kda_launch_count.restype = u64
+    lib.kda_bind_lowrank.argtypes = [vp, i32, i32, vp, vp, vp]
+    lib.kda_bind_lowrank.restype = i32
+    lib.kda_lowrank_workspace_bytes.argtypes = [vp, i32]
+    lib.kda_lowrank_workspace_bytes.restype = sz
+    lib.kda_lowrank.argtypes = [vp, i32, vp, vp, vp, vp, sz, vp]
+    lib.kda_lowrank.restype = i32
+    lib.kda_decode_lowrank_workspace_bytes.argtypes = [vp, i32]
+    lib.kda_decode_lowrank_workspace_bytes.restype = sz
+    lib.kda_decode_step_lowrank.argtypes = [vp, i32] + [vp] * 10 + [sz, vp]
+    lib.kda_decode_step_lowrank.restype = i32
     lib.kda_testing_bounded_wait.argtypes = [vp, ctypes.c_uint, vp]
     lib.kda_testing_bounded_wait.restype = i32
     _lib = lib
@@ -163,6 +174,38 @@ def kda_prefill_varlen(ctx, B, cu_seqlens, total_T, q, k, v, z, beta_logit, gate
     _check(load().kda_prefill_varlen(ctx, int(B), _p(cu_seqlens), int(total_T), _p(q), _p(k), _p(v),
                                      _p(z), _p(beta_logit), _p(gate_logit), _p(conv_state), _p(S),
                                      _p(o), _stream(stream)), "kda_prefill_varlen")
+
+
+def _nbytes(buf, given):
+    if buf is None or isinstance(buf, int) or given:
+        return int(given)
+    return buf.numel() * buf.element_size()
+
+
+def kda_bind_lowrank(ctx, hidden, rank, W_fa, W_fb, W_bp) -> None:
+    _check(load().kda_bind_lowrank(ctx, int(hidden), int(rank), _p(W_fa), _p(W_fb), _p(W_bp)),
+           "kda_bind_lowrank")
+
+
+def kda_lowrank_workspace_bytes(ctx, N) -> int:
+    return int(load().kda_lowrank_workspace_bytes(ctx, int(N)))
+
+
+def kda_lowrank(ctx, N, x, z, beta_logit, workspace, workspace_bytes=0, stream=None) -> None:
+    _check(load().kda_lowrank(ctx, int(N), _p(x), _p(z), _p(beta_logit), _p(workspace),
+                              _nbytes(workspace, workspace_bytes), _stream(stream)), "kda_lowrank")
+
+
+def kda_decode_lowrank_workspace_bytes(ctx, B) -> int:
+    return int(load().kda_decode_lowrank_workspace_bytes(ctx, int(B)))
+
+
+def kda_decode_step_lowrank(ctx, B, x, q, k, v, gate_logit, conv_state, S, o, o_pre, workspace,
+                            workspace_bytes=0, stream=None) -> None:
+    _check(load().kda_decode_step_lowrank(ctx, int(B), _p(x), _p(q), _p(k), _p(v), _p(gate_logit),
+                                          _p(conv_state), _p(S), _p(o), _p(o_pre), _p(workspace),
+                                          _nbytes(workspace, workspace_bytes), _stream(stream)),
+           "kda_decode_step_lowrank")
 
 
 def kda_sync_status(ctx, stream=None) -> int:

@@ -24,6 +24,8 @@ struct kda_ctx {
     kda::DeviceInfo dev;
     int* err_word;    // device int: nonzero after a kernel gave up on a bounded wait
     unsigned inject;  // launches replaced by an injected failure (KDA_FAULT_INJECT)
+    bool has_lowrank;
+    kda::LowRank lowrank;  // bound by kda_bind_lowrank
 };
 
 namespace kda {
@@ -55,7 +57,7 @@ kda_status check_device(const kda_ctx* ctx) {
     return KDA_OK;
 }
 
-constexpr unsigned kInjectDecode = 1u, kInjectPrefill = 2u, kInjectVarlen = 4u;
+constexpr unsigned kInjectDecode = 1u, kInjectPrefill = 2u, kInjectVarlen = 4u, kInjectLowrank = 8u;
 
 // Parse KDA_FAULT_INJECT (see the top of this file).
 unsigned parse_inject(const char* v) {
@@ -70,7 +72,8 @@ unsigned parse_inject(const char* v) {
         if (is("decode")) m |= kInjectDecode;
         else if (is("prefill")) m |= kInjectPrefill;
         else if (is("prefill_varlen")) m |= kInjectVarlen;
-        else if (is("all")) m |= kInjectDecode | kInjectPrefill | kInjectVarlen;
+        else if (is("lowrank")) m |= kInjectLowrank;
+        else if (is("all")) m |= kInjectDecode | kInjectPrefill | kInjectVarlen | kInjectLowrank;
         p = *e ? e + 1 : e;
     }
     return m;
@@ -276,6 +279,98 @@ kda_status kda_sync_status(kda_ctx* ctx, void* stream) {
             return KDA_ERR_CUDA;
         }
         return KDA_ERR_TIMEOUT;
+    }
+    return KDA_OK;
+}
+
+kda_status kda_bind_lowrank(kda_ctx* ctx, int hidden, int rank, const float* W_fa, const float* W_fb,
+                            const float* W_bp) {
+    if (!ctx || !W_fa || !W_fb || !W_bp) return KDA_ERR_INVALID_ARG;
+    if (hidden < 4 || rank < 4 || rank > 512 || (hidden & 3) || (rank & 3)) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail),
+                      "hidden (%d) and rank (%d) must be multiples of 4, rank at most 512", hidden, rank);
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (!aligned16(W_fa) || !aligned16(W_fb) || !aligned16(W_bp)) return KDA_ERR_ALIGNMENT;
+    ctx->lowrank = kda::LowRank{hidden, rank, W_fa, W_fb, W_bp};
+    ctx->has_lowrank = true;
+    return KDA_OK;
+}
+
+size_t kda_lowrank_workspace_bytes(const kda_ctx* ctx, int N) {
+    if (!ctx || !ctx->has_lowrank || N <= 0) return 0;
+    return kda::lowrank_workspace_bytes(ctx->params, ctx->lowrank, ctx->dev, N);
+}
+
+kda_status kda_lowrank(kda_ctx* ctx, int N, const float* x, float* z, float* beta_logit, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    if (!ctx || N < 0) return KDA_ERR_INVALID_ARG;
+    if (!ctx->has_lowrank) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail), "no low-rank weights bound (kda_bind_lowrank)");
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (N == 0) return KDA_OK;
+    if (!x || !z || !beta_logit || !workspace) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(z) || !aligned4(beta_logit) || !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
+    if (workspace_bytes < kda::lowrank_workspace_bytes(ctx->params, ctx->lowrank, ctx->dev, N))
+        return KDA_ERR_INVALID_ARG;
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
+    cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectLowrank, [&] {
+        return kda::launch_lowrank(ctx->params, ctx->lowrank, N, x, z, beta_logit, workspace, ctx->dev,
+                                   ctx->err_word, static_cast<cudaStream_t>(stream));
+    });
+    if (e != cudaSuccess) { kda::set_launch_detail(ctx, kda::kInjectLowrank, "lowrank launch", e); return KDA_ERR_CUDA; }
+    return KDA_OK;
+}
+
+// Workspace of kda_decode_step_lowrank: the front-end's own, then z [B][H][d]
+// and beta_logit [B][H].
+static size_t decode_lowrank_parts(const kda_ctx* ctx, int B, size_t* off_z, size_t* off_b) {
+    const size_t a = (kda::lowrank_workspace_bytes(ctx->params, ctx->lowrank, ctx->dev, B) + 255) & ~size_t(255);
+    const size_t zb = (size_t)B * ctx->params.H * kda::kHeadDim * 4;
+    *off_z = a;
+    *off_b = (a + zb + 255) & ~size_t(255);
+    return *off_b + (size_t)B * ctx->params.H * 4;
+}
+
+size_t kda_decode_lowrank_workspace_bytes(const kda_ctx* ctx, int B) {
+    if (!ctx || !ctx->has_lowrank || B <= 0) return 0;
+    size_t oz, ob;
+    return decode_lowrank_parts(ctx, B, &oz, &ob);
+}
+
+kda_status kda_decode_step_lowrank(kda_ctx* ctx, int B, const float* x, const float* q, const float* k,
+                                   const float* v, const float* gate_logit, float* conv_state, float* S,
+                                   float* o, float* o_pre, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    if (!ctx || B < 0) return KDA_ERR_INVALID_ARG;
+    if (!ctx->has_lowrank) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail), "no low-rank weights bound (kda_bind_lowrank)");
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (B == 0) return KDA_OK;
+    if (!x || !q || !k || !v || !gate_logit || !conv_state || !S || !o || !workspace) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, q, k, v, gate_logit, conv_state, S, o, workspace};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (o_pre && !aligned16(o_pre)) return KDA_ERR_ALIGNMENT;
+    if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    size_t oz, ob;
+    if (workspace_bytes < decode_lowrank_parts(ctx, B, &oz, &ob)) return KDA_ERR_INVALID_ARG;
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
+    float* z = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + oz);
+    float* bl = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ob);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectLowrank | kda::kInjectDecode, [&] {
+        cudaError_t r = kda::launch_lowrank(ctx->params, ctx->lowrank, B, x, z, bl, workspace, ctx->dev,
+                                            ctx->err_word, st);
+        if (r != cudaSuccess) return r;
+        kda::DecodeIO io{B, q, k, v, z, bl, gate_logit, conv_state, S, o, o_pre};
+        return kda::launch_decode(ctx->params, io, ctx->dev, ctx->err_word, st);
+    });
+    if (e != cudaSuccess) {
+        kda::set_launch_detail(ctx, kda::kInjectLowrank | kda::kInjectDecode, "decode_lowrank launch", e);
+        return KDA_ERR_CUDA;
     }
     return KDA_OK;
 }

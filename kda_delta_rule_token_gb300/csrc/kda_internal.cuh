@@ -55,6 +55,15 @@ struct PrefillIO {
     size_t workspace_bytes;
 };
 
+// Low-rank front-end weights bound to a context (borrowed, fp32).
+struct LowRank {
+    int hidden;           // width of the hidden input x
+    int rank;             // inner width of W_fb W_fa
+    const float* W_fa;    // [rank][hidden]
+    const float* W_fb;    // [H*d][rank]
+    const float* W_bp;    // [H][hidden]
+};
+
 // Device facts the launchers need, queried once per context.
 struct DeviceInfo {
     int device;
@@ -69,6 +78,13 @@ cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const Device
 size_t prefill_workspace_bytes(int H, int B, int T);
 cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const DeviceInfo& dev,
                            int* err_word, cudaStream_t stream);
+
+// Low-rank front-end (csrc/lowrank.cu): z [N][H*d] and beta_logit [N][H] of
+// N tokens of hidden input x [N][hidden]; workspace of lowrank_workspace_bytes.
+size_t lowrank_workspace_bytes(const LayerParams& p, const LowRank& lr, const DeviceInfo& dev, int N);
+cudaError_t launch_lowrank(const LayerParams& p, const LowRank& lr, int N, const float* x, float* z,
+                           float* beta_logit, void* workspace, const DeviceInfo& dev, int* err_word,
+                           cudaStream_t stream);
 
 // Test hook (csrc/testing.cu): a kernel whose bounded wait runs out.
 cudaError_t launch_testing_wait(int* err_word, unsigned long long limit_ns, cudaStream_t stream);

@@ -1,0 +1,363 @@
+// Low-rank front-end of the decay and beta inputs, on tcgen05 tensor cores.
+//
+// "Metal (Apple GPU) backend for Kimi K3", table "What runs where (per
+// layer)", row "KDA low-rank (fa,fb,bp)", and "Kimi K3 Metal Gap Analysis",
+// section 2, row "Decay compute" (z = W_fb W_fa x): per token with hidden
+// input x,
+//
+//   u          = W_fa x     (rank)
+//   z          = W_fb u     (H * d: the decay input of every head)
+//   beta_logit = W_bp x     (H)
+//
+// These are dense contractions shared by every head of a token (u) and by
+// every token (the weights), so they run as GEMMs over all N tokens of a call
+// before the per-(sequence, head) kernels, not inside them:
+//
+//   GEMM A  [u | beta_logit]^T = [W_fa ; W_bp] x^T, split over K (hidden) so
+//           that a decode batch of 64..256 tokens still spreads over the SMs;
+//           partial sums go to the workspace;
+//   reduce  the partial sums in a fixed order (deterministic) into u and
+//           beta_logit;
+//   GEMM C  z^T = W_fb u^T.
+//
+// One GEMM kernel serves both: C[n][m] = sum_k A[m][k] B[n][k] with A the
+// weights (row-major [rows][K], i.e. K-major) and B the activations
+// (row-major [N][K], K-major too), fp32 accumulation in TMEM.  The products
+// keep fp32 accuracy with three tf32 MMAs per product (the split of each
+// operand a = hi + lo, hi its tf32 truncation): hi*hi + hi*lo + lo*hi, whose
+// dropped lo*lo term and tf32 rounding of lo are below 2^-20 of the product.
+// (A single tf32 product would leave z about 5e-4 off at K = 7168, and z
+// reaches the state through e^gk at every token.)  The MMA itself reads an
+// fp32 operand as its tf32 truncation, so the TMA-landed tile serves as hi;
+// two warps write lo = a - hi beside it.
+//
+// A CTA owns a 128-row tile of A, an N tile of up to 256 tokens and one K
+// split; one thread streams 32-wide K slices of both operands with TMA
+// (128-byte swizzle) through a ring of stages, warps 2-3 form the lo parts
+// of each landed slice, one thread issues the kind::tf32 MMAs (M = 128,
+// N = the tile, 3 x 4 per slice) and releases the stage with a commit, and
+// all four warps read the accumulator back (TMEM lane = output row) and
+// store it token-major, so a warp writes 128 contiguous bytes per token.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
+#include "kda_internal.cuh"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kMaxStages = 4;
+constexpr uint32_t kStageBudget = 200 * 1024;    // shared memory for the ring
+constexpr int kKStep = 32;                       // fp32 elements in one 128-byte swizzled row
+constexpr uint32_t kATileBytes = 128 * 128;      // 128 rows x 128 bytes
+constexpr int kThreads = 128;
+
+struct GemmMaps {
+    CUtensorMap a0, a1;   // weights, (K, rows) with boxes of (32, 128)
+    CUtensorMap b;        // activations, (K, N) with boxes of (32, Nt)
+};
+
+struct GemmArgs {
+    int M0, M1;     // rows of the first and second weight matrix (M1 = 0: none)
+    int tiles0;     // 128-row tiles of the first matrix
+    int N, K;
+    int Nt;         // token tile: 16, 32, 64, 128 or 256
+    int kslice;     // K elements per split, a multiple of 32
+    int stages;     // depth of the ring
+    float* out;     // [splits][N][M0 + M1]
+};
+
+// A stage: A hi, B hi (TMA), then A lo, B lo (split warps); each part a
+// multiple of 1024 bytes, so every operand starts on a swizzle atom.
+__host__ __device__ constexpr uint32_t half_bytes(int Nt) { return kATileBytes + (uint32_t)Nt * 128; }
+__host__ __device__ constexpr uint32_t stage_bytes(int Nt) { return 2 * half_bytes(Nt); }
+constexpr int ring_stages(int Nt) {
+    return (int)(kStageBudget / stage_bytes(Nt)) < kMaxStages ? (int)(kStageBudget / stage_bytes(Nt)) : kMaxStages;
+}
+constexpr uint32_t gemm_smem_bytes(int Nt) { return ring_stages(Nt) * stage_bytes(Nt) + 1024; }
+constexpr int kSplitThreads = 64;   // warps 2 and 3
+
+// Bounded wait shared by the roles of the GEMM CTA: gives up after the wall
+// time limit (or at once when another thread already gave up), marks the CTA
+// dead and records the error bit.
+__device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, int* dead, int* err) {
+    if (*(volatile int*)dead) return false;
+    if (ptx::mbar_wait_timed(bar, parity, dead)) return true;
+    *(volatile int*)dead = 1;
+    atomicOr(err, ptx::kErrLowrankWait);
+    return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+kda_lowrank_gemm_kernel(const GemmArgs g, int* err, const __grid_constant__ GemmMaps maps) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int S = g.stages;
+    const uint32_t hbytes = half_bytes(g.Nt), sbytes = stage_bytes(g.Nt);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S * sbytes);   // slice landed (hi parts)
+    uint64_t* split = full + kMaxStages;                             // lo parts written
+    uint64_t* empty = split + kMaxStages;                            // slice consumed by the MMAs
+    uint64_t* accb = empty + kMaxStages;                             // accumulator complete
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(accb + 1);
+    int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
+    int* s_issued = s_dead + 1;                                            // slices the producer issued
+
+    const int mt = blockIdx.x, nt = blockIdx.y, ks = blockIdx.z;
+    const bool second = mt >= g.tiles0;
+    const int arow = (second ? mt - g.tiles0 : mt) * 128;    // first row of the tile in its matrix
+    const int mrows = second ? g.M1 : g.M0;                  // rows of that matrix
+    const int mbase = second ? g.M0 + arow : arow;           // output row of TMEM lane 0
+    const int n0 = nt * g.Nt;
+    const int k0 = ks * g.kslice;
+    const int k1 = min(g.K, k0 + g.kslice);
+    const int nk = (k1 - k0 + kKStep - 1) / kKStep;          // >= 1: the host makes no empty split
+    const uint32_t ncols = g.Nt < 32 ? 32u : (uint32_t)g.Nt;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&split[s], kSplitThreads);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        ptx::mbar_init(accb, 1);
+        ptx::fence_mbar_init();
+        *s_dead = 0;
+        *s_issued = 0;
+    }
+    if (warp == 0) tc::alloc(s_tmem, ncols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *s_tmem;
+    const CUtensorMap* amap = second ? &maps.a1 : &maps.a0;
+
+    if (tid == 0) {
+        // TMA producer: slice i goes to stage i % S once the MMAs of slice
+        // i - S have released it.
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % S;
+            if (i >= S && !gwait(&empty[s], (uint32_t)((i / S - 1) & 1), s_dead, err)) break;
+            uint8_t* st = sm + s * sbytes;
+            ptx::mbar_arrive_expect_tx(&full[s], hbytes);
+            ptx::tma_load_2d(st, amap, k0 + i * kKStep, arow, &full[s]);
+            ptx::tma_load_2d(st + kATileBytes, &maps.b, k0 + i * kKStep, n0, &full[s]);
+            *s_issued = i + 1;
+        }
+    } else if (tid == 32) {
+        // MMA issuer: per 32-wide slice, for each K = 8 step, hi*hi, hi*lo and
+        // lo*hi; then release the stage.
+        const uint32_t id = tc::idesc_tf32(128, g.Nt);
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % S;
+            if (!gwait(&split[s], (uint32_t)((i / S) & 1), s_dead, err)) break;
+            tc::fence_after();
+            const uint32_t ah = ptx::smem_u32(sm + s * sbytes), bh = ah + kATileBytes;
+            const uint32_t al = ah + hbytes, bl = al + kATileBytes;
+#pragma unroll
+            for (int kin = 0; kin < 4; ++kin) {
+                tc::mma_ss(tm, tc::desc_sw128(ah + kin * 32), tc::desc_sw128(bh + kin * 32), id,
+                           (i | kin) != 0 ? 1u : 0u);
+                tc::mma_ss(tm, tc::desc_sw128(ah + kin * 32), tc::desc_sw128(bl + kin * 32), id, 1u);
+                tc::mma_ss(tm, tc::desc_sw128(al + kin * 32), tc::desc_sw128(bh + kin * 32), id, 1u);
+            }
+            tc::commit(&empty[s]);
+        }
+        tc::commit(accb);   // completes once every MMA this thread issued has completed
+    } else if (warp >= 2) {
+        // Split warps: lo = a - trunc_tf32(a) for every element of the slice
+        // (same byte offsets, so the swizzle carries over), made visible to
+        // the tensor cores, then one arrival each on the stage's split barrier.
+        const int st = tid - 64;
+        const uint32_t n4 = hbytes / 16;
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % S;
+            if (!gwait(&full[s], (uint32_t)((i / S) & 1), s_dead, err)) break;
+            const uint4* hi = reinterpret_cast<const uint4*>(sm + s * sbytes);
+            uint4* lo = reinterpret_cast<uint4*>(sm + s * sbytes + hbytes);
+            for (uint32_t j = st; j < n4; j += kSplitThreads) {
+                const uint4 a = hi[j];
+                lo[j] = make_uint4(__float_as_uint(__uint_as_float(a.x) - __uint_as_float(a.x & 0xffffe000u)),
+                                   __float_as_uint(__uint_as_float(a.y) - __uint_as_float(a.y & 0xffffe000u)),
+                                   __float_as_uint(__uint_as_float(a.z) - __uint_as_float(a.z & 0xffffe000u)),
+                                   __float_as_uint(__uint_as_float(a.w) - __uint_as_float(a.w & 0xffffe000u)));
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&split[s]);
+        }
+    }
+
+    // Epilogue: TMEM lane = output row m, column = token; a warp stores 32
+    // consecutive rows of one token at a time.
+    const bool ok = gwait(accb, 0, s_dead, err);
+    tc::fence_after();
+    const int r = warp * 32 + lane;
+    const bool mrow = ok && arow + r < mrows;
+    const size_t ldo = (size_t)(g.M0 + g.M1);
+    float* out = g.out + (size_t)ks * g.N * ldo + mbase + r;
+    for (int c0 = 0; c0 < g.Nt; c0 += 32) {
+        uint32_t v[32];
+        tc::ld32(tc::taddr(tm, warp, c0), v);
+        tc::wait_ld();
+        if (mrow) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int n = n0 + c0 + j;
+                if (c0 + j < g.Nt && n < g.N) out[(size_t)n * ldo] = __uint_as_float(v[j]);
+            }
+        }
+    }
+
+    tc::fence_before();
+    const bool dead = __syncthreads_or(*(volatile int*)s_dead) != 0;
+    if (dead && tid == 0) {
+        // Give-up path: every slice the producer issued has landed (bounded
+        // waits) before the shared memory is released.
+        const int issued = *s_issued;
+        for (int s = 0; s < S && s < issued; ++s) {
+            const int uses = (issued - s + S - 1) / S;
+            ptx::mbar_wait_timed(&full[s], (uint32_t)((uses - 1) & 1));
+        }
+    }
+    __syncthreads();
+    if (warp == 0) tc::dealloc(tm, ncols);
+}
+
+// Partial sums of GEMM A over the K splits, in split order, into u [N][M0]
+// and beta_logit [N][M1].
+__global__ void kda_lowrank_reduce_kernel(const float* __restrict__ part, int splits, int N, int M0, int M1,
+                                          float* __restrict__ u, float* __restrict__ beta_logit) {
+    const size_t M = (size_t)(M0 + M1);
+    const size_t total = (size_t)N * M;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        float s = 0.0f;
+        for (int k = 0; k < splits; ++k) s += part[(size_t)k * total + i];
+        const size_t n = i / M, m = i - n * M;
+        if (m < (size_t)M0) u[n * M0 + m] = s;
+        else beta_logit[n * M1 + (m - M0)] = s;
+    }
+}
+
+std::atomic<bool> g_attr_done[64];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// Row-major fp32 [rows][K] seen as 2-D (K, rows), boxes of (32, box_rows),
+// 128-byte swizzle; rows and columns past the end read as zeros.
+bool make_map2d(CUtensorMap* m, const float* base, int K, int rows, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)kKStep, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int token_tile(int N) {
+    int t = 16;
+    while (t < N && t < 256) t <<= 1;
+    return t;
+}
+
+struct Plan {
+    int Nt, ntiles, tiles0, tiles1, kslice, splits;
+};
+
+// Tiling of C[N][M0 + M1] = [A0; A1] B^T: the K dimension is split so that
+// the grid holds about one CTA per SM, each split keeping at least four
+// 32-wide slices.
+Plan plan_gemm(int M0, int M1, int N, int K, int sm_count) {
+    Plan p{};
+    p.Nt = token_tile(N);
+    p.ntiles = (N + p.Nt - 1) / p.Nt;
+    p.tiles0 = (M0 + 127) / 128;
+    p.tiles1 = (M1 + 127) / 128;
+    const int ksteps = (K + kKStep - 1) / kKStep;
+    const int tiles = (p.tiles0 + p.tiles1) * p.ntiles;
+    int splits = (sm_count + tiles - 1) / tiles;
+    splits = max(1, min(splits, (ksteps + 3) / 4));
+    const int per = (ksteps + splits - 1) / splits;
+    p.kslice = per * kKStep;
+    p.splits = (K + p.kslice - 1) / p.kslice;   // no empty split
+    return p;
+}
+
+cudaError_t run_gemm(const Plan& pl, const GemmMaps& maps, int M0, int M1, int N, int K, float* out,
+                     const DeviceInfo& dev, int* err_word, cudaStream_t stream) {
+    GemmArgs g{M0, M1, pl.tiles0, N, K, pl.Nt, pl.kslice, ring_stages(pl.Nt), out};
+    const dim3 grid((unsigned)(pl.tiles0 + pl.tiles1), (unsigned)pl.ntiles, (unsigned)pl.splits);
+    kda_lowrank_gemm_kernel<<<grid, kThreads, gemm_smem_bytes(pl.Nt), stream>>>(g, err_word, maps);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+size_t align16(size_t b) { return (b + 15) & ~size_t(15); }
+
+}  // namespace
+
+size_t lowrank_workspace_bytes(const LayerParams& p, const LowRank& lr, const DeviceInfo& dev, int N) {
+    if (N <= 0) return 0;
+    const Plan pa = plan_gemm(lr.rank, p.H, N, lr.hidden, dev.sm_count);
+    return align16((size_t)pa.splits * N * (lr.rank + p.H) * 4) + align16((size_t)N * lr.rank * 4);
+}
+
+cudaError_t launch_lowrank(const LayerParams& p, const LowRank& lr, int N, const float* x, float* z,
+                           float* beta_logit, void* workspace, const DeviceInfo& dev, int* err_word,
+                           cudaStream_t stream) {
+    if (N <= 0) return cudaSuccess;
+    if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(kda_lowrank_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)gemm_smem_bytes(256));
+        if (e != cudaSuccess) return e;
+        if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device].store(true, std::memory_order_release);
+    }
+    const int H = p.H, HD = p.H * kHeadDim;
+    const Plan pa = plan_gemm(lr.rank, H, N, lr.hidden, dev.sm_count);
+    float* part = static_cast<float*>(workspace);
+    float* u = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                        align16((size_t)pa.splits * N * (lr.rank + H) * 4));
+    // GEMM A: [u | beta_logit] partial sums over the K splits.
+    GemmMaps ma{};
+    if (!make_map2d(&ma.a0, lr.W_fa, lr.hidden, lr.rank, 128) || !make_map2d(&ma.a1, lr.W_bp, lr.hidden, H, 128) ||
+        !make_map2d(&ma.b, x, lr.hidden, N, pa.Nt))
+        return cudaErrorInvalidValue;
+    cudaError_t e = run_gemm(pa, ma, lr.rank, H, N, lr.hidden, part, dev, err_word, stream);
+    if (e != cudaSuccess) return e;
+    // Reduce the splits.
+    {
+        const size_t total = (size_t)N * (lr.rank + H);
+        const size_t want = (total + 255) / 256, cap = (size_t)dev.sm_count * 8;
+        const unsigned blocks = (unsigned)(want < cap ? want : cap);
+        kda_lowrank_reduce_kernel<<<blocks, 256, 0, stream>>>(part, pa.splits, N, lr.rank, H, u, beta_logit);
+        count_launches(1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // GEMM C: z = W_fb u, one split (K = rank).
+    Plan pc = plan_gemm(HD, 0, N, lr.rank, dev.sm_count);
+    pc.kslice = ((lr.rank + kKStep - 1) / kKStep) * kKStep;
+    pc.splits = 1;
+    GemmMaps mc{};
+    if (!make_map2d(&mc.a0, lr.W_fb, lr.rank, HD, 128) || !make_map2d(&mc.b, u, lr.rank, N, pc.Nt))
+        return cudaErrorInvalidValue;
+    mc.a1 = mc.a0;
+    return run_gemm(pc, mc, HD, 0, N, lr.rank, z, dev, err_word, stream);
+}
+
+}  // namespace kda

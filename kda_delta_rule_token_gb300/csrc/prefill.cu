@@ -231,11 +231,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     float* s_part = s_rk + 64;                                    // [4][64] RMS partial sums
     float* s_gh0 = s_part + 256;                                  // [128] decay sum over tokens 0..31
     float* s_gh1 = s_gh0 + 128;                                   // [128] decay sum over tokens 32..63
+    float* s_gam = s_gh1 + 128;                                   // [128] gamma / 2 of this head
     float* s_win = reinterpret_cast<float*>(sm + OFF_WIN);        // [2][3][3][128], by chunk parity
     // mbarriers.  Each completes at most one phase per chunk and every thread
     // that waits on one waits on it once per chunk, so no waiter can fall two
     // phases behind (a parity wait would then alias onto a later phase).
-    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_gh1 + 128);   // MMA0 done
+    uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_gam + 128);   // MMA0 done
     uint64_t* s_tbar = s_bar + 1;                                 // input tiles landed
     uint64_t* s_gbar = s_bar + 2;                                 // gate tile landed
     uint64_t* s_tbarT = s_bar + 3;                                // MMA_T done
@@ -311,6 +312,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         *s_nt = 0;
         *s_ng = 0;
     }
+    if (tid < D) s_gam[tid] = 0.5f * p.gamma[h * D + tid];   // gamma sigmoid(g) = s_gam + s_gam tanh(g / 2)
     sync_tc();
     const uint32_t tm = *s_tmem;
     Waiter wt{s_bar, s_dead, err, 0u};
@@ -848,25 +850,6 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             tc::commit(s_bar2);
         }
-        // Under MMA2: each output-epilogue thread (lane quadrants 2, 3) turns
-        // the 32 gate values it reads later (token row r, box grp) into
-        // gamma * sigmoid(gate) in place; no other thread touches them, so
-        // this pass and the epilogue need no barrier between them.
-        if ((warp & 3) >= 2) {
-            wgate.wait();
-            const int r = qrow - C;
-            const uint32_t gbase = OFF_OG + grp * kOGBox + r * 128;
-            const float* gam = p.gamma + h * D + grp * 32;
-#pragma unroll 4
-            for (int cc = 0; cc < 8; ++cc) {   // 16-byte chunk cc of the row: channels 4 cc .. 4 cc + 3
-                float4 gm = *reinterpret_cast<const float4*>(gam + cc * 4);
-                gm.x *= 0.5f; gm.y *= 0.5f; gm.z *= 0.5f; gm.w *= 0.5f;   // gamma sigmoid(g) = gm + gm tanh(g / 2)
-                const uint32_t o = gbase + ((cc ^ (r & 7)) << 4);
-                const float4 gv = at<float4>(sm, o);
-                at<float4>(sm, o) = make_float4(fmaf(gm.x, tanhf_(0.5f * gv.x), gm.x), fmaf(gm.y, tanhf_(0.5f * gv.y), gm.y),
-                                                fmaf(gm.z, tanhf_(0.5f * gv.z), gm.z), fmaf(gm.w, tanhf_(0.5f * gv.w), gm.w));
-            }
-        }
         wt2.wait();   // MMA2
 
         // ---- F and the output epilogue, as two independent groups of 8 warps
@@ -920,17 +903,28 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             named_barrier_sync(3, 256);   // the four column groups' partial sums
             const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
                                          (1.0f / D) + p.rms_eps);
+            // The gate logits of this row (box grp) become gamma sigmoid(gate) here,
+            // by the thread that writes the output over them: no other thread
+            // reads or writes these 32 values.
+            wgate.wait();
             const uint32_t gbase = OFF_OG + grp * kOGBox + r * 128;   // row r of box grp (SW128)
+            const float* gam = s_gam + grp * 32;
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 const uint32_t* v = w + g8 * 8;
                 const uint32_t oa_at = gbase + (((2 * g8) ^ (r & 7)) << 4);
                 const uint32_t ob_at = gbase + (((2 * g8 + 1) ^ (r & 7)) << 4);
                 const float4 ga = at<float4>(sm, oa_at), gb = at<float4>(sm, ob_at);
-                const float4 oa = make_float4(ga.x * __uint_as_float(v[0]) * inv, ga.y * __uint_as_float(v[1]) * inv,
-                                              ga.z * __uint_as_float(v[2]) * inv, ga.w * __uint_as_float(v[3]) * inv);
-                const float4 ob = make_float4(gb.x * __uint_as_float(v[4]) * inv, gb.y * __uint_as_float(v[5]) * inv,
-                                              gb.z * __uint_as_float(v[6]) * inv, gb.w * __uint_as_float(v[7]) * inv);
+                const float4 ma = *reinterpret_cast<const float4*>(gam + g8 * 8);
+                const float4 mb = *reinterpret_cast<const float4*>(gam + g8 * 8 + 4);
+                const float4 oa = make_float4(fmaf(ma.x, tanhf_(0.5f * ga.x), ma.x) * (__uint_as_float(v[0]) * inv),
+                                              fmaf(ma.y, tanhf_(0.5f * ga.y), ma.y) * (__uint_as_float(v[1]) * inv),
+                                              fmaf(ma.z, tanhf_(0.5f * ga.z), ma.z) * (__uint_as_float(v[2]) * inv),
+                                              fmaf(ma.w, tanhf_(0.5f * ga.w), ma.w) * (__uint_as_float(v[3]) * inv));
+                const float4 ob = make_float4(fmaf(mb.x, tanhf_(0.5f * gb.x), mb.x) * (__uint_as_float(v[4]) * inv),
+                                              fmaf(mb.y, tanhf_(0.5f * gb.y), mb.y) * (__uint_as_float(v[5]) * inv),
+                                              fmaf(mb.z, tanhf_(0.5f * gb.z), mb.z) * (__uint_as_float(v[6]) * inv),
+                                              fmaf(mb.w, tanhf_(0.5f * gb.w), mb.w) * (__uint_as_float(v[7]) * inv));
                 if (!direct) {
                     at<float4>(sm, oa_at) = oa;
                     at<float4>(sm, ob_at) = ob;

@@ -14,6 +14,7 @@ namespace ptx {
 constexpr int kErrDecodeLoadWait = 1 << 0;
 constexpr int kErrPrefillWait = 1 << 1;
 constexpr int kErrTestingWait = 1 << 2;
+constexpr int kErrLowrankWait = 1 << 3;
 
 // Longest a kernel waits on one barrier phase before it reports an error.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
@@ -117,6 +118,16 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0,
         "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4, %5}], [%6];"
         ::"r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(m))
+        : "memory");
+}
+
+// Tiled TMA load of a 2-D box (coordinates innermost first) into shared
+// memory, completing its bytes on mbarrier m.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int c0, int c1, uint64_t* m) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(m))
         : "memory");
 }
 

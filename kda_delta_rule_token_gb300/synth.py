@@ -24,7 +24,13 @@ _IDS = {
     "conv_w": 1, "dt_bias": 2, "A_log": 3, "gamma": 4,
     "q": 10, "k": 11, "v": 12, "z": 13, "beta_logit": 14, "gate_logit": 15,
     "S0": 20, "conv0": 21,
+    "x": 30, "W_fa": 31, "W_fb": 32, "W_bp": 33,
 }
+
+# Low-rank front-end widths: the pages give none; the hidden width of the
+# Kimi K2 / K3 family (7168) and a rank of one head width (128).
+LOWRANK_HIDDEN = 7168
+LOWRANK_RANK = 128
 _WARM_OFFSET = 100
 
 
@@ -161,3 +167,23 @@ def sample_heads(wl: Workload, n: int) -> list[tuple[int, int]]:
         return [(0, 0)]
     idx = sorted({round(i * (total - 1) / (n - 1)) for i in range(n)})
     return [(p // wl.H, p % wl.H) for p in idx]
+
+
+def make_lowrank(wl: Workload, device="cpu", hidden: int = LOWRANK_HIDDEN, rank: int = LOWRANK_RANK,
+                 T: int | None = None) -> dict:
+    """Low-rank front-end weights and hidden inputs, fp32.
+
+    W_fa [rank, hidden] ~ N(0, 1/hidden), W_fb [H*d, rank] ~ N(0, 1/rank),
+    W_bp [H, hidden] ~ N(0, 1/hidden) and x ~ N(0, 1), so that z = W_fb W_fa x
+    and beta_logit = W_bp x come out about N(0, 1), the distribution the
+    workloads give those inputs directly.  x is [T, B, hidden] (call-major)
+    for decode workloads and [B, T, hidden] for prefill ones.
+    """
+    T = wl.T if T is None else T
+    H, d = wl.H, wl.d
+    W_fa = _normal((rank, hidden), hidden ** -0.5, 0.0, _gen(wl, "W_fa", device), device)
+    W_fb = _normal((H * d, rank), rank ** -0.5, 0.0, _gen(wl, "W_fb", device), device)
+    W_bp = _normal((H, hidden), hidden ** -0.5, 0.0, _gen(wl, "W_bp", device), device)
+    shp = (T, wl.B, hidden) if wl.mode == "decode" else (wl.B, T, hidden)
+    x = _normal(shp, 1.0, 0.0, _gen(wl, "x", device), device)
+    return {"W_fa": W_fa, "W_fb": W_fb, "W_bp": W_bp, "x": x, "hidden": hidden, "rank": rank}

@@ -32,7 +32,8 @@ def lib():
 def test_header_declares_the_api():
     names = declared_functions()
     for n in ("kda_create", "kda_decode_step", "kda_prefill", "kda_prefill_varlen", "kda_destroy",
-              "kda_strerror", "kda_prefill_workspace_bytes", "kda_sync_status"):
+              "kda_strerror", "kda_prefill_workspace_bytes", "kda_sync_status", "kda_bind_lowrank",
+              "kda_lowrank", "kda_decode_step_lowrank"):
         assert n in names
 
 
@@ -76,5 +77,10 @@ def test_host_side_rejections(lib):
     assert lib.kda_prefill_varlen(null, 1, 16, 1, *([16] * 9), null) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_sync_status(null, null) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_prefill_workspace_bytes(null, 1, 1) == 0
+    assert lib.kda_bind_lowrank(null, 64, 32, 16, 16, 16) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_lowrank(null, 1, 16, 16, 16, 16, 1 << 20, null) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_step_lowrank(null, 1, *([16] * 10), 1 << 20, null) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_lowrank_workspace_bytes(null, 8) == 0
+    assert lib.kda_decode_lowrank_workspace_bytes(null, 8) == 0
     lib.kda_destroy(null)  # ignored
 

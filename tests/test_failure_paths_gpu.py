@@ -151,3 +151,34 @@ def test_injection_is_off_when_unset(monkeypatch):
         assert kda.kda_sync_status(ctx) == kda.KDA_OK
     finally:
         kda.kda_destroy(ctx)
+
+
+def test_injected_lowrank_launch_failure(inject):
+    wl = synth.shrink(synth.WORKLOADS["decode_b64_h32_x256"], B=4, H=2, T=1)
+    params, tokens = synth.make_params(wl, DEV), synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    lr = synth.make_lowrank(wl, DEV, hidden=64, rank=32)
+    S, conv = st["S"], st["conv_state"]
+    S0, c0 = S.clone(), conv.clone()
+    inject("lowrank")
+    ctx = _create(wl, params)
+    try:
+        kda.kda_bind_lowrank(ctx, 64, 32, lr["W_fa"], lr["W_fb"], lr["W_bp"])
+        z = torch.full((4, 2, 128), 3.0, device=DEV)
+        bl = torch.full((4, 2), 3.0, device=DEV)
+        ws = torch.empty(kda.kda_decode_lowrank_workspace_bytes(ctx, 4), dtype=torch.uint8, device=DEV)
+        o = torch.full((4, 2, 128), 3.0, device=DEV)
+        n0 = kda.kda_launch_count()
+        with pytest.raises(kda.KDAError) as ei:
+            kda.kda_lowrank(ctx, 4, lr["x"][0], z, bl, ws)
+        assert ei.value.status == kda.KDA_ERR_CUDA
+        with pytest.raises(kda.KDAError) as ei:
+            kda.kda_decode_step_lowrank(ctx, 4, lr["x"][0], tokens["q"][0], tokens["k"][0], tokens["v"][0],
+                                        tokens["gate_logit"][0], conv, S, o, None, ws)
+        assert ei.value.status == kda.KDA_ERR_CUDA
+        assert kda.kda_launch_count() == n0
+        torch.cuda.synchronize()
+        assert bool((z == 3.0).all()) and bool((bl == 3.0).all()) and bool((o == 3.0).all())
+        assert torch.equal(S, S0) and torch.equal(conv, c0)
+    finally:
+        kda.kda_destroy(ctx)
