@@ -235,6 +235,38 @@ KDA_API size_t kda_lowrank_workspace_bytes(const kda_ctx *ctx, int N);
 KDA_API kda_status kda_lowrank(kda_ctx *ctx, int N, const float *x, float *z, float *beta_logit,
                                void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Size of the static device array kda_lowrank_noalloc keeps its scratch in
+ * (every GPU that loads this library holds it until the process exits).
+ */
+#define KDA_LOWRANK_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * kda_lowrank without a workspace argument.  The paper has no counterpart:
+ * this entry point exists for callers that cannot give the library device
+ * memory of its own for a call (a host runtime that passes a plugin only the
+ * layer's tensors and owns the rest of the device, or a serving loop that
+ * must not allocate once it runs).  Its scratch (the split-K partial sums
+ * and u) lives in one file-scope static device array of
+ * KDA_LOWRANK_NOALLOC_SCRATCH_BYTES; it calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   x, z, beta_logit   as for kda_lowrank
+ * A call whose scratch would exceed the array (it grows with N, rank and H;
+ * the K split count is lowered first to make it fit) returns
+ * KDA_ERR_INVALID_ARG, launches nothing, and kda_last_error_detail gives the
+ * bytes needed and the limit.  The result equals kda_lowrank's within
+ * rounding (the K split count may differ, so the order of the partial sums
+ * may too).
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with the context's device current); make that
+ * first call before any stream capture.  All calls on a device share the
+ * array and it keeps the last call's contents: calls that overlap on the GPU
+ * (on different streams, or not ordered by one stream) race on it.  N == 0
+ * is a no-op.
+ */
+KDA_API kda_status kda_lowrank_noalloc(kda_ctx *ctx, int N, const float *x, float *z,
+                                       float *beta_logit, void *stream);
+
 /* Bytes of device workspace kda_decode_step_lowrank needs for B sequences. */
 KDA_API size_t kda_decode_lowrank_workspace_bytes(const kda_ctx *ctx, int B);
 

@@ -17,7 +17,8 @@ __all__ = [
     "KDAError", "load", "kda_create", "kda_destroy", "kda_strerror", "kda_last_error_detail",
     "kda_decode_step", "kda_prefill", "kda_prefill_varlen", "kda_prefill_workspace_bytes", "kda_sync_status",
     "kda_launch_count", "kda_bind_lowrank", "kda_lowrank", "kda_lowrank_workspace_bytes",
-    "kda_decode_step_lowrank", "kda_decode_lowrank_workspace_bytes", "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_ALIGNMENT",
+    "kda_decode_step_lowrank", "kda_decode_lowrank_workspace_bytes", "kda_lowrank_noalloc",
+    "LOWRANK_NOALLOC_SCRATCH_BYTES", "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_ALIGNMENT",
     "KDA_ERR_UNSUPPORTED", "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "HEAD_DIM", "CHUNK",
 ]
 
@@ -25,6 +26,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_ALIGNMENT, KDA_ERR_UNSUPPORTED, KDA_ERR_CUD
     KDA_ERR_TIMEOUT = range(6)
 HEAD_DIM = 128
 CHUNK = 64
+LOWRANK_NOALLOC_SCRATCH_BYTES = 4 << 20   # KDA_LOWRANK_NOALLOC_SCRATCH_BYTES of include/kda.h
 
 _lib = None
 
@@ -92,6 +94,8 @@ def load(path: str | None = None):
     lib.kda_decode_lowrank_workspace_bytes.restype = sz
     lib.kda_decode_step_lowrank.argtypes = [vp, i32] + [vp] * 10 + [sz, vp]
     lib.kda_decode_step_lowrank.restype = i32
+    lib.kda_lowrank_noalloc.argtypes = [vp, i32, vp, vp, vp, vp]
+    lib.kda_lowrank_noalloc.restype = i32
     lib.kda_testing_bounded_wait.argtypes = [vp, ctypes.c_uint, vp]
     lib.kda_testing_bounded_wait.restype = i32
     _lib = lib
@@ -194,6 +198,13 @@ def kda_lowrank_workspace_bytes(ctx, N) -> int:
 def kda_lowrank(ctx, N, x, z, beta_logit, workspace, workspace_bytes=0, stream=None) -> None:
     _check(load().kda_lowrank(ctx, int(N), _p(x), _p(z), _p(beta_logit), _p(workspace),
                               _nbytes(workspace, workspace_bytes), _stream(stream)), "kda_lowrank")
+
+
+def kda_lowrank_noalloc(ctx, N, x, z, beta_logit, stream=None) -> None:
+    """The front-end with its scratch in the library's static device array
+    (no workspace argument; see kda.h)."""
+    _check(load().kda_lowrank_noalloc(ctx, int(N), _p(x), _p(z), _p(beta_logit), _stream(stream)),
+           "kda_lowrank_noalloc")
 
 
 def kda_decode_lowrank_workspace_bytes(ctx, B) -> int:

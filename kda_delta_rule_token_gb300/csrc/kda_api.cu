@@ -323,6 +323,34 @@ kda_status kda_lowrank(kda_ctx* ctx, int N, const float* x, float* z, float* bet
     return KDA_OK;
 }
 
+kda_status kda_lowrank_noalloc(kda_ctx* ctx, int N, const float* x, float* z, float* beta_logit, void* stream) {
+    if (!ctx || N < 0) return KDA_ERR_INVALID_ARG;
+    if (!ctx->has_lowrank) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail), "no low-rank weights bound (kda_bind_lowrank)");
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (N == 0) return KDA_OK;
+    if (!x || !z || !beta_logit) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(z) || !aligned4(beta_logit)) return KDA_ERR_ALIGNMENT;
+    const size_t need = kda::lowrank_noalloc_need(ctx->params, ctx->lowrank, ctx->dev, N);
+    if (need > (size_t)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail),
+                      "kda_lowrank_noalloc: %d tokens need %zu bytes of scratch, more than its static %u-byte array",
+                      N, need, (unsigned)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES);
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
+    cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectLowrank, [&] {
+        return kda::launch_lowrank_noalloc(ctx->params, ctx->lowrank, N, x, z, beta_logit, ctx->dev, ctx->err_word,
+                                           static_cast<cudaStream_t>(stream));
+    });
+    if (e != cudaSuccess) {
+        kda::set_launch_detail(ctx, kda::kInjectLowrank, "lowrank_noalloc launch", e);
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
 // Workspace of kda_decode_step_lowrank: the front-end's own, then z [B][H][d]
 // and beta_logit [B][H].
 static size_t decode_lowrank_parts(const kda_ctx* ctx, int B, size_t* off_z, size_t* off_b) {

@@ -86,6 +86,13 @@ cudaError_t launch_lowrank(const LayerParams& p, const LowRank& lr, int N, const
                            float* beta_logit, void* workspace, const DeviceInfo& dev, int* err_word,
                            cudaStream_t stream);
 
+// The front-end with its scratch in a static device array (csrc/lowrank.cu):
+// bytes of that array a call for N tokens needs (more than
+// KDA_LOWRANK_NOALLOC_SCRATCH_BYTES: the call cannot run), and the launch.
+size_t lowrank_noalloc_need(const LayerParams& p, const LowRank& lr, const DeviceInfo& dev, int N);
+cudaError_t launch_lowrank_noalloc(const LayerParams& p, const LowRank& lr, int N, const float* x, float* z,
+                                   float* beta_logit, const DeviceInfo& dev, int* err_word, cudaStream_t stream);
+
 // Test hook (csrc/testing.cu): a kernel whose bounded wait runs out.
 cudaError_t launch_testing_wait(int* err_word, unsigned long long limit_ns, cudaStream_t stream);
 

@@ -42,6 +42,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "kda_internal.cuh"
 #include "ptx.cuh"
@@ -350,6 +351,116 @@ cudaError_t launch_lowrank(const LayerParams& p, const LowRank& lr, int N, const
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // GEMM C: z = W_fb u, one split (K = rank).
+    Plan pc = plan_gemm(HD, 0, N, lr.rank, dev.sm_count);
+    pc.kslice = ((lr.rank + kKStep - 1) / kKStep) * kKStep;
+    pc.splits = 1;
+    GemmMaps mc{};
+    if (!make_map2d(&mc.a0, lr.W_fb, lr.rank, HD, 128) || !make_map2d(&mc.b, u, lr.rank, N, pc.Nt))
+        return cudaErrorInvalidValue;
+    mc.a1 = mc.a0;
+    return run_gemm(pc, mc, HD, 0, N, lr.rank, z, dev, err_word, stream);
+}
+
+
+// ---------------------------------------------------------------------------
+// The front-end without a caller-supplied workspace (kda_lowrank_noalloc).
+//
+// Some callers cannot hand this library a workspace: a host runtime that
+// passes a plugin only the tensors of the layer and owns every other byte of
+// device memory, or a serving loop that must not allocate once it runs.  For
+// them the front-end's scratch (the split-K partial sums and u) lives in one
+// file-scope array of static device memory that comes with the library.
+// Every GPU that loads the library holds the array until the process exits,
+// so it is kept to KDA_LOWRANK_NOALLOC_SCRATCH_BYTES (4 MiB); a call whose
+// scratch would not fit is rejected on the host.  All calls share the
+// array: two calls that overlap on the GPU (different streams, or a second
+// call before the first has finished on another stream) race on it.  It
+// needs no clearing: every element a call reads was written earlier in the
+// same call.
+namespace {
+
+static __device__ __align__(256) uint8_t g_lowrank_scratch[KDA_LOWRANK_NOALLOC_SCRATCH_BYTES];
+
+// Host address of the array on each device, looked up once per device with
+// that device current (the array's name in host code is only a stand-in).
+struct ScratchAddr {
+    std::once_flag once;
+    void* ptr = nullptr;
+    cudaError_t err = cudaSuccess;
+};
+ScratchAddr g_scratch_addr[64];
+
+// The plan of kda_lowrank, with the K split count lowered when the partial
+// sums would not fit beside u in the static array.  Returns false when even
+// one split does not fit.
+bool plan_noalloc(const LayerParams& p, const LowRank& lr, const DeviceInfo& dev, int N, Plan* out,
+                  size_t* need) {
+    Plan pa = plan_gemm(lr.rank, p.H, N, lr.hidden, dev.sm_count);
+    const size_t ub = align16((size_t)N * lr.rank * 4);
+    const size_t per_split = (size_t)N * (lr.rank + p.H) * 4;
+    *need = align16((size_t)pa.splits * per_split) + ub;
+    if (*need > (size_t)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES) {
+        const size_t room = (size_t)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES > ub + 16
+                                ? (size_t)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES - ub - 16 : 0;
+        const int cap = (int)(room / per_split);
+        if (cap < 1) {
+            *need = align16(per_split) + ub;
+            return false;
+        }
+        const int ksteps = (lr.hidden + kKStep - 1) / kKStep;
+        const int per = (ksteps + cap - 1) / cap;
+        pa.kslice = per * kKStep;
+        pa.splits = (lr.hidden + pa.kslice - 1) / pa.kslice;
+        *need = align16((size_t)pa.splits * per_split) + ub;
+    }
+    *out = pa;
+    return true;
+}
+
+}  // namespace
+
+size_t lowrank_noalloc_need(const LayerParams& p, const LowRank& lr, const DeviceInfo& dev, int N) {
+    Plan pa;
+    size_t need = 0;
+    plan_noalloc(p, lr, dev, N, &pa, &need);
+    return need;
+}
+
+cudaError_t launch_lowrank_noalloc(const LayerParams& p, const LowRank& lr, int N, const float* x, float* z,
+                                   float* beta_logit, const DeviceInfo& dev, int* err_word, cudaStream_t stream) {
+    if (N <= 0) return cudaSuccess;
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    ScratchAddr& sa = g_scratch_addr[dev.device];
+    std::call_once(sa.once, [&] { sa.err = cudaGetSymbolAddress(&sa.ptr, g_lowrank_scratch); });
+    if (sa.err != cudaSuccess) return sa.err;
+    if (!sa.ptr) return cudaErrorInvalidSymbol;
+    Plan pa;
+    size_t need = 0;
+    if (!plan_noalloc(p, lr, dev, N, &pa, &need)) return cudaErrorInvalidValue;   // the host checked the size
+    if (!g_attr_done[dev.device].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(kda_lowrank_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)gemm_smem_bytes(256));
+        if (e != cudaSuccess) return e;
+        g_attr_done[dev.device].store(true, std::memory_order_release);
+    }
+    const int H = p.H, HD = p.H * kHeadDim;
+    float* part = static_cast<float*>(sa.ptr);
+    float* u = reinterpret_cast<float*>(static_cast<uint8_t*>(sa.ptr) +
+                                        align16((size_t)pa.splits * N * (lr.rank + H) * 4));
+    GemmMaps ma{};
+    if (!make_map2d(&ma.a0, lr.W_fa, lr.hidden, lr.rank, 128) || !make_map2d(&ma.a1, lr.W_bp, lr.hidden, H, 128) ||
+        !make_map2d(&ma.b, x, lr.hidden, N, pa.Nt))
+        return cudaErrorInvalidValue;
+    cudaError_t e = run_gemm(pa, ma, lr.rank, H, N, lr.hidden, part, dev, err_word, stream);
+    if (e != cudaSuccess) return e;
+    {
+        const size_t total = (size_t)N * (lr.rank + H);
+        const size_t want = (total + 255) / 256, cap = (size_t)dev.sm_count * 8;
+        const unsigned blocks = (unsigned)(want < cap ? want : cap);
+        kda_lowrank_reduce_kernel<<<blocks, 256, 0, stream>>>(part, pa.splits, N, lr.rank, H, u, beta_logit);
+        count_launches(1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     Plan pc = plan_gemm(HD, 0, N, lr.rank, dev.sm_count);
     pc.kslice = ((lr.rank + kKStep - 1) / kKStep) * kKStep;
     pc.splits = 1;
