@@ -770,6 +770,8 @@ def main():
                     help="profiling only: time this prefill workload alone")
     ap.add_argument("--decode-workload", default=None,
                     help="profiling only: time this decode workload alone (no e2e, no graph)")
+    ap.add_argument("--lowrank-only", action="store_true",
+                    help="profiling only: time the low-rank front-end decode line alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-split", type=int, default=2,
                     help="groups of sequences the decode end-to-end step is pipelined over")
@@ -782,8 +784,11 @@ def main():
 
     ours = Ours(args, world, rank, local)
     peaks = load_peaks()
-    if args.prefill_workload or args.decode_workload:   # profiling runs: one workload alone
+    if args.prefill_workload or args.decode_workload or args.lowrank_only:   # profiling runs
         out = {"profiling_only": True}
+        if args.lowrank_only:
+            r = ours.decode_lowrank(DECODE_WL)
+            out.update(lowrank_step_ms=round(r["ms_step"], 5), lowrank_frontend_ms=round(r["ms_frontend"], 5))
         if args.prefill_workload:
             r = ours.prefill(args.prefill_workload, e2e=False)
             out.update(prefill_workload=args.prefill_workload, prefill_ms=round(r["ms"], 4))

@@ -192,6 +192,12 @@ __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrive on named barrier `id` without waiting for it (the threads that
+// need the arrivals' earlier shared-memory writes bar.sync on it).
+__device__ __forceinline__ void named_barrier_arrive(int id, int count) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void sync_tc() {
     tc::fence_before();
     __syncthreads();
@@ -279,10 +285,13 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     // back as zeros).  q, k, z land in the S^T operand region and may be
     // issued once MMA1 has read it; v lands in the Minv^T region and may be
     // issued once MMA_T has read it.  One barrier phase covers all four.
-    // After a bounded wait gave up (*s_dead), no new copy or MMA is issued.
-    auto alive = [&]() { return *(volatile int*)s_dead == 0; };
+    // Staged copies and MMAs are issued without looking at *s_dead (a shared
+    // load on the issuing thread's path measurably slows every chunk); after
+    // a bounded wait gave up, the CTA leaves at the end of that chunk (the
+    // vote at the loop's end) and drains what it issued before returning.
+    // The counts of issued tile phases let the drain wait for the last ones.
     auto stage_qkz = [&](int ci) {
-        if (tid == kStager && alive()) {
+        if (tid == kStager) {
             ++*s_nt;
             ptx::mbar_arrive_expect_tx(s_tbar, kStageBytes);
             ptx::tma_load_4d(sm + STG_Q, &maps.q, 0, h, tb0 + ci * C, bmap, s_tbar);
@@ -291,12 +300,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             ptx::tma_prefetch_4d(&maps.v, 0, h, tb0 + ci * C, bmap);   // v lands later; have it in L2
         }
     };
-    // v joins the phase stage_qkz opened for the same chunk, and only if that
-    // phase was opened (for ci > 0 a block barrier separates the two issues,
-    // so the count written by the stager is visible here).
-    auto stage_v = [&](int ci) {
-        if (tid == 0 && alive() && (ci == 0 || *(volatile int*)s_nt == ci + 1))
-            ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, tb0 + ci * C, bmap, s_tbar);
+    auto stage_v = [&](int ci) {   // joins the phase stage_qkz opened for the same chunk
+        if (tid == 0) ptx::tma_load_4d(sm + STG_V, &maps.v, 0, h, tb0 + ci * C, bmap, s_tbar);
     };
     if (tid == 0) {
         ptx::mbar_init(s_bar, 1);
@@ -609,7 +614,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         publish();
 
         // ---- MMA0: [A'; P] = L R^T.
-        if (!fb && tid == 0 && alive()) {
+        if (!fb && tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll 1
             for (int ks = 0; ks < D / 8; ++ks) {
@@ -634,7 +639,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             if (half == 1) tc::commit(s_bar1);
         };
-        if (tid == kIssuer1 && alive()) mma1_part(0);
+        if (tid == kIssuer1) mma1_part(0);
         if (!fb) wt.wait();   // MMA0
 
         // ---- C1: N = Diag(beta) A' to shared memory as N^T (row b holds
@@ -664,7 +669,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         tc::wait_st();
         sync_tc();
 
-        if (tid == kIssuer1 && alive()) mma1_part(1);
+        if (tid == kIssuer1) mma1_part(1);
 
         // ---- C2: Minv = (I + N)^{-1} (N strictly lower) by 16 x 16 blocks.
         //      Pass 1: forward substitution with the diagonal block I + N_II
@@ -767,7 +772,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 }
                 // ---- MMA_T: [Minv; P Minv] = [I; P] Minv, issued by the warp that
                 //      wrote the last block (runs under the rest of the X epilogue).
-                if (tid == kIssuerB && alive()) {
+                if (tid == kIssuerB) {
                     tc::fence_after();
                     constexpr uint32_t id = tc::idesc_tf32(128, 64);
 #pragma unroll 1
@@ -783,8 +788,6 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         wt1.wait();   // MMA1
         if (tid == kStager) {
             if (ci + 1 < nchunks) stage_qkz(ci + 1);   // the S^T region is free now
-        }
-        if (tid == kStager && alive()) {
             // this chunk's gate tile into the upper half of the L region
             ++*s_ng;
             ptx::mbar_arrive_expect_tx(s_gbar, C * D * 4);
@@ -840,7 +843,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
 
         // ---- MMA2: D1 += [Minv; P Minv] Diag(beta) X = [U; P U] (N = 128: a
         //      tf32 MMA costs about the same per instruction at N = 64 and 128).
-        if (tid == 0 && alive()) {
+        if (tid == 0) {
             constexpr uint32_t id = tc::idesc_tf32(128, 128);
 #pragma unroll 1
             for (int ks = 0; ks < C / 8; ++ks) {
@@ -850,6 +853,25 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             tc::commit(s_bar2);
         }
+        // Under MMA2: the gate tile becomes gamma * sigmoid(gate) in place, rows
+        // spread over warps 1..15 (warp 0 issued MMA2).  The output epilogue
+        // (lane quadrants 2, 3) reads rows written by every warp, so it syncs
+        // on named barrier 4, on which the U-operand warps (quadrants 0, 1)
+        // only arrive: their own path to MMA3 does not wait for the O rows.
+        wgate.wait();
+        if (warp > 0) {   // lane = (box, 16-byte chunk) of a row: channels 4 lane .. 4 lane + 3
+            const int box = lane >> 3, ch = lane & 7;
+            const float4 gm = *reinterpret_cast<const float4*>(s_gam + lane * 4);
+#pragma unroll 1
+            for (int r = warp - 1; r < C; r += 15) {
+                const uint32_t o = OFF_OG + box * kOGBox + r * 128 + ((ch ^ (r & 7)) << 4);
+                const float4 gv = at<float4>(sm, o);
+                at<float4>(sm, o) = make_float4(fmaf(gm.x, tanhf_(0.5f * gv.x), gm.x), fmaf(gm.y, tanhf_(0.5f * gv.y), gm.y),
+                                                fmaf(gm.z, tanhf_(0.5f * gv.z), gm.z), fmaf(gm.w, tanhf_(0.5f * gv.w), gm.w));
+            }
+        }
+        if ((warp & 3) < 2) named_barrier_arrive(4, kThreads);
+        else named_barrier_sync(4, kThreads);
         wt2.wait();   // MMA2
 
         // ---- F and the output epilogue, as two independent groups of 8 warps
@@ -877,7 +899,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             tc::fence_before();
             named_barrier_sync(2, 256);   // U operand complete
             // ---- MMA3 (overlaps the output epilogue): M += R^T U.
-            if (tid == 0 && alive()) {
+            if (tid == 0) {
                 tc::fence_after();
                 constexpr uint32_t id = tc::idesc_tf32(128, 128);
 #pragma unroll 1
@@ -903,28 +925,17 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             named_barrier_sync(3, 256);   // the four column groups' partial sums
             const float inv = rsqrtf((s_part[r] + s_part[C + r] + s_part[2 * C + r] + s_part[3 * C + r]) *
                                          (1.0f / D) + p.rms_eps);
-            // The gate logits of this row (box grp) become gamma sigmoid(gate) here,
-            // by the thread that writes the output over them: no other thread
-            // reads or writes these 32 values.
-            wgate.wait();
             const uint32_t gbase = OFF_OG + grp * kOGBox + r * 128;   // row r of box grp (SW128)
-            const float* gam = s_gam + grp * 32;
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
                 const uint32_t* v = w + g8 * 8;
                 const uint32_t oa_at = gbase + (((2 * g8) ^ (r & 7)) << 4);
                 const uint32_t ob_at = gbase + (((2 * g8 + 1) ^ (r & 7)) << 4);
                 const float4 ga = at<float4>(sm, oa_at), gb = at<float4>(sm, ob_at);
-                const float4 ma = *reinterpret_cast<const float4*>(gam + g8 * 8);
-                const float4 mb = *reinterpret_cast<const float4*>(gam + g8 * 8 + 4);
-                const float4 oa = make_float4(fmaf(ma.x, tanhf_(0.5f * ga.x), ma.x) * (__uint_as_float(v[0]) * inv),
-                                              fmaf(ma.y, tanhf_(0.5f * ga.y), ma.y) * (__uint_as_float(v[1]) * inv),
-                                              fmaf(ma.z, tanhf_(0.5f * ga.z), ma.z) * (__uint_as_float(v[2]) * inv),
-                                              fmaf(ma.w, tanhf_(0.5f * ga.w), ma.w) * (__uint_as_float(v[3]) * inv));
-                const float4 ob = make_float4(fmaf(mb.x, tanhf_(0.5f * gb.x), mb.x) * (__uint_as_float(v[4]) * inv),
-                                              fmaf(mb.y, tanhf_(0.5f * gb.y), mb.y) * (__uint_as_float(v[5]) * inv),
-                                              fmaf(mb.z, tanhf_(0.5f * gb.z), mb.z) * (__uint_as_float(v[6]) * inv),
-                                              fmaf(mb.w, tanhf_(0.5f * gb.w), mb.w) * (__uint_as_float(v[7]) * inv));
+                const float4 oa = make_float4(ga.x * __uint_as_float(v[0]) * inv, ga.y * __uint_as_float(v[1]) * inv,
+                                              ga.z * __uint_as_float(v[2]) * inv, ga.w * __uint_as_float(v[3]) * inv);
+                const float4 ob = make_float4(gb.x * __uint_as_float(v[4]) * inv, gb.y * __uint_as_float(v[5]) * inv,
+                                              gb.z * __uint_as_float(v[6]) * inv, gb.w * __uint_as_float(v[7]) * inv);
                 if (!direct) {
                     at<float4>(sm, oa_at) = oa;
                     at<float4>(sm, ob_at) = ob;
@@ -936,7 +947,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             ptx::fence_proxy_async_smem();
             named_barrier_sync(3, 256);   // the o tile is complete
-            if (tid == kOStore && !direct && alive()) {
+            if (tid == kOStore && !direct) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     ptx::tma_store_4d(&maps.o, j * 32, h, tb0 + t0, bmap, sm + OFF_OG + j * kOGBox);
