@@ -292,7 +292,17 @@ kda_status kda_bind_lowrank(kda_ctx* ctx, int hidden, int rank, const float* W_f
         return KDA_ERR_INVALID_ARG;
     }
     if (!aligned16(W_fa) || !aligned16(W_fb) || !aligned16(W_bp)) return KDA_ERR_ALIGNMENT;
-    ctx->lowrank = kda::LowRank{hidden, rank, W_fa, W_fb, W_bp};
+    kda::LowRank lr{};
+    lr.hidden = hidden;
+    lr.rank = rank;
+    lr.W_fa = W_fa;
+    lr.W_fb = W_fb;
+    lr.W_bp = W_bp;
+    if (!kda::lowrank_prepare(ctx->params, lr)) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail), "cuTensorMapEncodeTiled failed for the low-rank weights");
+        return KDA_ERR_CUDA;
+    }
+    ctx->lowrank = lr;
     ctx->has_lowrank = true;
     return KDA_OK;
 }

@@ -2,6 +2,7 @@
 // library.  Nothing here is part of the public C ABI (include/kda.h).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -55,13 +56,16 @@ struct PrefillIO {
     size_t workspace_bytes;
 };
 
-// Low-rank front-end weights bound to a context (borrowed, fp32).
+// Low-rank front-end weights bound to a context (borrowed, fp32), with
+// their TMA tensor maps (encoded once, at binding, by lowrank_prepare).
 struct LowRank {
     int hidden;           // width of the hidden input x
     int rank;             // inner width of W_fb W_fa
     const float* W_fa;    // [rank][hidden]
     const float* W_fb;    // [H*d][rank]
     const float* W_bp;    // [H][hidden]
+    bool maps_ready;
+    CUtensorMap map_fa, map_bp, map_fb;
 };
 
 // Device facts the launchers need, queried once per context.
@@ -81,6 +85,8 @@ cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const Devi
 
 // Low-rank front-end (csrc/lowrank.cu): z [N][H*d] and beta_logit [N][H] of
 // N tokens of hidden input x [N][hidden]; workspace of lowrank_workspace_bytes.
+// lowrank_prepare encodes the weights' tensor maps (false if it cannot).
+bool lowrank_prepare(const LayerParams& p, LowRank& lr);
 size_t lowrank_workspace_bytes(const LayerParams& p, const LowRank& lr, const DeviceInfo& dev, int N);
 cudaError_t launch_lowrank(const LayerParams& p, const LowRank& lr, int N, const float* x, float* z,
                            float* beta_logit, void* workspace, const DeviceInfo& dev, int* err_word,

@@ -31,13 +31,15 @@
 // fp32 operand as its tf32 truncation, so the TMA-landed tile serves as hi;
 // two warps write lo = a - hi beside it.
 //
-// A CTA owns a 128-row tile of A, an N tile of up to 256 tokens and one K
-// split; one thread streams 32-wide K slices of both operands with TMA
-// (128-byte swizzle) through a ring of stages, warps 2-3 form the lo parts
-// of each landed slice, one thread issues the kind::tf32 MMAs (M = 128,
-// N = the tile, 3 x 4 per slice) and releases the stage with a commit, and
-// all four warps read the accumulator back (TMEM lane = output row) and
-// store it token-major, so a warp writes 128 contiguous bytes per token.
+// A CTA owns a 128-row tile of A, an N tile of 32 to 256 tokens and one K
+// split; one thread (warp 0) streams 32-wide K slices of both operands with
+// TMA (128-byte swizzle) through a ring of stages, warps 2-5 form the lo
+// parts of each landed slice, one thread (warp 1) issues the kind::tf32 MMAs
+// (M = 128, N = the tile, 3 x 4 per slice) and releases the stage with a
+// commit.  Warps 2-5 then read the accumulator back (TMEM lane = output
+// row), transpose it through shared memory and store it token-major with
+// 16-byte stores, a row of 128 outputs (512 contiguous bytes) per token.
+// The weights' tensor maps are encoded once, when the weights are bound.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -55,7 +57,8 @@ constexpr int kMaxStages = 4;
 constexpr uint32_t kStageBudget = 200 * 1024;    // shared memory for the ring
 constexpr int kKStep = 32;                       // fp32 elements in one 128-byte swizzled row
 constexpr uint32_t kATileBytes = 128 * 128;      // 128 rows x 128 bytes
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;                    // warp 0 TMA, warp 1 MMA, warps 2-5 split + epilogue
+constexpr int kSplitThreads = 128;
 
 struct GemmMaps {
     CUtensorMap a0, a1;   // weights, (K, rows) with boxes of (32, 128)
@@ -63,13 +66,13 @@ struct GemmMaps {
 };
 
 struct GemmArgs {
-    int M0, M1;     // rows of the first and second weight matrix (M1 = 0: none)
-    int tiles0;     // 128-row tiles of the first matrix
+    int tiles0;     // 128-row tiles taken from the first weight matrix (the rest from the second)
     int N, K;
-    int Nt;         // token tile: 16, 32, 64, 128 or 256
+    int Nt;         // token tile: 32, 64, 128 or 256
     int kslice;     // K elements per split, a multiple of 32
     int stages;     // depth of the ring
-    float* out;     // [splits][N][M0 + M1]
+    int ldo;        // row stride of the output: 128 x (number of 128-row tiles)
+    float* out;     // [splits][N][ldo]; tile t owns columns [128 t, 128 t + 128)
 };
 
 // A stage: A hi, B hi (TMA), then A lo, B lo (split warps); each part a
@@ -80,7 +83,6 @@ constexpr int ring_stages(int Nt) {
     return (int)(kStageBudget / stage_bytes(Nt)) < kMaxStages ? (int)(kStageBudget / stage_bytes(Nt)) : kMaxStages;
 }
 constexpr uint32_t gemm_smem_bytes(int Nt) { return ring_stages(Nt) * stage_bytes(Nt) + 1024; }
-constexpr int kSplitThreads = 64;   // warps 2 and 3
 
 // Bounded wait shared by the roles of the GEMM CTA: gives up after the wall
 // time limit (or at once when another thread already gave up), marks the CTA
@@ -91,6 +93,10 @@ __device__ __forceinline__ bool gwait(uint64_t* bar, uint32_t parity, int* dead,
     *(volatile int*)dead = 1;
     atomicOr(err, ptx::kErrLowrankWait);
     return false;
+}
+
+__device__ __forceinline__ uint32_t lo_part(uint32_t a) {
+    return __float_as_uint(__uint_as_float(a) - __uint_as_float(a & 0xffffe000u));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -105,18 +111,16 @@ kda_lowrank_gemm_kernel(const GemmArgs g, int* err, const __grid_constant__ Gemm
     uint64_t* accb = empty + kMaxStages;                             // accumulator complete
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(accb + 1);
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
-    int* s_issued = s_dead + 1;                                            // slices the producer issued
+    int* s_issued = s_dead + 1;                                      // slices the producer issued
 
     const int mt = blockIdx.x, nt = blockIdx.y, ks = blockIdx.z;
     const bool second = mt >= g.tiles0;
     const int arow = (second ? mt - g.tiles0 : mt) * 128;    // first row of the tile in its matrix
-    const int mrows = second ? g.M1 : g.M0;                  // rows of that matrix
-    const int mbase = second ? g.M0 + arow : arow;           // output row of TMEM lane 0
     const int n0 = nt * g.Nt;
     const int k0 = ks * g.kslice;
     const int k1 = min(g.K, k0 + g.kslice);
     const int nk = (k1 - k0 + kKStep - 1) / kKStep;          // >= 1: the host makes no empty split
-    const uint32_t ncols = g.Nt < 32 ? 32u : (uint32_t)g.Nt;
+    const uint32_t ncols = (uint32_t)g.Nt;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -171,74 +175,111 @@ kda_lowrank_gemm_kernel(const GemmArgs g, int* err, const __grid_constant__ Gemm
     } else if (warp >= 2) {
         // Split warps: lo = a - trunc_tf32(a) for every element of the slice
         // (same byte offsets, so the swizzle carries over), made visible to
-        // the tensor cores, then one arrival each on the stage's split barrier.
-        const int st = tid - 64;
+        // the tensor cores, then one arrival each on the stage's split
+        // barrier.  Four 16-byte words per thread are loaded before any of
+        // them is stored.
+        const uint32_t t = (uint32_t)(tid - 64);
         const uint32_t n4 = hbytes / 16;
         for (int i = 0; i < nk; ++i) {
             const int s = i % S;
             if (!gwait(&full[s], (uint32_t)((i / S) & 1), s_dead, err)) break;
             const uint4* hi = reinterpret_cast<const uint4*>(sm + s * sbytes);
             uint4* lo = reinterpret_cast<uint4*>(sm + s * sbytes + hbytes);
-            for (uint32_t j = st; j < n4; j += kSplitThreads) {
-                const uint4 a = hi[j];
-                lo[j] = make_uint4(__float_as_uint(__uint_as_float(a.x) - __uint_as_float(a.x & 0xffffe000u)),
-                                   __float_as_uint(__uint_as_float(a.y) - __uint_as_float(a.y & 0xffffe000u)),
-                                   __float_as_uint(__uint_as_float(a.z) - __uint_as_float(a.z & 0xffffe000u)),
-                                   __float_as_uint(__uint_as_float(a.w) - __uint_as_float(a.w & 0xffffe000u)));
+            for (uint32_t j = t; j < n4; j += 4 * kSplitThreads) {
+                uint4 a[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (j + q * kSplitThreads < n4) a[q] = hi[j + q * kSplitThreads];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (j + q * kSplitThreads < n4)
+                        lo[j + q * kSplitThreads] =
+                            make_uint4(lo_part(a[q].x), lo_part(a[q].y), lo_part(a[q].z), lo_part(a[q].w));
             }
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(&split[s]);
         }
     }
 
-    // Epilogue: TMEM lane = output row m, column = token; a warp stores 32
-    // consecutive rows of one token at a time.
-    const bool ok = gwait(accb, 0, s_dead, err);
-    tc::fence_after();
-    const int r = warp * 32 + lane;
-    const bool mrow = ok && arow + r < mrows;
-    const size_t ldo = (size_t)(g.M0 + g.M1);
-    float* out = g.out + (size_t)ks * g.N * ldo + mbase + r;
-    for (int c0 = 0; c0 < g.Nt; c0 += 32) {
-        uint32_t v[32];
-        tc::ld32(tc::taddr(tm, warp, c0), v);
-        tc::wait_ld();
-        if (mrow) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int n = n0 + c0 + j;
-                if (c0 + j < g.Nt && n < g.N) out[(size_t)n * ldo] = __uint_as_float(v[j]);
-            }
-        }
-    }
-
+    if (warp >= 2) gwait(accb, 0, s_dead, err);
     tc::fence_before();
     const bool dead = __syncthreads_or(*(volatile int*)s_dead) != 0;
-    if (dead && tid == 0) {
+    tc::fence_after();
+    if (!dead) {
+        // Epilogue (warps 2-5; warp w reads TMEM lanes 32 (w % 4) ..): the
+        // tile as [Nt][128] fp32 in the ring (every slice has been consumed),
+        // then 512-byte rows to the output, one per token.
+        float* T = reinterpret_cast<float*>(sm);
+        if (warp >= 2) {
+            const int r = 32 * (warp & 3) + lane;
+            for (int c0 = 0; c0 < g.Nt; c0 += 32) {
+                uint32_t v[32];
+                tc::ld32(tc::taddr(tm, warp, c0), v);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) T[(c0 + j) * 128 + r] = __uint_as_float(v[j]);
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kSplitThreads) : "memory");
+            float* out = g.out + ((size_t)ks * g.N + n0) * g.ldo + 128 * mt;
+            const int rows = min(g.Nt, g.N - n0);
+            for (int idx = tid - 64; idx < rows * 32; idx += kSplitThreads) {
+                const int n = idx >> 5, c4 = idx & 31;
+                reinterpret_cast<float4*>(out + (size_t)n * g.ldo)[c4] =
+                    reinterpret_cast<const float4*>(T + n * 128)[c4];
+            }
+        }
+    } else if (tid == 0) {
         // Give-up path: every slice the producer issued has landed (bounded
-        // waits) before the shared memory is released.
+        // waits) before the shared memory is released ...
         const int issued = *s_issued;
         for (int s = 0; s < S && s < issued; ++s) {
             const int uses = (issued - s + S - 1) / S;
             ptx::mbar_wait_timed(&full[s], (uint32_t)((uses - 1) & 1));
         }
+    } else if (tid == 32) {
+        ptx::mbar_wait_timed(accb, 0);   // ... and every MMA has completed before TMEM is freed
     }
+    tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::dealloc(tm, ncols);
 }
 
-// Partial sums of GEMM A over the K splits, in split order, into u [N][M0]
-// and beta_logit [N][M1].
-__global__ void kda_lowrank_reduce_kernel(const float* __restrict__ part, int splits, int N, int M0, int M1,
-                                          float* __restrict__ u, float* __restrict__ beta_logit) {
+// Partial sums of GEMM A over the K splits into u [N][M0] and beta_logit
+// [N][M1]; partial row n holds tile t's outputs at columns [128 t, 128 t +
+// 128) (u tiles first).  A block takes 32 consecutive outputs: warp g sums
+// the splits g, g + 8, g + 16, ... of each (coalesced loads, independent of
+// one another), and warp 0 adds the eight warp sums in warp order, so the
+// order of the additions is fixed (results do not vary from run to run).
+constexpr int kReduceWarps = 8;
+
+__global__ void __launch_bounds__(32 * kReduceWarps)
+kda_lowrank_reduce_kernel(const float* __restrict__ part, int splits, int N, int ldo, int M0, int M1,
+                          int col1, float* __restrict__ u, float* __restrict__ beta_logit) {
+    __shared__ float sp[kReduceWarps][32];
     const size_t M = (size_t)(M0 + M1);
     const size_t total = (size_t)N * M;
-    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-        float s = 0.0f;
-        for (int k = 0; k < splits; ++k) s += part[(size_t)k * total + i];
-        const size_t n = i / M, m = i - n * M;
-        if (m < (size_t)M0) u[n * M0 + m] = s;
-        else beta_logit[n * M1 + (m - M0)] = s;
+    const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+    const size_t i = (size_t)blockIdx.x * 32 + lane;
+    size_t n = 0, m = 0, src = 0;
+    if (i < total) {
+        n = i / M;
+        m = i - n * M;
+        src = n * ldo + (m < (size_t)M0 ? m : col1 + (m - M0));
+    }
+    const size_t plane = (size_t)N * ldo;
+    float s = 0.0f;
+    if (i < total) {
+#pragma unroll 4
+        for (int k = g; k < splits; k += kReduceWarps) s += part[(size_t)k * plane + src];
+    }
+    sp[g][lane] = s;
+    __syncthreads();
+    if (g == 0 && i < total) {
+        float t = sp[0][lane];
+#pragma unroll
+        for (int w = 1; w < kReduceWarps; ++w) t += sp[w][lane];
+        if (m < (size_t)M0) u[n * M0 + m] = t;
+        else beta_logit[n * M1 + (m - M0)] = t;
     }
 }
 
@@ -271,25 +312,27 @@ bool make_map2d(CUtensorMap* m, const float* base, int K, int rows, int box_rows
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Token tile: a power of two from 32 to 256.
 int token_tile(int N) {
-    int t = 16;
+    int t = 32;
     while (t < N && t < 256) t <<= 1;
     return t;
 }
 
 struct Plan {
-    int Nt, ntiles, tiles0, tiles1, kslice, splits;
+    int Nt, ntiles, tiles0, tiles1, kslice, splits, ldo;
 };
 
-// Tiling of C[N][M0 + M1] = [A0; A1] B^T: the K dimension is split so that
-// the grid holds about one CTA per SM, each split keeping at least four
-// 32-wide slices.
+// Tiling of the output [N][128 x tiles] of [A0; A1] B^T: the K dimension is
+// split so that the grid holds about one CTA per SM, each split keeping at
+// least four 32-wide slices.
 Plan plan_gemm(int M0, int M1, int N, int K, int sm_count) {
     Plan p{};
     p.Nt = token_tile(N);
     p.ntiles = (N + p.Nt - 1) / p.Nt;
     p.tiles0 = (M0 + 127) / 128;
     p.tiles1 = (M1 + 127) / 128;
+    p.ldo = 128 * (p.tiles0 + p.tiles1);
     const int ksteps = (K + kKStep - 1) / kKStep;
     const int tiles = (p.tiles0 + p.tiles1) * p.ntiles;
     int splits = (sm_count + tiles - 1) / tiles;
@@ -300,67 +343,88 @@ Plan plan_gemm(int M0, int M1, int N, int K, int sm_count) {
     return p;
 }
 
-cudaError_t run_gemm(const Plan& pl, const GemmMaps& maps, int M0, int M1, int N, int K, float* out,
-                     const DeviceInfo& dev, int* err_word, cudaStream_t stream) {
-    GemmArgs g{M0, M1, pl.tiles0, N, K, pl.Nt, pl.kslice, ring_stages(pl.Nt), out};
+// GEMM C's plan: one split over K = rank.
+Plan plan_gemm_c(const LayerParams& p, const LowRank& lr, int N, int sm_count) {
+    Plan pc = plan_gemm(p.H * kHeadDim, 0, N, lr.rank, sm_count);
+    pc.kslice = ((lr.rank + kKStep - 1) / kKStep) * kKStep;
+    pc.splits = 1;
+    return pc;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Scratch of one front-end call: GEMM A's partial sums, then u.
+size_t scratch_bytes(const Plan& pa, int N, int rank) {
+    return align256((size_t)pa.splits * N * pa.ldo * 4) + align256((size_t)N * rank * 4);
+}
+
+cudaError_t run_gemm(const Plan& pl, const GemmMaps& maps, int N, int K, float* out, int* err_word,
+                     cudaStream_t stream) {
+    GemmArgs g{pl.tiles0, N, K, pl.Nt, pl.kslice, ring_stages(pl.Nt), pl.ldo, out};
     const dim3 grid((unsigned)(pl.tiles0 + pl.tiles1), (unsigned)pl.ntiles, (unsigned)pl.splits);
     kda_lowrank_gemm_kernel<<<grid, kThreads, gemm_smem_bytes(pl.Nt), stream>>>(g, err_word, maps);
     count_launches(1);
     return cudaGetLastError();
 }
 
-size_t align16(size_t b) { return (b + 15) & ~size_t(15); }
+// The three launches of one front-end call, with its scratch at `scratch`.
+cudaError_t run_frontend(const LayerParams& p, const LowRank& lr, const Plan& pa, int N, const float* x,
+                         float* z, float* beta_logit, void* scratch, const DeviceInfo& dev, int* err_word,
+                         cudaStream_t stream) {
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    if (!g_attr_done[dev.device].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(kda_lowrank_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)gemm_smem_bytes(256));
+        if (e != cudaSuccess) return e;
+        g_attr_done[dev.device].store(true, std::memory_order_release);
+    }
+    if (!lr.maps_ready) return cudaErrorInvalidValue;
+    const int H = p.H;
+    float* part = static_cast<float*>(scratch);
+    float* u = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align256((size_t)pa.splits * N * pa.ldo * 4));
+    // GEMM A: [u | beta_logit] partial sums over the K splits.
+    GemmMaps ma{};
+    ma.a0 = lr.map_fa;
+    ma.a1 = lr.map_bp;
+    if (!make_map2d(&ma.b, x, lr.hidden, N, pa.Nt)) return cudaErrorInvalidValue;
+    cudaError_t e = run_gemm(pa, ma, N, lr.hidden, part, err_word, stream);
+    if (e != cudaSuccess) return e;
+    // Reduce the splits.
+    const size_t total = (size_t)N * (lr.rank + H);
+    kda_lowrank_reduce_kernel<<<(unsigned)((total + 31) / 32), 32 * kReduceWarps, 0, stream>>>(
+        part, pa.splits, N, pa.ldo, lr.rank, H, 128 * pa.tiles0, u, beta_logit);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // GEMM C: z = W_fb u, one split (K = rank).
+    const Plan pc = plan_gemm_c(p, lr, N, dev.sm_count);
+    GemmMaps mc{};
+    mc.a0 = lr.map_fb;
+    mc.a1 = lr.map_fb;
+    if (!make_map2d(&mc.b, u, lr.rank, N, pc.Nt)) return cudaErrorInvalidValue;
+    return run_gemm(pc, mc, N, lr.rank, z, err_word, stream);
+}
 
 }  // namespace
 
+bool lowrank_prepare(const LayerParams& p, LowRank& lr) {
+    lr.maps_ready = make_map2d(&lr.map_fa, lr.W_fa, lr.hidden, lr.rank, 128) &&
+                    make_map2d(&lr.map_bp, lr.W_bp, lr.hidden, p.H, 128) &&
+                    make_map2d(&lr.map_fb, lr.W_fb, lr.rank, p.H * kHeadDim, 128);
+    return lr.maps_ready;
+}
+
 size_t lowrank_workspace_bytes(const LayerParams& p, const LowRank& lr, const DeviceInfo& dev, int N) {
     if (N <= 0) return 0;
-    const Plan pa = plan_gemm(lr.rank, p.H, N, lr.hidden, dev.sm_count);
-    return align16((size_t)pa.splits * N * (lr.rank + p.H) * 4) + align16((size_t)N * lr.rank * 4);
+    return scratch_bytes(plan_gemm(lr.rank, p.H, N, lr.hidden, dev.sm_count), N, lr.rank);
 }
 
 cudaError_t launch_lowrank(const LayerParams& p, const LowRank& lr, int N, const float* x, float* z,
                            float* beta_logit, void* workspace, const DeviceInfo& dev, int* err_word,
                            cudaStream_t stream) {
     if (N <= 0) return cudaSuccess;
-    if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(kda_lowrank_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)gemm_smem_bytes(256));
-        if (e != cudaSuccess) return e;
-        if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device].store(true, std::memory_order_release);
-    }
-    const int H = p.H, HD = p.H * kHeadDim;
-    const Plan pa = plan_gemm(lr.rank, H, N, lr.hidden, dev.sm_count);
-    float* part = static_cast<float*>(workspace);
-    float* u = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                        align16((size_t)pa.splits * N * (lr.rank + H) * 4));
-    // GEMM A: [u | beta_logit] partial sums over the K splits.
-    GemmMaps ma{};
-    if (!make_map2d(&ma.a0, lr.W_fa, lr.hidden, lr.rank, 128) || !make_map2d(&ma.a1, lr.W_bp, lr.hidden, H, 128) ||
-        !make_map2d(&ma.b, x, lr.hidden, N, pa.Nt))
-        return cudaErrorInvalidValue;
-    cudaError_t e = run_gemm(pa, ma, lr.rank, H, N, lr.hidden, part, dev, err_word, stream);
-    if (e != cudaSuccess) return e;
-    // Reduce the splits.
-    {
-        const size_t total = (size_t)N * (lr.rank + H);
-        const size_t want = (total + 255) / 256, cap = (size_t)dev.sm_count * 8;
-        const unsigned blocks = (unsigned)(want < cap ? want : cap);
-        kda_lowrank_reduce_kernel<<<blocks, 256, 0, stream>>>(part, pa.splits, N, lr.rank, H, u, beta_logit);
-        count_launches(1);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    // GEMM C: z = W_fb u, one split (K = rank).
-    Plan pc = plan_gemm(HD, 0, N, lr.rank, dev.sm_count);
-    pc.kslice = ((lr.rank + kKStep - 1) / kKStep) * kKStep;
-    pc.splits = 1;
-    GemmMaps mc{};
-    if (!make_map2d(&mc.a0, lr.W_fb, lr.rank, HD, 128) || !make_map2d(&mc.b, u, lr.rank, N, pc.Nt))
-        return cudaErrorInvalidValue;
-    mc.a1 = mc.a0;
-    return run_gemm(pc, mc, HD, 0, N, lr.rank, z, dev, err_word, stream);
+    const Plan pa = plan_gemm(lr.rank, p.H, N, lr.hidden, dev.sm_count);
+    return run_frontend(p, lr, pa, N, x, z, beta_logit, workspace, dev, err_word, stream);
 }
-
 
 // ---------------------------------------------------------------------------
 // The front-end without a caller-supplied workspace (kda_lowrank_noalloc).
@@ -396,22 +460,23 @@ ScratchAddr g_scratch_addr[64];
 bool plan_noalloc(const LayerParams& p, const LowRank& lr, const DeviceInfo& dev, int N, Plan* out,
                   size_t* need) {
     Plan pa = plan_gemm(lr.rank, p.H, N, lr.hidden, dev.sm_count);
-    const size_t ub = align16((size_t)N * lr.rank * 4);
-    const size_t per_split = (size_t)N * (lr.rank + p.H) * 4;
-    *need = align16((size_t)pa.splits * per_split) + ub;
+    *need = scratch_bytes(pa, N, lr.rank);
     if (*need > (size_t)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES) {
-        const size_t room = (size_t)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES > ub + 16
-                                ? (size_t)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES - ub - 16 : 0;
+        const size_t ub = align256((size_t)N * lr.rank * 4);
+        const size_t per_split = (size_t)N * pa.ldo * 4;
+        const size_t room = (size_t)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES > ub + 256
+                                ? (size_t)KDA_LOWRANK_NOALLOC_SCRATCH_BYTES - ub - 256 : 0;
         const int cap = (int)(room / per_split);
         if (cap < 1) {
-            *need = align16(per_split) + ub;
+            pa.splits = 1;
+            *need = scratch_bytes(pa, N, lr.rank);
             return false;
         }
         const int ksteps = (lr.hidden + kKStep - 1) / kKStep;
         const int per = (ksteps + cap - 1) / cap;
         pa.kslice = per * kKStep;
         pa.splits = (lr.hidden + pa.kslice - 1) / pa.kslice;
-        *need = align16((size_t)pa.splits * per_split) + ub;
+        *need = scratch_bytes(pa, N, lr.rank);
     }
     *out = pa;
     return true;
@@ -437,38 +502,7 @@ cudaError_t launch_lowrank_noalloc(const LayerParams& p, const LowRank& lr, int 
     Plan pa;
     size_t need = 0;
     if (!plan_noalloc(p, lr, dev, N, &pa, &need)) return cudaErrorInvalidValue;   // the host checked the size
-    if (!g_attr_done[dev.device].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(kda_lowrank_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)gemm_smem_bytes(256));
-        if (e != cudaSuccess) return e;
-        g_attr_done[dev.device].store(true, std::memory_order_release);
-    }
-    const int H = p.H, HD = p.H * kHeadDim;
-    float* part = static_cast<float*>(sa.ptr);
-    float* u = reinterpret_cast<float*>(static_cast<uint8_t*>(sa.ptr) +
-                                        align16((size_t)pa.splits * N * (lr.rank + H) * 4));
-    GemmMaps ma{};
-    if (!make_map2d(&ma.a0, lr.W_fa, lr.hidden, lr.rank, 128) || !make_map2d(&ma.a1, lr.W_bp, lr.hidden, H, 128) ||
-        !make_map2d(&ma.b, x, lr.hidden, N, pa.Nt))
-        return cudaErrorInvalidValue;
-    cudaError_t e = run_gemm(pa, ma, lr.rank, H, N, lr.hidden, part, dev, err_word, stream);
-    if (e != cudaSuccess) return e;
-    {
-        const size_t total = (size_t)N * (lr.rank + H);
-        const size_t want = (total + 255) / 256, cap = (size_t)dev.sm_count * 8;
-        const unsigned blocks = (unsigned)(want < cap ? want : cap);
-        kda_lowrank_reduce_kernel<<<blocks, 256, 0, stream>>>(part, pa.splits, N, lr.rank, H, u, beta_logit);
-        count_launches(1);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    Plan pc = plan_gemm(HD, 0, N, lr.rank, dev.sm_count);
-    pc.kslice = ((lr.rank + kKStep - 1) / kKStep) * kKStep;
-    pc.splits = 1;
-    GemmMaps mc{};
-    if (!make_map2d(&mc.a0, lr.W_fb, lr.rank, HD, 128) || !make_map2d(&mc.b, u, lr.rank, N, pc.Nt))
-        return cudaErrorInvalidValue;
-    mc.a1 = mc.a0;
-    return run_gemm(pc, mc, HD, 0, N, lr.rank, z, dev, err_word, stream);
+    return run_frontend(p, lr, pa, N, x, z, beta_logit, sa.ptr, dev, err_word, stream);
 }
 
 }  // namespace kda
