@@ -71,6 +71,8 @@ def _load(lib_path: str | None = None):
         lib.kda_oracle_cpu_count.argtypes = []
         lib.kda_oracle_lowrank.restype = ctypes.c_int
         lib.kda_oracle_lowrank.argtypes = [ctypes.c_int] * 5 + [dp] * 6
+        lib.kda_oracle_project.restype = ctypes.c_int
+        lib.kda_oracle_project.argtypes = [ctypes.c_int] * 3 + [dp] * 3
         _libs[path] = lib
     return _libs[path]
 
@@ -162,3 +164,20 @@ def lowrank(x, W_fa, W_fb, W_bp, H, d=128, *, lib_path: str | None = None):
     if rc != 0:
         raise ValueError(f"kda_oracle_lowrank rejected its arguments (rc={rc})")
     return z.reshape(*lead, H, d), bl.reshape(*lead, H)
+
+
+def project(x, W, *, lib_path: str | None = None):
+    """Projection y = W x per token: x [..., in], W [out, in] -> y [..., out], float64."""
+    x = _f64(x)
+    W = _f64(W)
+    lead = x.shape[:-1]
+    n_in = x.shape[-1]
+    n_out = W.shape[0]
+    assert W.shape == (n_out, n_in)
+    N = int(np.prod(lead)) if lead else 1
+    xf = np.ascontiguousarray(x.reshape(N, n_in))
+    y = np.zeros((N, n_out))
+    rc = _load(lib_path).kda_oracle_project(N, n_in, n_out, _ptr(xf), _ptr(W), _ptr(y))
+    if rc != 0:
+        raise ValueError(f"kda_oracle_project rejected its arguments (rc={rc})")
+    return y.reshape(*lead, n_out)

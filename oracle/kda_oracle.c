@@ -212,6 +212,28 @@ int kda_oracle_lowrank(int N, int hidden, int rank, int H, int d,
     return 0;
 }
 
+/*
+ * Projections ("What runs where (per layer)", row "KDA projections
+ * (q,k,v,g,o)"; "O projection" row): y = W x, one token at a time, each
+ * output a plain sum over the input index.
+ */
+int kda_oracle_project(int N, int in, int out, const double *x, const double *W, double *y)
+{
+    if (N < 0 || in <= 0 || out <= 0) return -1;
+    if (N == 0) return 0;
+    if (!x || !W || !y) return -1;
+    for (int n = 0; n < N; ++n) {
+        const double *xn = x + (size_t)n * in;
+        for (int i = 0; i < out; ++i) {
+            const double *wi = W + (size_t)i * in;
+            double s = 0.0;
+            for (int j = 0; j < in; ++j) s += wi[j] * xn[j];
+            y[(size_t)n * out + i] = s;
+        }
+    }
+    return 0;
+}
+
 int kda_oracle_cpu_count(void)
 {
 #ifdef __linux__

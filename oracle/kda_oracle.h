@@ -64,6 +64,18 @@ int kda_oracle_lowrank(int N, int hidden, int rank, int H, int d,
                        const double *x, const double *W_fa, const double *W_fb,
                        const double *W_bp, double *z, double *beta_logit);
 
+/*
+ * Projections on either side of the token step ("Metal (Apple GPU) backend
+ * for Kimi K3", table "What runs where (per layer)", row "KDA projections
+ * (q,k,v,g,o)"; "Kimi K3 Metal Gap Analysis", section 2, row "O projection":
+ * W_o[sig(W_g x) * RMSNorm_head(S^T q)]).  A plain product y = W x per token:
+ *   x [N][in], W [out][in], y [N][out]:  y[n][i] = sum_j W[i][j] x[n][j].
+ * The input projections are this with W the rows of W_q, W_k, W_v and W_g;
+ * the output projection is this with W = W_o and x the gated, normalised o.
+ * Returns 0 on success, -1 on a bad argument.
+ */
+int kda_oracle_project(int N, int in, int out, const double *x, const double *W, double *y);
+
 /* Number of hardware threads this process may run on (sched affinity). */
 int kda_oracle_cpu_count(void);
 

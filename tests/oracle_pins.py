@@ -10,7 +10,8 @@ Sources: "Kimi K3 Metal Gap Analysis" section 2 "KDA Attention" (rows Conv4 +
 SiLU, L2 normalize q/k, Decay compute, Recurrence, O projection) and "Metal
 (Apple GPU) backend for Kimi K3" section "Correctness" (token-0 zero-state
 identity o / (v * beta) = q_hat . k_hat) and table "What runs where (per
-layer)" (the low-rank fa, fb, bp matmuls feeding the decay and beta).
+layer)" (the low-rank fa, fb, bp matmuls feeding the decay and beta, and
+the q, k, v, g, o projections).
 """
 from __future__ import annotations
 
@@ -303,7 +304,40 @@ def pin_lowrank_rank_and_linearity(lib_path=None):
     assert sv[rank - 1] > 1e-6 * sv[0] and sv[rank] < 1e-10 * sv[0]
 
 
+def pin_project_one_hot_and_linearity(lib_path=None):
+    """Projections ("What runs where (per layer)", row "KDA projections
+    (q,k,v,g,o)"; "O projection" row): y = W x.  A single nonzero weight
+    W[i][j] = c routes c x_j to output i alone (exactly), and y is linear in
+    x and in W (to rounding)."""
+    rng = np.random.default_rng(401)
+    N, n_in, n_out = 6, 24, 10
+    x = rng.standard_normal((N, n_in))
+    W = np.zeros((n_out, n_in)); W[7, 3] = -1.5
+    y = oracle.project(x, W, lib_path=lib_path)
+    e = np.zeros((N, n_out)); e[:, 7] = -1.5 * x[:, 3]
+    assert np.array_equal(y, e)
+    W1, W2 = rng.standard_normal((n_out, n_in)), rng.standard_normal((n_out, n_in))
+    x2 = rng.standard_normal((N, n_in))
+    f = lambda xx, ww: oracle.project(xx, ww, lib_path=lib_path)
+    y1 = f(x, W1)
+    tol = 1e-12 * np.abs(y1).max()
+    np.testing.assert_allclose(f(2.0 * x - x2, W1), 2.0 * y1 - f(x2, W1), rtol=0, atol=tol)
+    np.testing.assert_allclose(f(x, W1 + 3.0 * W2), y1 + 3.0 * f(x, W2), rtol=0, atol=10 * tol)
+
+
+def pin_project_orthogonal(lib_path=None):
+    """With W orthogonal (from a QR factorisation) the projection keeps
+    every token's norm, and W^T applied to y gives x back."""
+    rng = np.random.default_rng(402)
+    Q, _ = np.linalg.qr(rng.standard_normal((16, 16)))
+    x = rng.standard_normal((5, 16))
+    y = oracle.project(x, Q, lib_path=lib_path)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-12)
+    np.testing.assert_allclose(oracle.project(y, Q.T.copy(), lib_path=lib_path), x, rtol=0, atol=1e-12)
+
+
 PINS = [pin_token0_identity, pin_identity_when_no_write_no_decay, pin_decay_only_closed_form,
         pin_delta_rule_write, pin_bruteforce_products, pin_conv_one_hot_tap, pin_conv_impulse,
         pin_window_continuity, pin_l2_norm, pin_rmsnorm_gate_gamma, pin_contraction_bound,
-        pin_decay_values, pin_lowrank_one_hot, pin_lowrank_zero_fa, pin_lowrank_rank_and_linearity]
+        pin_decay_values, pin_lowrank_one_hot, pin_lowrank_zero_fa, pin_lowrank_rank_and_linearity,
+        pin_project_one_hot_and_linearity, pin_project_orthogonal]

@@ -37,6 +37,10 @@ MUTANTS = [
     ("lowrank_beta_from_fa", "W_bp[(size_t)h * hidden + j] * xn[j]", "W_fa[(size_t)h * hidden + j] * xn[j]"),
     ("lowrank_token_stride", "const double *xn = x + (size_t)n * hidden;", "const double *xn = x + (size_t)n * rank;"),
     ("lowrank_head_offset", "z[(size_t)n * HD + m] = s;", "z[(size_t)n * HD + (m + d) % HD] = s;"),
+    # projections
+    ("project_transposed", "s += wi[j] * xn[j];", "s += W[(size_t)j * out + i] * xn[j];"),
+    ("project_token_stride", "const double *xn = x + (size_t)n * in;", "const double *xn = x + (size_t)n * out;"),
+    ("project_output_shifted", "y[(size_t)n * out + i] = s;", "y[(size_t)n * out + (i + 1) % out] = s;"),
 ]
 
 
