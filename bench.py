@@ -438,6 +438,63 @@ class Ours:
         torch.cuda.empty_cache()
         return res
 
+    # ---------------------------------------------------------------- projections
+    def projections(self, wl_name, with_cublas=True):
+        """kda_project_qkvg (bf16 q/k/v and fp32 gate logits for prefill
+        workloads, fp32 for decode ones) and kda_project_o on the tokens of
+        one call of a workload (hidden 7168); cuBLAS bf16 GEMMs of the same
+        shapes are timed beside them for context.  Inputs larger than L2 (or
+        the weights, at decode size)."""
+        torch, kda, synth = self.torch, self.kda, self.synth
+        wl = synth.WORKLOADS[wl_name]
+        pr = synth.make_projections(wl, self.dev)
+        N, H, hid = pr["x"].shape[0], wl.H, pr["hidden"]
+        HD = H * D
+        p = synth.make_params(wl, self.dev)
+        ctx = kda.kda_create(H, p["conv_w"], p["dt_bias"], p["A_log"], p["gamma"])
+        kda.kda_bind_projections(ctx, hid, pr["W_qkvg"].view(torch.int16), pr["W_o"].view(torch.int16))
+        f32 = wl.mode == "decode"
+        dt = torch.float32 if f32 else torch.bfloat16
+        q, k, v = (torch.empty((N, HD), device=self.dev, dtype=dt) for _ in range(3))
+        g = torch.empty((N, HD), device=self.dev)
+        y = torch.empty((N, hid), device=self.dev)
+        ws = torch.empty(kda.kda_project_o_workspace_bytes(ctx, N), dtype=torch.uint8, device=self.dev)
+        xi = pr["x"].view(torch.int16)
+        K = 5 if N > 4096 else 50
+        W = max(3, self.args.warmup)
+
+        def timed(fn, n):
+            for _ in range(W):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            self.barrier_sync()
+            l0 = kda.kda_launch_count()
+            for i in range(n):
+                ev[i][0].record(self.stream)
+                fn()
+                ev[i][1].record(self.stream)
+            self.barrier_sync()
+            return (self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev)),
+                    kda.kda_launch_count() - l0)
+
+        ms_in, l_in = timed(lambda: kda.kda_project_qkvg(ctx, N, xi, q, k, v, g, qkv_f32=f32, stream=self.stream), K)
+        ms_out, l_out = timed(lambda: kda.kda_project_o(ctx, N, pr["o_in"], y, ws, 0, self.stream), K)
+        assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
+        kda.kda_destroy(ctx)
+        res = {"wl": wl, "N": N, "hidden": hid, "H": H, "ms_in": ms_in, "launches_in": l_in,
+               "ms_out": ms_out, "launches_out": l_out,
+               "flop_in": 2.0 * N * 4 * HD * hid, "flop_out": 2.0 * N * HD * hid,
+               "bytes_in": 2 * (N * hid + 4 * HD * hid) + N * HD * (3 * (4 if f32 else 2) + 4),
+               "bytes_out": 2 * hid * HD + N * HD * (4 + 2 + 2) + 4 * N * hid}
+        if with_cublas:
+            Wt = pr["W_qkvg"]
+            with torch.cuda.stream(self.stream):
+                ms_cb, _ = timed(lambda: torch.matmul(pr["x"], Wt.t()), K)
+            res["ms_cublas_in"] = ms_cb
+        del pr, q, k, v, g, y, ws
+        torch.cuda.empty_cache()
+        return res
+
     # ---------------------------------------------------------------- prefill
     def prefill(self, wl_name, e2e=True):
         torch, kda, synth = self.torch, self.kda, self.synth
@@ -772,6 +829,8 @@ def main():
                     help="profiling only: time this decode workload alone (no e2e, no graph)")
     ap.add_argument("--lowrank-only", action="store_true",
                     help="profiling only: time the low-rank front-end decode line alone")
+    ap.add_argument("--proj-only", default=None,
+                    help="profiling only: time the projections on this workload's tokens alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-split", type=int, default=2,
                     help="groups of sequences the decode end-to-end step is pipelined over")
@@ -784,8 +843,11 @@ def main():
 
     ours = Ours(args, world, rank, local)
     peaks = load_peaks()
-    if args.prefill_workload or args.decode_workload or args.lowrank_only:   # profiling runs
+    if args.prefill_workload or args.decode_workload or args.lowrank_only or args.proj_only:   # profiling runs
         out = {"profiling_only": True}
+        if args.proj_only:
+            r = ours.projections(args.proj_only, with_cublas=False)
+            out.update(proj_workload=args.proj_only, proj_in_ms=round(r["ms_in"], 4), proj_out_ms=round(r["ms_out"], 4))
         if args.lowrank_only:
             r = ours.decode_lowrank(DECODE_WL)
             out.update(lowrank_step_ms=round(r["ms_step"], 5), lowrank_frontend_ms=round(r["ms_frontend"], 5))
@@ -808,6 +870,8 @@ def main():
     pre = None if args.no_prefill else ours.prefill(PREFILL_WL)
     pre1 = None if args.no_prefill else ours.prefill(PREFILL1_WL, e2e=False)
     pvl = None if args.no_prefill else ours.prefill_varlen()
+    prj = None if args.no_prefill else ours.projections(PREFILL_WL)
+    prd = None if args.no_decode else ours.projections(DECODE_WL, with_cublas=False)
     clk = clocks.stop()
 
     if rank != 0:
@@ -883,6 +947,41 @@ def main():
                          "traffic": None, "kernel": "kda_prefill_kernel",
                          "alg_bytes_per_launch": pvl["alg_bytes"]},
         }
+    for key, r in (("projections", prj), ("projections_decode", prd)):
+        if r is None:
+            continue
+        w = r["wl"]
+        tin = r["flop_in"] / (r["ms_in"] * 1e-3) / 1e12
+        tout = r["flop_out"] / (r["ms_out"] * 1e-3) / 1e12
+        gin = r["bytes_in"] / (r["ms_in"] * 1e-3) / 1e9
+        gout = r["bytes_out"] / (r["ms_out"] * 1e-3) / 1e9
+        big = r["N"] > 4096
+        blk = {
+            "workload": f"{w.name}: {r['N']} tokens, hidden {r['hidden']}, H={r['H']}, bf16 operands, fp32 accumulation",
+            "qkvg": {"ms_per_call": round(r["ms_in"], 4), "tflops": round(tin, 1), "gbs": round(gin, 1),
+                     "gpu_launches": r["launches_in"],
+                     "roofline": ({"bound": "tensor", "achieved": round(tin, 1), "peak": peaks["bf16_tflops"],
+                                   "unit": "TFLOP/s", "frac": round(tin / peaks["bf16_tflops"], 4),
+                                   "peak_src": peaks["src"] + " bf16_tflops (burst)", "traffic": None}
+                                  if big else
+                                  {"bound": "hbm", "achieved": round(gin, 1), "peak": peaks["hbm_gbs"],
+                                   "unit": "GB/s", "frac": round(gin / peaks["hbm_gbs"], 4),
+                                   "peak_src": peaks["src"] + " hbm_gbs", "traffic": None}),
+                     "kernel": "kda_proj_gemm_kernel"},
+            "o": {"ms_per_call": round(r["ms_out"], 4), "tflops": round(tout, 1), "gbs": round(gout, 1),
+                  "gpu_launches": r["launches_out"],
+                  "roofline": ({"bound": "tensor", "achieved": round(tout, 1), "peak": peaks["bf16_tflops"],
+                                "unit": "TFLOP/s", "frac": round(tout / peaks["bf16_tflops"], 4),
+                                "peak_src": peaks["src"] + " bf16_tflops (burst)", "traffic": None}
+                               if big else
+                               {"bound": "hbm", "achieved": round(gout, 1), "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": round(gout / peaks["hbm_gbs"], 4),
+                                "peak_src": peaks["src"] + " hbm_gbs", "traffic": None}),
+                  "kernel": "kda_to_bf16_kernel + kda_proj_gemm_kernel"},
+        }
+        if "ms_cublas_in" in r:
+            blk["qkvg"]["context_cublas_bf16_ms"] = round(r["ms_cublas_in"], 4)
+        line[key] = blk
     print(json.dumps(line), flush=True)
     if ours.dist is not None:
         ours.dist.destroy_process_group()

@@ -46,7 +46,7 @@
  *    the same suspicion.
  *  - Host-side fault injection for tests: the environment variable
  *    KDA_FAULT_INJECT, read by kda_create, names entry points ("decode",
- *    "prefill", "prefill_varlen", "lowrank", "all"; comma-separated; the
+ *    "prefill", "prefill_varlen", "lowrank", "project", "all"; comma-separated; the
  *    low-rank decode step counts as "decode" and "lowrank") whose launches that
  *    context replaces by cudaErrorLaunchFailure: nothing is launched, no
  *    buffer changes, and the call returns KDA_ERR_CUDA.
@@ -286,6 +286,50 @@ KDA_API kda_status kda_decode_step_lowrank(kda_ctx *ctx, int B, const float *x,
                                            const float *gate_logit, float *conv_state, float *S,
                                            float *o, float *o_pre, void *workspace,
                                            size_t workspace_bytes, void *stream);
+
+/*
+ * Bind the layer's projection weights ("Metal (Apple GPU) backend for Kimi
+ * K3", table "What runs where (per layer)", row "KDA projections
+ * (q,k,v,g,o)"; "Kimi K3 Metal Gap Analysis", section 2, row "O
+ * projection": W_o[sig(W_g x) * RMSNorm_head(S^T q)]).  Device pointers,
+ * bf16 raw bit patterns, 16-byte aligned, borrowed:
+ *   hidden   width of the layer's hidden input x and of y; a multiple of 128
+ *   W_qkvg   [4*H*d][hidden]  W_q, W_k, W_v and W_g stacked by rows (row
+ *            j*H*d + h*d + c of block j feeds head h, channel c)
+ *   W_o      [hidden][H*d]
+ * Rebinding replaces the previous weights.  Launches nothing.
+ */
+KDA_API kda_status kda_bind_projections(kda_ctx *ctx, int hidden, const uint16_t *W_qkvg,
+                                        const uint16_t *W_o);
+
+/*
+ * Input projections of N tokens on tensor cores (bf16 operands, fp32
+ * accumulation): q = W_q x, k = W_k x, v = W_v x, gate_logit = W_g x.
+ *   x            [N][hidden] bf16 (in)
+ *   q, k, v      [N][H][d]: bf16 when qkv_f32 == 0 (the kda_prefill input
+ *                format, rounded to nearest even), fp32 when qkv_f32 != 0
+ *                (the kda_decode_step format)
+ *   gate_logit   [N][H][d] fp32
+ * All 16-byte aligned.  N == 0 is a no-op; KDA_ERR_INVALID_ARG if no
+ * weights are bound.
+ */
+KDA_API kda_status kda_project_qkvg(kda_ctx *ctx, int N, const uint16_t *x, void *q, void *k, void *v,
+                                    float *gate_logit, int qkv_f32, void *stream);
+
+/* Bytes of device workspace kda_project_o needs for N tokens (a bf16 copy of o). */
+KDA_API size_t kda_project_o_workspace_bytes(const kda_ctx *ctx, int N);
+
+/*
+ * Output projection of N tokens: y = W_o o, o rounded to bf16 (nearest even)
+ * into the workspace, then bf16 products with fp32 accumulation on tensor
+ * cores.
+ *   o            [N][H][d] fp32 (in): the o of kda_decode_step / kda_prefill
+ *   y            [N][hidden] fp32 (out)
+ *   workspace    at least kda_project_o_workspace_bytes(ctx, N) bytes
+ * All 16-byte aligned.  N == 0 is a no-op.
+ */
+KDA_API kda_status kda_project_o(kda_ctx *ctx, int N, const float *o, float *y, void *workspace,
+                                 size_t workspace_bytes, void *stream);
 
 /*
  * Synchronise `stream` and report whether any kernel launched with this

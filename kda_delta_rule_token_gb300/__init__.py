@@ -18,7 +18,8 @@ __all__ = [
     "kda_decode_step", "kda_prefill", "kda_prefill_varlen", "kda_prefill_workspace_bytes", "kda_sync_status",
     "kda_launch_count", "kda_bind_lowrank", "kda_lowrank", "kda_lowrank_workspace_bytes",
     "kda_decode_step_lowrank", "kda_decode_lowrank_workspace_bytes", "kda_lowrank_noalloc",
-    "LOWRANK_NOALLOC_SCRATCH_BYTES", "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_ALIGNMENT",
+    "LOWRANK_NOALLOC_SCRATCH_BYTES", "kda_bind_projections", "kda_project_qkvg", "kda_project_o",
+    "kda_project_o_workspace_bytes", "KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_ALIGNMENT",
     "KDA_ERR_UNSUPPORTED", "KDA_ERR_CUDA", "KDA_ERR_TIMEOUT", "HEAD_DIM", "CHUNK",
 ]
 
@@ -96,6 +97,14 @@ def load(path: str | None = None):
     lib.kda_decode_step_lowrank.restype = i32
     lib.kda_lowrank_noalloc.argtypes = [vp, i32, vp, vp, vp, vp]
     lib.kda_lowrank_noalloc.restype = i32
+    lib.kda_bind_projections.argtypes = [vp, i32, vp, vp]
+    lib.kda_bind_projections.restype = i32
+    lib.kda_project_qkvg.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, vp]
+    lib.kda_project_qkvg.restype = i32
+    lib.kda_project_o_workspace_bytes.argtypes = [vp, i32]
+    lib.kda_project_o_workspace_bytes.restype = sz
+    lib.kda_project_o.argtypes = [vp, i32, vp, vp, vp, sz, vp]
+    lib.kda_project_o.restype = i32
     lib.kda_testing_bounded_wait.argtypes = [vp, ctypes.c_uint, vp]
     lib.kda_testing_bounded_wait.restype = i32
     _lib = lib
@@ -217,6 +226,25 @@ def kda_decode_step_lowrank(ctx, B, x, q, k, v, gate_logit, conv_state, S, o, o_
                                           _p(conv_state), _p(S), _p(o), _p(o_pre), _p(workspace),
                                           _nbytes(workspace, workspace_bytes), _stream(stream)),
            "kda_decode_step_lowrank")
+
+
+def kda_bind_projections(ctx, hidden, W_qkvg, W_o) -> None:
+    """W_qkvg [4*H*d, hidden] and W_o [hidden, H*d]: bf16 tensors (or their int16 views)."""
+    _check(load().kda_bind_projections(ctx, int(hidden), _p(W_qkvg), _p(W_o)), "kda_bind_projections")
+
+
+def kda_project_qkvg(ctx, N, x, q, k, v, gate_logit, qkv_f32=False, stream=None) -> None:
+    _check(load().kda_project_qkvg(ctx, int(N), _p(x), _p(q), _p(k), _p(v), _p(gate_logit),
+                                   1 if qkv_f32 else 0, _stream(stream)), "kda_project_qkvg")
+
+
+def kda_project_o_workspace_bytes(ctx, N) -> int:
+    return int(load().kda_project_o_workspace_bytes(ctx, int(N)))
+
+
+def kda_project_o(ctx, N, o, y, workspace, workspace_bytes=0, stream=None) -> None:
+    _check(load().kda_project_o(ctx, int(N), _p(o), _p(y), _p(workspace),
+                                _nbytes(workspace, workspace_bytes), _stream(stream)), "kda_project_o")
 
 
 def kda_sync_status(ctx, stream=None) -> int:

@@ -26,6 +26,8 @@ struct kda_ctx {
     unsigned inject;  // launches replaced by an injected failure (KDA_FAULT_INJECT)
     bool has_lowrank;
     kda::LowRank lowrank;  // bound by kda_bind_lowrank
+    bool has_proj;
+    kda::Projections proj;  // bound by kda_bind_projections
 };
 
 namespace kda {
@@ -57,7 +59,8 @@ kda_status check_device(const kda_ctx* ctx) {
     return KDA_OK;
 }
 
-constexpr unsigned kInjectDecode = 1u, kInjectPrefill = 2u, kInjectVarlen = 4u, kInjectLowrank = 8u;
+constexpr unsigned kInjectDecode = 1u, kInjectPrefill = 2u, kInjectVarlen = 4u, kInjectLowrank = 8u,
+                   kInjectProject = 16u;
 
 // Parse KDA_FAULT_INJECT (see the top of this file).
 unsigned parse_inject(const char* v) {
@@ -73,7 +76,8 @@ unsigned parse_inject(const char* v) {
         else if (is("prefill")) m |= kInjectPrefill;
         else if (is("prefill_varlen")) m |= kInjectVarlen;
         else if (is("lowrank")) m |= kInjectLowrank;
-        else if (is("all")) m |= kInjectDecode | kInjectPrefill | kInjectVarlen | kInjectLowrank;
+        else if (is("project")) m |= kInjectProject;
+        else if (is("all")) m |= kInjectDecode | kInjectPrefill | kInjectVarlen | kInjectLowrank | kInjectProject;
         p = *e ? e + 1 : e;
     }
     return m;
@@ -410,6 +414,72 @@ kda_status kda_decode_step_lowrank(kda_ctx* ctx, int B, const float* x, const fl
         kda::set_launch_detail(ctx, kda::kInjectLowrank | kda::kInjectDecode, "decode_lowrank launch", e);
         return KDA_ERR_CUDA;
     }
+    return KDA_OK;
+}
+
+kda_status kda_bind_projections(kda_ctx* ctx, int hidden, const uint16_t* W_qkvg, const uint16_t* W_o) {
+    if (!ctx || !W_qkvg || !W_o) return KDA_ERR_INVALID_ARG;
+    if (hidden < 128 || hidden % 128) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail), "hidden (%d) must be a positive multiple of 128", hidden);
+        return KDA_ERR_INVALID_ARG;
+    }
+    if (!aligned16(W_qkvg) || !aligned16(W_o)) return KDA_ERR_ALIGNMENT;
+    kda::Projections pr{};
+    pr.hidden = hidden;
+    pr.W_qkvg = W_qkvg;
+    pr.W_o = W_o;
+    if (!kda::proj_prepare(ctx->params, pr)) {
+        std::snprintf(kda::g_detail, sizeof(kda::g_detail), "cuTensorMapEncodeTiled failed for the projection weights");
+        return KDA_ERR_CUDA;
+    }
+    ctx->proj = pr;
+    ctx->has_proj = true;
+    return KDA_OK;
+}
+
+static kda_status need_proj(const kda_ctx* ctx) {
+    if (ctx->has_proj) return KDA_OK;
+    std::snprintf(kda::g_detail, sizeof(kda::g_detail), "no projection weights bound (kda_bind_projections)");
+    return KDA_ERR_INVALID_ARG;
+}
+
+kda_status kda_project_qkvg(kda_ctx* ctx, int N, const uint16_t* x, void* q, void* k, void* v, float* gate_logit,
+                            int qkv_f32, void* stream) {
+    if (!ctx || N < 0) return KDA_ERR_INVALID_ARG;
+    if (const kda_status r = need_proj(ctx); r != KDA_OK) return r;
+    if (N == 0) return KDA_OK;
+    if (!x || !q || !k || !v || !gate_logit) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, q, k, v, gate_logit};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
+    cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectProject, [&] {
+        return kda::launch_project_qkvg(ctx->params, ctx->proj, N, x, q, k, v, gate_logit, qkv_f32 != 0, ctx->dev,
+                                        ctx->err_word, static_cast<cudaStream_t>(stream));
+    });
+    if (e != cudaSuccess) { kda::set_launch_detail(ctx, kda::kInjectProject, "project_qkvg launch", e); return KDA_ERR_CUDA; }
+    return KDA_OK;
+}
+
+size_t kda_project_o_workspace_bytes(const kda_ctx* ctx, int N) {
+    if (!ctx || N <= 0) return 0;
+    return kda::project_o_workspace_bytes(ctx->params, N);
+}
+
+kda_status kda_project_o(kda_ctx* ctx, int N, const float* o, float* y, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    if (!ctx || N < 0) return KDA_ERR_INVALID_ARG;
+    if (const kda_status r = need_proj(ctx); r != KDA_OK) return r;
+    if (N == 0) return KDA_OK;
+    if (!o || !y || !workspace) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(y) || !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
+    if (workspace_bytes < kda::project_o_workspace_bytes(ctx->params, N)) return KDA_ERR_INVALID_ARG;
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
+    cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectProject, [&] {
+        return kda::launch_project_o(ctx->params, ctx->proj, N, o, y, workspace, ctx->dev, ctx->err_word,
+                                     static_cast<cudaStream_t>(stream));
+    });
+    if (e != cudaSuccess) { kda::set_launch_detail(ctx, kda::kInjectProject, "project_o launch", e); return KDA_ERR_CUDA; }
     return KDA_OK;
 }
 

@@ -68,6 +68,16 @@ struct LowRank {
     CUtensorMap map_fa, map_bp, map_fb;
 };
 
+// Projection weights bound to a context (borrowed, bf16), with their TMA
+// tensor maps (encoded once, at binding, by proj_prepare).
+struct Projections {
+    int hidden;             // width of the hidden input x and of y
+    const void* W_qkvg;     // [4*H*d][hidden] bf16: W_q, W_k, W_v, W_g stacked by rows
+    const void* W_o;        // [hidden][H*d] bf16
+    bool maps_ready;
+    CUtensorMap map_qkvg, map_o;
+};
+
 // Device facts the launchers need, queried once per context.
 struct DeviceInfo {
     int device;
@@ -98,6 +108,18 @@ cudaError_t launch_lowrank(const LayerParams& p, const LowRank& lr, int N, const
 size_t lowrank_noalloc_need(const LayerParams& p, const LowRank& lr, const DeviceInfo& dev, int N);
 cudaError_t launch_lowrank_noalloc(const LayerParams& p, const LowRank& lr, int N, const float* x, float* z,
                                    float* beta_logit, const DeviceInfo& dev, int* err_word, cudaStream_t stream);
+
+// Projections (csrc/proj.cu): input projections of N tokens of bf16 x into
+// q, k, v (bf16, or fp32 when qkv_f32) and fp32 gate logits; output
+// projection of fp32 o into fp32 y through a bf16 copy of o in `workspace`
+// (project_o_workspace_bytes).
+bool proj_prepare(const LayerParams& p, Projections& pr);
+cudaError_t launch_project_qkvg(const LayerParams& p, const Projections& pr, int N, const void* x, void* q,
+                                void* k, void* v, float* gate_logit, bool qkv_f32, const DeviceInfo& dev,
+                                int* err_word, cudaStream_t stream);
+size_t project_o_workspace_bytes(const LayerParams& p, int N);
+cudaError_t launch_project_o(const LayerParams& p, const Projections& pr, int N, const float* o, float* y,
+                             void* workspace, const DeviceInfo& dev, int* err_word, cudaStream_t stream);
 
 // Test hook (csrc/testing.cu): a kernel whose bounded wait runs out.
 cudaError_t launch_testing_wait(int* err_word, unsigned long long limit_ns, cudaStream_t stream);

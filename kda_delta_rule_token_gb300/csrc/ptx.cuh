@@ -15,6 +15,7 @@ constexpr int kErrDecodeLoadWait = 1 << 0;
 constexpr int kErrPrefillWait = 1 << 1;
 constexpr int kErrTestingWait = 1 << 2;
 constexpr int kErrLowrankWait = 1 << 3;
+constexpr int kErrProjWait = 1 << 4;
 
 // Longest a kernel waits on one barrier phase before it reports an error.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s

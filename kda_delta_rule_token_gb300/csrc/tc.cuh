@@ -1,10 +1,10 @@
 // Inline-PTX wrappers for the 5th-generation tensor cores (tcgen05) and
-// tensor memory (TMEM), written from the PTX ISA: TMEM allocation,
-// kind::tf32 MMAs with operands in shared memory or TMEM, commits to an
-// mbarrier, and 32-lane x 32-bit TMEM loads/stores.
+// tensor memory (TMEM), written from the PTX ISA: TMEM allocation, kind::tf32
+// and kind::f16 (bf16) MMAs with operands in shared memory or TMEM, commits
+// to an mbarrier, and 32-lane x 32-bit TMEM loads/stores.
 //
 // Shared-memory operands use the K-major, 128-byte-swizzled layout: rows of
-// 128 bytes (32 fp32/tf32 elements of K), 8-row atoms of 1024 bytes, the
+// 128 bytes (32 fp32/tf32 or 64 bf16 elements of K), 8-row atoms of 1024 bytes, the
 // 16-byte chunk index XOR-ed with (row % 8); K beyond 32 elements continues
 // in further blocks of rows x 128 bytes.
 #pragma once
@@ -39,6 +39,11 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor: kind::f16 with bf16 A and B, D = f32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Whole-warp TMEM allocation; the base address is written to *dst (shared).
 __device__ __forceinline__ void alloc(uint32_t* dst, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -55,6 +60,14 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 operands (kind::f16, K = 16 per instruction)
+__device__ __forceinline__ void mma_ss_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
         ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 

@@ -25,6 +25,7 @@ _IDS = {
     "q": 10, "k": 11, "v": 12, "z": 13, "beta_logit": 14, "gate_logit": 15,
     "S0": 20, "conv0": 21,
     "x": 30, "W_fa": 31, "W_fb": 32, "W_bp": 33,
+    "xh": 40, "W_qkvg": 41, "W_o": 42, "o_in": 43,
 }
 
 # Low-rank front-end widths: the pages give none; the hidden width of the
@@ -187,3 +188,23 @@ def make_lowrank(wl: Workload, device="cpu", hidden: int = LOWRANK_HIDDEN, rank:
     shp = (T, wl.B, hidden) if wl.mode == "decode" else (wl.B, T, hidden)
     x = _normal(shp, 1.0, 0.0, _gen(wl, "x", device), device)
     return {"W_fa": W_fa, "W_fb": W_fb, "W_bp": W_bp, "x": x, "hidden": hidden, "rank": rank}
+
+
+def make_projections(wl: Workload, device="cpu", hidden: int = LOWRANK_HIDDEN, N: int | None = None) -> dict:
+    """Projection weights and inputs, bf16 (round to nearest even).
+
+    W_qkvg [4*H*d, hidden] ~ N(0, 1/hidden) (W_q, W_k, W_v, W_g stacked by
+    rows), W_o [hidden, H*d] ~ N(0, 1/(H*d)), x [N, hidden] ~ N(0, 1), so that
+    q, k, v and the gate logits come out about N(0, 1) like the workloads'
+    direct draws; o_in [N, H, d] ~ N(0, 1) fp32 stands in for the token
+    step's output when the output projection is checked alone.  N defaults to
+    the workload's tokens per call (B for decode, B*T for prefill).
+    """
+    H, d = wl.H, wl.d
+    HD = H * d
+    N = (wl.B if wl.mode == "decode" else wl.B * wl.T) if N is None else N
+    W_qkvg = _normal((4 * HD, hidden), hidden ** -0.5, 0.0, _gen(wl, "W_qkvg", device), device).to(torch.bfloat16)
+    W_o = _normal((hidden, HD), HD ** -0.5, 0.0, _gen(wl, "W_o", device), device).to(torch.bfloat16)
+    x = _normal((N, hidden), 1.0, 0.0, _gen(wl, "xh", device), device).to(torch.bfloat16)
+    o_in = _normal((N, H, d), 1.0, 0.0, _gen(wl, "o_in", device), device)
+    return {"W_qkvg": W_qkvg, "W_o": W_o, "x": x, "o_in": o_in, "hidden": hidden}
