@@ -141,7 +141,8 @@ KDA_API kda_status kda_decode_step(kda_ctx *ctx, int B,
 
 /*
  * Bytes of device workspace kda_prefill needs for B sequences of T tokens
- * (0 when none is needed).
+ * (0 when none is needed; the current kernels need none, callers should
+ * still ask).
  */
 KDA_API size_t kda_prefill_workspace_bytes(const kda_ctx *ctx, int B, int T);
 
@@ -157,8 +158,14 @@ KDA_API size_t kda_prefill_workspace_bytes(const kda_ctx *ctx, int B, int T);
  *   S            [B][H][d][d] fp32 (in/out)
  *   o            [B][T][H][d] fp32 (out)
  *   workspace    device buffer of at least kda_prefill_workspace_bytes(ctx,B,T)
- *                bytes (may be NULL when that is 0); workspace_bytes is its size
- * B == 0 or T == 0 is a no-op returning KDA_OK.
+ *                bytes, 16-byte aligned (may be NULL when that is 0);
+ *                workspace_bytes is its size.  A smaller buffer gives
+ *                KDA_ERR_INVALID_ARG.
+ * B == 0 or T == 0 is a no-op returning KDA_OK.  Sequence-head pairs that
+ * would leave SMs idle (all of them when two CTAs per pair fit on the device,
+ * else those of a last partial wave) run as two CTAs that take alternate
+ * chunks and hand the state to each other; they compute the same arithmetic
+ * as one CTA, bit for bit, so results do not depend on the split.
  * After a give-up (KDA_ERR_TIMEOUT from kda_sync_status) an affected pair
  * stops at the end of a chunk and keeps its old S and window; the o rows of
  * its chunks from the one that gave up onwards are not written (earlier rows
@@ -173,8 +180,8 @@ KDA_API kda_status kda_prefill(kda_ctx *ctx, int B, int T,
 /*
  * Prefill of B packed sequences of different lengths: sequence b is tokens
  * [cu_seqlens[b], cu_seqlens[b+1]) of one token axis of total_T tokens, and
- * the result for it is that of kda_prefill on those tokens alone (same
- * arithmetic, computed by the same kernel), continuing from its own
+ * the result for it is that of kda_prefill on those tokens alone (the same
+ * arithmetic, bit for bit), continuing from its own
  * conv_state[b] and S[b].  This is the recurrence of "Kimi K3 Metal Gap
  * Analysis", section 2 "KDA Attention", row "Recurrence", run per sequence;
  * the packed layout is this library's (the pages process one sequence).

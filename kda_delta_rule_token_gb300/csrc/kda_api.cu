@@ -212,7 +212,7 @@ kda_status kda_decode_step(kda_ctx* ctx, int B, const float* q, const float* k, 
 
 size_t kda_prefill_workspace_bytes(const kda_ctx* ctx, int B, int T) {
     if (!ctx || B <= 0 || T <= 0) return 0;
-    return kda::prefill_workspace_bytes(ctx->params.H, B, T);
+    return kda::prefill_workspace_bytes(ctx->params.H, B, T, ctx->dev);
 }
 
 kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint16_t* k,
@@ -228,14 +228,14 @@ kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint
         if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
     if (!aligned4(beta_logit)) return KDA_ERR_ALIGNMENT;
     if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
-    const size_t need = kda::prefill_workspace_bytes(ctx->params.H, B, T);
+    const size_t need = kda::prefill_workspace_bytes(ctx->params.H, B, T, ctx->dev);
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
         if (!aligned16(workspace)) return KDA_ERR_ALIGNMENT;
     }
     if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::PrefillIO io{B, T, nullptr, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
-                      workspace, workspace_bytes};
+                      workspace, workspace_bytes, 0};
     cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectPrefill, [&] {
         return kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word, static_cast<cudaStream_t>(stream));
     });
@@ -258,7 +258,7 @@ kda_status kda_prefill_varlen(kda_ctx* ctx, int B, const int32_t* cu_seqlens, in
     if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::PrefillIO io{B, total_T, cu_seqlens, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
-                      nullptr, 0};
+                      nullptr, 0, 0};
     cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectVarlen, [&] {
         return kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word, static_cast<cudaStream_t>(stream));
     });

@@ -54,6 +54,10 @@ struct PrefillIO {
     float* o;
     void* workspace;
     size_t workspace_bytes;
+    // Relay launches (set by launch_prefill): heads [head0, head0 + grid/2)
+    // run as clusters of two CTAs that take alternate chunks and hand the
+    // state over through distributed shared memory.
+    int head0;
 };
 
 // Low-rank front-end weights bound to a context (borrowed, fp32), with
@@ -89,7 +93,7 @@ struct DeviceInfo {
 // cudaError_t of the launch.
 cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const DeviceInfo& dev,
                           int* err_word, cudaStream_t stream);
-size_t prefill_workspace_bytes(int H, int B, int T);
+size_t prefill_workspace_bytes(int H, int B, int T, const DeviceInfo& dev);
 cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const DeviceInfo& dev,
                            int* err_word, cudaStream_t stream);
 

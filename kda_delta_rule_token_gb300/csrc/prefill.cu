@@ -73,6 +73,7 @@ constexpr uint32_t STG_Q = OFF_ST, STG_K = OFF_ST + 16384, STG_Z = OFF_ST + 3276
 constexpr uint32_t OFF_OG = OFF_L + 32768;
 constexpr uint32_t kOGBox = 8192;
 constexpr uint32_t kStageBytes = 3 * C * D * 2 + C * D * 4;   // 80 KiB per chunk
+constexpr uint32_t kRelayBytes = D * D * 4 + D * 4;             // relay: a state and its row scales
 
 // TMEM column map (512 columns allocated).
 constexpr int TM_S = 0;     // state master, lane = key channel, column = value channel
@@ -228,6 +229,12 @@ constexpr int kIssuerB = 480, kIssuer1 = 320, kStager = 384, kOStore = 96;
 // 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and takes column group
 // w / 4 of every TMEM pass; in the thread-per-channel passes the same thread
 // owns channel c = its TMEM lane and group grp = w / 4.
+// RELAY: two CTAs per (sequence, head) take alternate chunks (CTA role r
+// does the chunks r, r + 2, ...); each builds the state-independent part of
+// its chunk (conv, norms, L/R, MMA0, the inverse, MMA_T) while the other
+// runs the state chain of the chunk before, then takes the state over from
+// it through the relay buffer, runs the chain and hands the state on.
+template <bool RELAY>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __grid_constant__ Maps maps) {
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -250,13 +257,18 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     uint64_t* s_drain = s_bar + 5;                                // give-up path: MMA issuers drained
     uint64_t* s_bar2 = s_bar + 6;                                 // MMA2 done
     uint64_t* s_bar3 = s_bar + 7;                                 // MMA3 done
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 8);
+    uint64_t* s_rxfull = s_bar + 8;                               // relay: the other CTA's state landed
+    uint64_t* s_rxfree = s_bar + 9;                               // relay: the other CTA can take a state
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bar + 10);
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
     int* s_nt = s_dead + 1;                                       // input-tile phases issued
     int* s_ng = s_dead + 2;                                       // gate-tile phases issued
+    float* s_rxesc = reinterpret_cast<float*>(s_dead + 3);        // [128] relay: received row scales
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x;
+    const int bh = RELAY ? io.head0 + (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int role = RELAY ? (int)(blockIdx.x & 1) : 0;   // first chunk of this CTA
+    constexpr int kStep = RELAY ? 2 : 1;                  // chunks between two of this CTA's
     const int b = bh / p.H, h = bh - b * p.H;
     const int H = p.H;
     // This sequence's tokens: rows [rowbase, rowbase + T) of the token axis.
@@ -312,6 +324,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         ptx::mbar_init(s_drain, 3);
         ptx::mbar_init(s_bar2, 1);
         ptx::mbar_init(s_bar3, 1);
+        ptx::mbar_init(s_rxfull, 1);
+        ptx::mbar_init(s_rxfree, 1);
         ptx::fence_mbar_init();
         *s_dead = 0;
         *s_nt = 0;
@@ -319,6 +333,9 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     }
     if (tid < D) s_gam[tid] = 0.5f * p.gamma[h * D + tid];   // gamma sigmoid(g) = s_gam + s_gam tanh(g / 2)
     sync_tc();
+    // Relay pairs: the other CTA's barriers are initialised before either
+    // CTA touches them (both CTAs of a cluster are scheduled together).
+    if constexpr (RELAY) ptx::cluster_sync();
     const uint32_t tm = *s_tmem;
     Waiter wt{s_bar, s_dead, err, 0u};
     Waiter wt2{s_bar2, s_dead, err, 0u};
@@ -327,9 +344,11 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     Waiter wgate{s_gbar, s_dead, err, 0u};
     Waiter wtT{s_tbarT, s_dead, err, 0u};
     Waiter wt1{s_bar1, s_dead, err, 0u};
-    if (nchunks > 0) {
-        stage_qkz(0);
-        stage_v(0);
+    Waiter wrx{s_rxfull, s_dead, err, 0u};
+    Waiter wfree{s_rxfree, s_dead, err, 0u};
+    if (role < nchunks) {
+        stage_qkz(role);
+        stage_v(role);
     }
 
     // Initial state into the TMEM master (row qrow, columns of this group).
@@ -383,7 +402,62 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     const int cch = (c >> 2) & 7;
 
     float esc_prev = 1.0f;   // pending e^{G_last - rho_R} of the previous chunk, per state row
-    for (int ci = 0; ci < nchunks; ++ci) {
+    // Relay pairs (a cluster of two CTAs): chunk ci's end state goes to the
+    // other CTA as the TMEM master M and its pending row scale, so that the
+    // next chunk computes exactly what a single CTA would.  M lands in the
+    // other CTA's S^T region (free there between its conv phase and its state
+    // pass), rows of 512 bytes with the 16-byte chunk index XOR (row & 7);
+    // the scales land in s_rxesc.  Each CTA says when its region is free
+    // (s_rxfree of the sender) and the stores complete on s_rxfull.
+    const uint32_t peer = (uint32_t)(role ^ 1);
+    const uint32_t peer_st = RELAY ? ptx::mapa(ptx::smem_u32(sm + OFF_ST), peer) : 0u;
+    const uint32_t peer_esc = RELAY ? ptx::mapa(ptx::smem_u32(s_rxesc), peer) : 0u;
+    const uint32_t peer_full = RELAY ? ptx::mapa(ptx::smem_u32(s_rxfull), peer) : 0u;
+    const uint32_t peer_free = RELAY ? ptx::mapa(ptx::smem_u32(s_rxfree), peer) : 0u;
+    int nrx = 0;   // relay: receives this CTA has announced (thread 0)
+
+    // State pass: the S^T operand of MMA1 scaled by e^{rho_L} to shared
+    // memory and the TMEM master scaled by e^{rho_R} (both also by the
+    // previous chunk's pending scale).  The state comes from the TMEM master,
+    // or (relay launches, after chunk 0) from the rows the other CTA stored
+    // into the S^T region, which the operand then overwrites.
+    auto state_pass = [&](bool rx, bool fb) {
+        uint32_t v[32];
+        const int j0 = grp * 32;
+        const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
+        if (rx) {
+            const uint32_t rb = OFF_ST + (uint32_t)qrow * 512;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const uint4 x = at<uint4>(sm, rb + ((uint32_t)(grp * 8 + (q4 ^ (qrow & 7))) << 4));
+                v[4 * q4] = x.x; v[4 * q4 + 1] = x.y; v[4 * q4 + 2] = x.z; v[4 * q4 + 3] = x.w;
+            }
+            esc_prev = s_rxesc[qrow];
+            __syncthreads();   // every received row is read before the operand overwrites it
+        } else {
+            tc::ld32(ta, v);
+            tc::wait_ld();
+        }
+        const float gl = s_gh0[qrow] + s_gh1[qrow];
+        const float eL = esc_prev * (fb ? 1.0f : __expf(0.5f * gl));
+        const float eR = esc_prev * __expf(fb ? gl : 0.5f * gl);
+        // S^T operand element (row j, K = qrow): K block and chunk are fixed per thread.
+        const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
+        const int kch = (qrow >> 2) & 7;
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int j = j0 + g8 * 8 + i;
+                const float sv = __uint_as_float(v[g8 * 8 + i]);
+                at<uint32_t>(sm, OFF_ST + kq + j * 128 + ((kch ^ (j & 7)) << 4)) = tc::f2tf32(sv * eL);
+                v[g8 * 8 + i] = __float_as_uint(sv * eR);
+            }
+        }
+        tc::st32(ta, v);
+    };
+
+    for (int ci = role; ci < nchunks; ci += kStep) {
         const int t0 = ci * C;
         const int n = min(C, T - t0);
 
@@ -400,7 +474,14 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const uint32_t dst = grp == 0 ? OFF_L + kpL + C * 128 : (grp == 1 ? OFF_L + kpL : OFF_V + kpR);
             auto unpk_bf2 = [](uint32_t u) { return pk(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)); };
             f32x2 M3, M2, M1;   // window, oldest first
-            if (th == 0) {
+            if (RELAY && th == 0 && ci > 0) {
+                // the chunk before ran in the other CTA: its last three inputs from global memory
+                const uint16_t* xg = (grp == 0 ? io.q : (grp == 1 ? io.k : io.v)) + (size_t)h * D + cp;
+                const size_t r3 = rowbase + (size_t)t0 - 3;
+                M3 = unpk_bf2(*reinterpret_cast<const uint32_t*>(xg + r3 * HD));
+                M2 = unpk_bf2(*reinterpret_cast<const uint32_t*>(xg + (r3 + 1) * HD));
+                M1 = unpk_bf2(*reinterpret_cast<const uint32_t*>(xg + (r3 + 2) * HD));
+            } else if (th == 0) {
                 const float* w = s_win + ((ci & 1) * 9 + grp * 3) * D + cp;
                 M3 = pk(w[0], w[1]); M2 = pk(w[D], w[D + 1]); M1 = pk(w[2 * D], w[2 * D + 1]);
             } else {
@@ -493,6 +574,13 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // The exact fallback when a chunk's decay may exceed kMaxSpan in some
         // channel (decided per half of the chunk, so conservatively).
         const bool fb = __syncthreads_or(big) != 0;
+        // Relay: the staged tiles in the S^T region are consumed, so the other
+        // CTA may store the state after chunk ci - 1 there.
+        if (RELAY && ci > 0 && tid == 0) {
+            ptx::mbar_arrive_expect_tx(s_rxfull, kRelayBytes);
+            ptx::mbar_arrive_remote(peer_free);
+            ++nrx;
+        }
 
         // ---- A2: per-token norms of the conv outputs (4 threads per row, one
         //      per 32-channel block; the 8 lanes of a quarter warp take 8 rows of
@@ -512,34 +600,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 s_beta[tid] = tid < n ? sigmoidf_(blog) : 0.f;
         }
 
-        // ---- D: state pass: S^T operand scaled by e^{rho_L}, master scaled by
-        //      e^{rho_R} (both also by the previous chunk's pending scale).
-        {
-            const float gl = s_gh0[qrow] + s_gh1[qrow];
-            const float eL = esc_prev * (fb ? 1.0f : __expf(0.5f * gl));
-            const float eR = esc_prev * __expf(fb ? gl : 0.5f * gl);
-            // S^T operand element (row j, K = qrow): K block and chunk are fixed per thread.
-            const uint32_t kq = (uint32_t)((qrow >> 5) * 128 * 128 + (qrow & 3) * 4);
-            const int kch = (qrow >> 2) & 7;
-            {
-                uint32_t v[32];
-                const int j0 = grp * 32;
-                const uint32_t ta = tc::taddr(tm, warp, TM_S + j0);
-                tc::ld32(ta, v);
-                tc::wait_ld();
-#pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int j = j0 + g8 * 8 + i;
-                        const float sv = __uint_as_float(v[g8 * 8 + i]);
-                        at<uint32_t>(sm, OFF_ST + kq + j * 128 + ((kch ^ (j & 7)) << 4)) = tc::f2tf32(sv * eL);
-                        v[g8 * 8 + i] = __float_as_uint(sv * eR);
-                    }
-                }
-                tc::st32(ta, v);
-            }
-        }
+        // ---- D: state pass (relay launches: later, once the state has arrived).
+        if (!RELAY) state_pass(false, fb);
         publish();   // norms, beta; S^T operand and rescaled master
 
         // ---- A2b (rare): exact [A'; P] when the chunk decays by more than kMaxSpan.
@@ -639,7 +701,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             if (half == 1) tc::commit(s_bar1);
         };
-        if (tid == kIssuer1) mma1_part(0);
+        if (!RELAY && tid == kIssuer1) mma1_part(0);
         if (!fb) wt.wait();   // MMA0
 
         // ---- C1: N = Diag(beta) A' to shared memory as N^T (row b holds
@@ -669,7 +731,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         tc::wait_st();
         sync_tc();
 
-        if (tid == kIssuer1) mma1_part(1);
+        if (!RELAY && tid == kIssuer1) mma1_part(1);
 
         // ---- C2: Minv = (I + N)^{-1} (N strictly lower) by 16 x 16 blocks.
         //      Pass 1: forward substitution with the diagonal block I + N_II
@@ -785,9 +847,20 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
                 }
             }
         }
+        if constexpr (RELAY) {
+            // The state after chunk ci - 1 (the other CTA's) arrives; chunk 0
+            // starts from the initial state in the TMEM master.
+            if (ci > 0) wrx.wait();
+            state_pass(ci > 0, fb);
+            publish();
+            if (tid == kIssuer1) {
+                mma1_part(0);
+                mma1_part(1);
+            }
+        }
         wt1.wait();   // MMA1
         if (tid == kStager) {
-            if (ci + 1 < nchunks) stage_qkz(ci + 1);   // the S^T region is free now
+            if (ci + kStep < nchunks) stage_qkz(ci + kStep);   // the S^T region is free now
             // this chunk's gate tile into the upper half of the L region
             ++*s_ng;
             ptx::mbar_arrive_expect_tx(s_gbar, C * D * 4);
@@ -827,7 +900,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
         publish();
         wtT.wait();   // MMA_T
-        if (ci + 1 < nchunks) stage_v(ci + 1);     // the Minv^T region is free now
+        if (ci + kStep < nchunks) stage_v(ci + kStep);     // the Minv^T region is free now
 
         // ---- DT -> tf32 in place (A operand of MMA2).
         {
@@ -964,6 +1037,23 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             const float gl = s_gh0[qrow] + s_gh1[qrow];
             esc_prev = __expf(fb ? 0.f : 0.5f * gl);   // e^{G_last - rho_R}
         }
+        if (RELAY && ci + 1 < nchunks) {
+            // The master after this chunk and its pending scale e^{G_last -
+            // rho_R} to the other CTA, once its region is free (row qrow, the
+            // columns of this group; the group-0 threads send the scale).
+            uint32_t sv[32];
+            tc::ld32(tc::taddr(tm, warp, TM_S + grp * 32), sv);
+            wfree.wait();
+            tc::wait_ld();
+            if (!*(volatile int*)s_dead) {
+                const uint32_t rb = peer_st + (uint32_t)qrow * 512;
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                    ptx::st_async_v4(rb + ((uint32_t)(grp * 8 + (q4 ^ (qrow & 7))) << 4), sv[4 * q4], sv[4 * q4 + 1],
+                                     sv[4 * q4 + 2], sv[4 * q4 + 3], peer_full);
+                if (grp == 0) ptx::st_async_b32(peer_esc + (uint32_t)qrow * 4, __float_as_uint(esc_prev), peer_full);
+            }
+        }
         // A bounded wait that gave up anywhere in the CTA ends the walk for
         // every thread at once (the vote is uniform).
         tc::fence_before();
@@ -974,8 +1064,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
     const bool dead = __syncthreads_or(*(volatile int*)s_dead) != 0;
 
     // Final state and conv window back to global memory (not after a give-up:
-    // S and the window then keep their old contents).
-    if (!dead) {
+    // S and the window then keep their old contents; in relay launches by the
+    // CTA that ran the last chunk).
+    const bool owns_end = !RELAY || (nchunks > 0 && (nchunks - 1) % 2 == role);
+    if (!dead && owns_end) {
         float* dst = io.S + ((size_t)bh * D + qrow) * D + grp * 32;
         uint32_t s[32];
         tc::ld32(tc::taddr(tm, warp, TM_S + grp * 32), s);
@@ -1015,7 +1107,13 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             if (*s_ng > 0) ptx::mbar_wait_timed(s_gbar, (uint32_t)((*s_ng - 1) & 1));
         }
         if (tid == 0) ptx::mbar_wait_timed(s_drain, 0);
+        // Relay: a state this CTA announced it could take may still be on
+        // its way into its shared memory.
+        if (RELAY && tid == 0 && nrx > 0) ptx::mbar_wait_timed(s_rxfull, (uint32_t)((nrx - 1) & 1));
     }
+    // Relay: neither CTA leaves while the other may still address its
+    // shared memory (every wait before this point is bounded, so both get here).
+    if constexpr (RELAY) ptx::cluster_sync();
     sync_tc();
     if (warp == 0) tc::dealloc(tm, 512);
 }
@@ -1053,17 +1151,31 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Heads that run as relay pairs: all of them when twice their number fits
+// on the SMs (few-head workloads: otherwise most SMs idle), else the heads of
+// a last, partial wave when it fills at most half of the SMs (its pairs then
+// finish in about half the time of single CTAs); none for single-chunk
+// sequences or packed ones.
+long long relay_heads(long long heads, int nchunks, int sm_count) {
+    if (nchunks < 2 || sm_count < 2) return 0;
+    if (2 * heads <= sm_count) return heads;
+    const long long rem = heads % sm_count;
+    return (rem > 0 && 2 * rem <= sm_count) ? rem : 0;
+}
+
 }  // namespace
 
-size_t prefill_workspace_bytes(int, int, int) { return 0; }
+size_t prefill_workspace_bytes(int, int, int, const DeviceInfo&) { return 0; }
 
 cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const DeviceInfo& dev,
                            int* err_word, cudaStream_t stream) {
     const long long grid = (long long)io.B * p.H;
     if (grid <= 0 || io.T <= 0) return cudaSuccess;
     if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(kda_prefill_kernel,
+        cudaError_t e = cudaFuncSetAttribute(kda_prefill_kernel<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(kda_prefill_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device].store(true, std::memory_order_release);
     }
@@ -1078,9 +1190,38 @@ cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const Devi
         !make_map(&maps.o, io.o, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.H, io.T, mB, 32,
                   CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    kda_prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p, io, err_word, maps);
-    count_launches(1);
-    return cudaGetLastError();
+    const long long rh = io.cu_seqlens ? 0 : relay_heads(grid, (io.T + C - 1) / C, dev.sm_count);
+    const long long single = grid - rh;
+    if (single > 0) {
+        PrefillIO io1 = io;
+        io1.head0 = 0;
+        kda_prefill_kernel<false><<<(unsigned)single, kThreads, kSmemBytes, stream>>>(p, io1, err_word, maps);
+        count_launches(1);
+        if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+    }
+    if (rh > 0) {
+        // The heads [single, grid) as CTA pairs, each pair one cluster of two
+        // (scheduled together; a pair waits on nothing outside itself).
+        PrefillIO io2 = io;
+        io2.head0 = (int)single;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)(2 * rh));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kda_prefill_kernel<true>, p, io2, err_word, maps);
+        count_launches(1);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
 }
 
 }  // namespace kda

@@ -83,6 +83,41 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity, int* err
     return false;
 }
 
+// Thread-block clusters.  The address, in the cluster's shared window, of
+// the location at shared-memory address `saddr` of CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (release at cluster
+// scope: this thread's earlier memory operations are visible to the CTA that
+// waits on it).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// 16-byte and 4-byte stores into another CTA's shared memory (cluster
+// addresses), each completing its bytes on an mbarrier of that CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(cluster_addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t cluster_addr, uint32_t a, uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 ::"r"(cluster_addr), "r"(a), "r"(cluster_bar)
+                 : "memory");
+}
+
+// Barrier over every thread of every CTA of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Bulk (non-tensor) TMA copy global -> this CTA's shared memory, completing
 // `bytes` of transaction count on mbarrier m.  Addresses 16-byte aligned,
 // bytes a multiple of 16.

@@ -115,10 +115,12 @@ def test_injected_prefill_launch_failures(inject):
     inject("prefill,prefill_varlen")
     ctx = _create(wl, params)
     try:
+        nws = kda.kda_prefill_workspace_bytes(ctx, wl.B, wl.T)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=DEV)
         n0 = kda.kda_launch_count()
         with pytest.raises(kda.KDAError) as ei:
             kda.kda_prefill(ctx, wl.B, wl.T, q, k, v, tokens["z"], tokens["beta_logit"],
-                            tokens["gate_logit"], conv, S, o)
+                            tokens["gate_logit"], conv, S, o, ws, nws)
         assert ei.value.status == kda.KDA_ERR_CUDA
         with pytest.raises(kda.KDAError) as ei:
             kda.kda_prefill_varlen(ctx, 1, cu, wl.T, q[0], k[0], v[0], tokens["z"][0],

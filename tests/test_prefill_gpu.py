@@ -227,3 +227,17 @@ def test_graph_replay_equals_launch():
     assert torch.equal(o_g, o_l)
     assert torch.equal(S2, S)
     assert torch.equal(c2, conv)
+
+
+def test_relay_pairs_match_oracle_and_tail_split():
+    """Heads run as CTA pairs that alternate chunks and relay the state
+    (few heads: every head; more heads than SMs: the last partial wave's).
+    200 heads = one full wave of single CTAs plus a 48-head tail of pairs on
+    152 SMs; sampled heads from both parts against the oracle."""
+    wl = synth.shrink(synth.WORKLOADS["prefill_b8_h64_t8192"], B=2, H=100, T=200)
+    params, tokens, S, conv = _setup(wl)
+    S0, c0 = S.clone(), conv.clone()
+    o = gpu_prefill(wl, params, tokens, S, conv)
+    pairs = [(0, 0), (0, 57), (1, 51), (1, 52), (1, 99)]
+    ref = oracle_pairs(params, tokens, S0, c0, pairs, call_major=False)
+    check(ref, o, S, conv, pairs)

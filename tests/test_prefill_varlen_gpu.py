@@ -3,7 +3,10 @@
 Each sequence is checked against the fp64 oracle run on that sequence alone
 (rel-L2 2e-3 over o and the final S; the conv window exactly), and the packed
 call must give exactly what one kda_prefill call per sequence gives: the
-same kernel runs the same arithmetic, only the addressing differs.  o, S and
+same arithmetic, only the addressing differs (a few-head kda_prefill call
+runs its heads as CTA pairs that relay the state; the relay carries the
+state in the form a single CTA keeps it, so the results stay bit for bit
+equal).  o, S and
 the windows sit inside poisoned guard regions during each packed call.
 """
 import numpy as np
@@ -66,8 +69,10 @@ def run_separate(H, params, tokens, lengths, S, conv):
             sl = {n: tokens[n][b:b + 1, :L].contiguous() for n in tokens}
             o = torch.empty((1, L, H, 128), device=DEV)
             Sb, cb = S[b:b + 1].clone(), conv[b:b + 1].clone()
+            nws = kda.kda_prefill_workspace_bytes(ctx, 1, L)
+            ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=DEV)
             kda.kda_prefill(ctx, 1, L, bits(sl["q"]), bits(sl["k"]), bits(sl["v"]), sl["z"],
-                            sl["beta_logit"], sl["gate_logit"], cb, Sb, o)
+                            sl["beta_logit"], sl["gate_logit"], cb, Sb, o, ws, nws)
             S[b:b + 1].copy_(Sb)
             conv[b:b + 1].copy_(cb)
             outs.append(o[0])
