@@ -67,6 +67,13 @@ def _load(lib_path: str | None = None):
         lib.kda_oracle_run.restype = ctypes.c_int
         lib.kda_oracle_run.argtypes = (
             [ctypes.c_int] * 4 + [dp] * 10 + [ctypes.c_double] * 2 + [dp] * 9 + [ctypes.c_int])
+        lib.kda_oracle_run_bf16_state.restype = ctypes.c_int
+        lib.kda_oracle_run_bf16_state.argtypes = lib.kda_oracle_run.argtypes
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        lib.kda_oracle_bf16_round_n.restype = None
+        lib.kda_oracle_bf16_round_n.argtypes = [ctypes.c_size_t, dp, u16p]
+        lib.kda_oracle_bf16_value_n.restype = None
+        lib.kda_oracle_bf16_value_n.argtypes = [ctypes.c_size_t, u16p, dp]
         lib.kda_oracle_cpu_count.restype = ctypes.c_int
         lib.kda_oracle_cpu_count.argtypes = []
         lib.kda_oracle_lowrank.restype = ctypes.c_int
@@ -107,14 +114,16 @@ def _f64(x):
 
 def run(q, k, v, z, beta_logit, gate_logit, conv_w, dt_bias, A_log, gamma,
         conv_state, S, *, l2_eps=1e-6, rms_eps=1e-6, intermediates=False,
-        nthreads=1, lib_path: str | None = None) -> OracleOut:
+        nthreads=1, state_bf16=False, lib_path: str | None = None) -> OracleOut:
     """Run T tokens of the KDA step for every (sequence, head).
 
     q, k, v, z, gate_logit: [B, T, H, d]; beta_logit: [B, T, H];
     conv_w: [3, H*d, 4]; dt_bias, A_log, gamma: [H, d];
     conv_state: [B, 3, 3*H*d]; S: [B, H, d, d].  Inputs are copied to
     float64 (exact for fp32 and bf16 values); S and conv_state are returned
-    updated, the caller's arrays are left untouched.
+    updated, the caller's arrays are left untouched.  With state_bf16 the
+    state is stored as bfloat16 between tokens (S must hold bfloat16 values
+    on entry and is returned rounded); the read-outs are unchanged in form.
     """
     q, k, v, z, gate_logit = (_f64(a) for a in (q, k, v, z, gate_logit))
     beta_logit, conv_w, dt_bias, A_log, gamma = (
@@ -133,7 +142,11 @@ def run(q, k, v, z, beta_logit, gate_logit, conv_w, dt_bias, A_log, gamma,
     o_pre = np.zeros((B, T, H, d))
     extra = [np.zeros((B, T, H, d)) for _ in range(4)] + [np.zeros((B, T, H))] \
         if intermediates else [None] * 5
-    rc = _load(lib_path).kda_oracle_run(
+    lib = _load(lib_path)
+    if state_bf16:
+        assert np.array_equal(bf16_value(bf16_round(St, lib_path=lib_path), lib_path=lib_path), St), \
+            "state_bf16 wants S made of bfloat16 values"
+    rc = (lib.kda_oracle_run_bf16_state if state_bf16 else lib.kda_oracle_run)(
         B, T, H, d, _ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta_logit),
         _ptr(gate_logit), _ptr(conv_w), _ptr(dt_bias), _ptr(A_log), _ptr(gamma),
         float(l2_eps), float(rms_eps), _ptr(cs), _ptr(St), _ptr(o), _ptr(o_pre),
@@ -141,6 +154,24 @@ def run(q, k, v, z, beta_logit, gate_logit, conv_w, dt_bias, A_log, gamma,
     if rc != 0:
         raise ValueError(f"kda_oracle_run rejected its arguments (rc={rc})")
     return OracleOut(o, o_pre, St, cs, *extra)
+
+
+def bf16_round(x, *, lib_path: str | None = None) -> np.ndarray:
+    """bfloat16 patterns (uint16) of x rounded to nearest, ties to even."""
+    x = _f64(x)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load(lib_path).kda_oracle_bf16_round_n(
+        x.size, _ptr(x), out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)))
+    return out
+
+
+def bf16_value(b, *, lib_path: str | None = None) -> np.ndarray:
+    """Exact float64 values of bfloat16 patterns."""
+    b = np.ascontiguousarray(np.asarray(b, dtype=np.uint16))
+    out = np.empty(b.shape, dtype=np.float64)
+    _load(lib_path).kda_oracle_bf16_value_n(
+        b.size, b.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)), _ptr(out))
+    return out
 
 
 def lowrank(x, W_fa, W_fb, W_bp, H, d=128, *, lib_path: str | None = None):

@@ -27,6 +27,7 @@
 
 #include <math.h>
 #include <pthread.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 #ifdef __linux__
@@ -44,6 +45,54 @@ static double softplus(double x)
     return log1p(exp(x));
 }
 
+/*
+ * bfloat16: 1 sign bit, the 8 exponent bits of IEEE binary32 and 7 stored
+ * fraction bits, i.e. binary32 with 8 significant bits.  Normal values are
+ * m * 2^(E-7) with m in [128, 255] and E in [-126, 127]; subnormals are
+ * m * 2^-133 with m in [0, 127].  Rounding is to nearest, ties to the even
+ * m; a magnitude that rounds to 2^128 or above becomes infinity.  The bit
+ * pattern is the upper half of the binary32 pattern of the same value.
+ */
+uint16_t kda_oracle_bf16_round(double x)
+{
+    if (isnan(x)) return 0x7FC0;
+    const uint16_t sign = signbit(x) ? 0x8000 : 0;
+    const double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7F80;
+    int e;
+    frexp(a, &e);                   /* a in [2^(e-1), 2^e) */
+    int E = e - 1;
+    if (E < -126) E = -126;         /* the subnormal spacing is that of E = -126 */
+    const double spacing = ldexp(1.0, E - 7);
+    const double m = a / spacing;   /* exact: a power-of-two scaling */
+    const double r = nearbyint(m);  /* to nearest, ties to even (default mode) */
+    const double val = r * spacing;
+    if (val >= ldexp(1.0, 128)) return sign | 0x7F80;
+    const float f = (float)val;     /* exact: every bfloat16 value is a binary32 value */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof(bits));
+    return (uint16_t)(sign | (bits >> 16));
+}
+
+double kda_oracle_bf16_value(uint16_t b)
+{
+    const uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof(f));
+    return (double)f;
+}
+
+void kda_oracle_bf16_round_n(size_t n, const double *x, uint16_t *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = kda_oracle_bf16_round(x[i]);
+}
+
+void kda_oracle_bf16_value_n(size_t n, const uint16_t *b, double *out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = kda_oracle_bf16_value(b[i]);
+}
+
 typedef struct {
     int B, T, H, d;
     const double *q, *k, *v, *z, *beta_logit, *gate_logit;
@@ -51,6 +100,7 @@ typedef struct {
     double l2_eps, rms_eps;
     double *conv_state, *S, *o, *o_pre;
     double *qhat, *khat, *vconv, *gk_out, *beta_out;
+    int state_bf16;   /* store S as bfloat16 between tokens */
 } job_t;
 
 /*
@@ -154,6 +204,13 @@ static void run_head(const job_t *J, int b, int h)
             if (J->o_pre) J->o_pre[row + j] = op[j];
         }
 
+        /* bfloat16 state: the token's arithmetic and read-out use the new
+         * state as computed; what is kept for the next token is its
+         * rounding to bfloat16. */
+        if (J->state_bf16)
+            for (size_t i = 0; i < (size_t)d * d; ++i)
+                S[i] = kda_oracle_bf16_value(kda_oracle_bf16_round(S[i]));
+
         if (J->qhat) memcpy(J->qhat + row, qv, sizeof(double) * d);
         if (J->khat) memcpy(J->khat + row, kv, sizeof(double) * d);
         if (J->vconv) memcpy(J->vconv + row, vv, sizeof(double) * d);
@@ -243,7 +300,7 @@ int kda_oracle_cpu_count(void)
     return 1;
 }
 
-int kda_oracle_run(int B, int T, int H, int d,
+static int run_all(int B, int T, int H, int d,
                    const double *q, const double *k, const double *v,
                    const double *z, const double *beta_logit,
                    const double *gate_logit,
@@ -254,7 +311,7 @@ int kda_oracle_run(int B, int T, int H, int d,
                    double *o, double *o_pre,
                    double *qhat, double *khat, double *vconv,
                    double *gk, double *beta,
-                   int nthreads)
+                   int nthreads, int state_bf16)
 {
     if (B < 0 || T < 0 || H <= 0 || d <= 0) return -1;
     if (B == 0 || T == 0) return 0;
@@ -263,7 +320,7 @@ int kda_oracle_run(int B, int T, int H, int d,
         return -1;
     job_t J = {B, T, H, d, q, k, v, z, beta_logit, gate_logit, conv_w,
                dt_bias, A_log, gamma, l2_eps, rms_eps, conv_state, S, o,
-               o_pre, qhat, khat, vconv, gk, beta};
+               o_pre, qhat, khat, vconv, gk, beta, state_bf16};
     const int n = B * H;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > n) nthreads = n;
@@ -288,4 +345,40 @@ int kda_oracle_run(int B, int T, int H, int d,
     free(tid);
     free(ws);
     return 0;
+}
+
+int kda_oracle_run(int B, int T, int H, int d,
+                   const double *q, const double *k, const double *v,
+                   const double *z, const double *beta_logit,
+                   const double *gate_logit,
+                   const double *conv_w, const double *dt_bias,
+                   const double *A_log, const double *gamma,
+                   double l2_eps, double rms_eps,
+                   double *conv_state, double *S,
+                   double *o, double *o_pre,
+                   double *qhat, double *khat, double *vconv,
+                   double *gk, double *beta,
+                   int nthreads)
+{
+    return run_all(B, T, H, d, q, k, v, z, beta_logit, gate_logit, conv_w, dt_bias, A_log, gamma,
+                   l2_eps, rms_eps, conv_state, S, o, o_pre, qhat, khat, vconv, gk, beta,
+                   nthreads, 0);
+}
+
+int kda_oracle_run_bf16_state(int B, int T, int H, int d,
+                              const double *q, const double *k, const double *v,
+                              const double *z, const double *beta_logit,
+                              const double *gate_logit,
+                              const double *conv_w, const double *dt_bias,
+                              const double *A_log, const double *gamma,
+                              double l2_eps, double rms_eps,
+                              double *conv_state, double *S,
+                              double *o, double *o_pre,
+                              double *qhat, double *khat, double *vconv,
+                              double *gk, double *beta,
+                              int nthreads)
+{
+    return run_all(B, T, H, d, q, k, v, z, beta_logit, gate_logit, conv_w, dt_bias, A_log, gamma,
+                   l2_eps, rms_eps, conv_state, S, o, o_pre, qhat, khat, vconv, gk, beta,
+                   nthreads, 1);
 }

@@ -30,6 +30,9 @@
 #ifndef KDA_ORACLE_H
 #define KDA_ORACLE_H
 
+#include <stddef.h>
+#include <stdint.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -75,6 +78,43 @@ int kda_oracle_lowrank(int N, int hidden, int rank, int H, int d,
  * Returns 0 on success, -1 on a bad argument.
  */
 int kda_oracle_project(int N, int in, int out, const double *x, const double *W, double *y);
+
+/*
+ * The same T tokens with the state stored as bfloat16 between tokens: each
+ * token runs in double precision from the stored state, its read-out uses
+ * the new state as computed, and the new state is then rounded to bfloat16
+ * (to nearest, ties to even) for the next token.  S comes in as bfloat16
+ * values (doubles that kda_oracle_bf16_round maps to themselves) and goes out
+ * rounded.  This is the storage of the "Zero-copy state persistence" and
+ * "Wrap-once buffer cache" notes of "Metal (Apple GPU) backend for Kimi K3"
+ * (model-lifetime state kept across tokens) at half the bytes; the pages
+ * give no state precision, so the rounding point is this reading.
+ * Returns 0 on success, -1 on a bad argument.
+ */
+int kda_oracle_run_bf16_state(int B, int T, int H, int d,
+                              const double *q, const double *k, const double *v,
+                              const double *z, const double *beta_logit,
+                              const double *gate_logit,
+                              const double *conv_w, const double *dt_bias,
+                              const double *A_log, const double *gamma,
+                              double l2_eps, double rms_eps,
+                              double *conv_state, double *S,
+                              double *o, double *o_pre,
+                              double *qhat, double *khat, double *vconv,
+                              double *gk, double *beta,
+                              int nthreads);
+
+/*
+ * bfloat16 (binary32's sign and 8 exponent bits, 7 stored fraction bits):
+ * kda_oracle_bf16_round rounds a double to nearest, ties to even (overflow
+ * to infinity, subnormals kept) and returns the 16-bit pattern;
+ * kda_oracle_bf16_value returns the exact value of a pattern.  The _n forms
+ * map arrays of n elements.
+ */
+uint16_t kda_oracle_bf16_round(double x);
+double kda_oracle_bf16_value(uint16_t b);
+void kda_oracle_bf16_round_n(size_t n, const double *x, uint16_t *out);
+void kda_oracle_bf16_value_n(size_t n, const uint16_t *b, double *out);
 
 /* Number of hardware threads this process may run on (sched affinity). */
 int kda_oracle_cpu_count(void);

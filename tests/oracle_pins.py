@@ -336,8 +336,112 @@ def pin_project_orthogonal(lib_path=None):
     np.testing.assert_allclose(oracle.project(y, Q.T.copy(), lib_path=lib_path), x, rtol=0, atol=1e-12)
 
 
+# ---- bfloat16 state storage -------------------------------------------------
+# bfloat16 = IEEE binary32's sign and 8 exponent bits with 7 stored fraction
+# bits: normal values m * 2^(E-7), m in [128, 255], E in [-126, 127];
+# subnormals m * 2^-133, m in [0, 127]; pattern = upper half of the binary32
+# pattern.  Rounding to nearest, ties to the even m, overflow to infinity.
+
+_BF16_TABLE = [   # (value, pattern), each worked out from the format by hand
+    (1.0, 0x3F80),
+    (1.0 + 2.0 ** -7, 0x3F81),                  # next value above 1
+    (1.0 + 2.0 ** -8, 0x3F80),                  # tie between m = 128 and 129: even 128
+    (1.0 + 3 * 2.0 ** -8, 0x3F82),              # tie between m = 129 and 130: even 130
+    (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81),     # just above the tie
+    (-(1.0 + 2.0 ** -8 + 2.0 ** -40), 0xBF81),
+    (2.0 - 2.0 ** -9, 0x4000),                  # rounds up across the exponent: 2.0
+    (-2.5, 0xC020),
+    (0.0, 0x0000),
+    (-0.0, 0x8000),
+    (2.0 ** -126, 0x0080),                      # smallest normal
+    (2.0 ** -133, 0x0001),                      # smallest subnormal
+    (2.0 ** -134, 0x0000),                      # tie between 0 and 2^-133: even 0
+    (3 * 2.0 ** -134, 0x0002),                  # tie between m = 1 and 2: even 2
+    (127 * 2.0 ** -133 + 2.0 ** -134, 0x0080),  # tie between m = 127 and 128: even 128
+    ((2.0 - 2.0 ** -7) * 2.0 ** 127, 0x7F7F),   # largest finite
+    ((2.0 - 2.0 ** -8) * 2.0 ** 127, 0x7F80),   # tie between largest (m odd) and 2^128: infinity
+    (-1e39, 0xFF80),
+]
+
+
+def pin_bf16_round_table(lib_path=None):
+    """Rounding to bfloat16 at ties, carries, subnormals and overflow,
+    against values worked out from the format's definition."""
+    vals = np.array([v for v, _ in _BF16_TABLE])
+    want = np.array([b for _, b in _BF16_TABLE], dtype=np.uint16)
+    got = oracle.bf16_round(vals, lib_path=lib_path)
+    assert np.array_equal(got, want), [(v, hex(g), hex(w)) for v, g, w in zip(vals, got, want) if g != w]
+    finite = want[(want & 0x7F80) != 0x7F80]
+    back = oracle.bf16_value(finite, lib_path=lib_path)
+    assert np.array_equal(oracle.bf16_round(back, lib_path=lib_path), finite)   # values round to themselves
+
+
+def pin_bf16_round_matches_library(lib_path=None):
+    """On binary32 inputs (exact in double) the rounding equals the
+    library's float32 -> bfloat16 conversion (round to nearest even), across
+    normal, subnormal and near-overflow magnitudes."""
+    import torch
+    rng = np.random.default_rng(501)
+    bits = rng.integers(0, 2 ** 32, 200_000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    got = oracle.bf16_round(f.astype(np.float64), lib_path=lib_path)
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref), int((got != ref).sum())
+    assert np.array_equal(oracle.bf16_value(got, lib_path=lib_path),
+                          torch.from_numpy(ref.view(np.int16).copy()).view(torch.bfloat16).double().numpy())
+
+
+def pin_bf16_state_halving(lib_path=None):
+    """bfloat16 state storage, beta = 0 and a = e^gk = 1/2 exactly (A_log =
+    z = dt_bias = 0: gk = -softplus(0) = -ln 2): every token halves the
+    state and stores the rounding, so subnormal states walk down their own
+    sequences with ties to even (3 -> 2 -> 1 -> 0, 7 -> 4 -> 2 -> 1 units of
+    2^-133), while normal values halve exactly.  Without bfloat16 storage
+    the same run gives S0 * 2^-T exactly."""
+    T, H = 4, 1
+    inp = _inputs(503, T=T, H=H)
+    inp["beta_logit"] = np.full((1, T, H), -np.inf)
+    inp["A_log"] = np.zeros((H, D))
+    inp["dt_bias"] = np.zeros((H, D))
+    inp["z"] = np.zeros((1, T, H, D))
+    S0 = np.zeros((1, H, D, D))
+    unit = 2.0 ** -133
+    S0[0, 0, 0, :4] = np.array([3, 5, 6, 7]) * unit
+    S0[0, 0, 1, :3] = [1.0, -0.75, 2.0 ** -120]
+    inp["S"] = S0
+    walk = {3: [2, 1, 0, 0], 5: [2, 1, 0, 0], 6: [3, 2, 1, 0], 7: [4, 2, 1, 0]}
+    for t in range(1, T + 1):
+        step = dict(inp, q=inp["q"][:, :t], k=inp["k"][:, :t], v=inp["v"][:, :t], z=inp["z"][:, :t],
+                    beta_logit=inp["beta_logit"][:, :t], gate_logit=inp["gate_logit"][:, :t])
+        Sb = _run(step, lib_path, state_bf16=True).S[0, 0]
+        np.testing.assert_array_equal(Sb[0, :4], [walk[m][t - 1] * unit for m in (3, 5, 6, 7)])
+        np.testing.assert_array_equal(Sb[1, :3], np.array([1.0, -0.75, 2.0 ** -120]) * 2.0 ** -t)
+        assert not Sb[2:].any() and not Sb[:2, 4:].any()
+        Sf = _run(step, lib_path).S[0, 0]
+        np.testing.assert_array_equal(Sf, S0[0, 0] * 2.0 ** -t)
+
+
+def pin_bf16_state_readout_unrounded(lib_path=None):
+    """bfloat16 state storage keeps the read-out of the token on the new
+    state as computed: from a zero state and window, o_pre = beta v_conv
+    (q_hat . k_hat) to double rounding, while the stored S_1 is the
+    bfloat16 rounding of beta k_hat v_conv^T."""
+    inp = _inputs(505, T=1, H=2)
+    full = _run(inp, lib_path, intermediates=True)
+    out = _run(inp, lib_path, intermediates=True, state_bf16=True)
+    for h in range(2):
+        qh, kh, vc = out.qhat[0, 0, h], out.khat[0, 0, h], out.vconv[0, 0, h]
+        beta = out.beta[0, 0, h]
+        np.testing.assert_allclose(out.o_pre[0, 0, h], beta * vc * float(qh @ kh), rtol=1e-12, atol=1e-15)
+        want = oracle.bf16_value(oracle.bf16_round(full.S[0, h], lib_path=lib_path), lib_path=lib_path)
+        np.testing.assert_array_equal(out.S[0, h], want)
+        assert not np.array_equal(out.S[0, h], full.S[0, h])   # the rounding did happen
+
+
 PINS = [pin_token0_identity, pin_identity_when_no_write_no_decay, pin_decay_only_closed_form,
         pin_delta_rule_write, pin_bruteforce_products, pin_conv_one_hot_tap, pin_conv_impulse,
         pin_window_continuity, pin_l2_norm, pin_rmsnorm_gate_gamma, pin_contraction_bound,
         pin_decay_values, pin_lowrank_one_hot, pin_lowrank_zero_fa, pin_lowrank_rank_and_linearity,
-        pin_project_one_hot_and_linearity, pin_project_orthogonal]
+        pin_project_one_hot_and_linearity, pin_project_orthogonal, pin_bf16_round_table,
+        pin_bf16_round_matches_library, pin_bf16_state_halving, pin_bf16_state_readout_unrounded]

@@ -41,6 +41,14 @@ MUTANTS = [
     ("project_transposed", "s += wi[j] * xn[j];", "s += W[(size_t)j * out + i] * xn[j];"),
     ("project_token_stride", "const double *xn = x + (size_t)n * in;", "const double *xn = x + (size_t)n * out;"),
     ("project_output_shifted", "y[(size_t)n * out + i] = s;", "y[(size_t)n * out + (i + 1) % out] = s;"),
+    # bfloat16 state storage
+    ("bf16_ties_away", "const double r = nearbyint(m);", "const double r = round(m);"),
+    ("bf16_truncates", "const double r = nearbyint(m);", "const double r = trunc(m);"),
+    ("bf16_no_subnormal_spacing", "if (E < -126) E = -126;", ""),
+    ("bf16_state_not_rounded", "if (J->state_bf16)\n", "if (0)\n"),
+    ("bf16_rounds_before_readout", "/* \"O projection\" without the W_o / W_g matmuls: o_pre = S^T q. */",
+     "if (J->state_bf16) for (size_t i = 0; i < (size_t)d * d; ++i)\n"
+     "            S[i] = kda_oracle_bf16_value(kda_oracle_bf16_round(S[i]));"),
 ]
 
 
