@@ -204,7 +204,7 @@ class Ours:
         self.torch.sum(self.flush_r, 0, out=self.sink)
 
     # ---------------------------------------------------------------- decode
-    def decode(self, wl_name, flush, graph=False, e2e=True):
+    def decode(self, wl_name, flush, graph=False, e2e=True, state_bf16=False):
         """Decode calls of one workload, one launch per call, device-timed.
 
         flush: write and read 256 MiB between timed calls (for workloads whose
@@ -214,22 +214,30 @@ class Ours:
         also time the workload's calls captured once as a CUDA graph and
         replayed (per-call time = replay time / calls).  e2e: the same calls
         through the C ABI with the inputs copied in from pinned host memory
-        and o copied out, inside the timed region.
+        and o copied out, inside the timed region.  state_bf16: the state is
+        kept as bf16 (kda_decode_step_bf16state; a workload whose initial
+        state is zero, so that its bf16 form needs no conversion).
         """
         torch, kda, synth = self.torch, self.kda, self.synth
         wl = synth.WORKLOADS[wl_name]
         p = synth.make_params(wl, self.dev)
         st = synth.make_state(wl, self.dev)
         S, cs = st["S"], st["conv_state"]
+        if state_bf16:
+            assert wl.s0_std == 0 and not graph and not e2e
+            S = torch.zeros(S.shape, dtype=torch.int16, device=self.dev)
+            del st
+        step_fn = kda.kda_decode_step_bf16state if state_bf16 else kda.kda_decode_step
+        state_bytes = STATE_BYTES // 2 if state_bf16 else STATE_BYTES
         B, H = wl.B, wl.H
         o = torch.empty((B, H, D), device=self.dev)
         ctx = kda.kda_create(H, p["conv_w"], p["dt_bias"], p["A_log"], p["gamma"])
         K, W = self.args.steps, self.args.warmup
 
         def run(tk, t, out=o, stream=None):
-            kda.kda_decode_step(ctx, B, tk["q"][t], tk["k"][t], tk["v"][t], tk["z"][t],
-                                tk["beta_logit"][t], tk["gate_logit"][t], cs, S, out, None,
-                                self.stream if stream is None else stream)
+            step_fn(ctx, B, tk["q"][t], tk["k"][t], tk["v"][t], tk["z"][t],
+                    tk["beta_logit"][t], tk["gate_logit"][t], cs, S, out, None,
+                    self.stream if stream is None else stream)
 
         if wl.warmup_tokens:
             warm = synth.make_tokens(wl, self.dev, T=wl.warmup_tokens, warm=True)
@@ -360,10 +368,11 @@ class Ours:
         kda.kda_destroy(ctx)
 
         units = B * H                                   # (sequence, head) pairs per call
-        alg_bytes = units * (STATE_BYTES + 5 * D * 4 + 4 + D * 4 + 2 * 9 * D * 4) + H * 7680
+        alg_bytes = units * (state_bytes + 5 * D * 4 + 4 + D * 4 + 2 * 9 * D * 4) + H * 7680
         res = {
             "wl": wl, "ms": ms, "times": times, "launches": launches, "wall": t_wall,
-            "state_gbs": self.world * units * STATE_BYTES / (ms * 1e-3) / 1e9,
+            "state_elem_bytes": 2 if state_bf16 else 4,
+            "state_gbs": self.world * units * state_bytes / (ms * 1e-3) / 1e9,
             "alg_gbs": alg_bytes / (ms * 1e-3) / 1e9, "alg_bytes": alg_bytes,
             "ms_graph": ms_graph, "graph_launches": graph_launches,
         }
@@ -755,12 +764,12 @@ def run_reference(args, world, rank):
 
 # ----------------------------------------------------------------------------- main
 
-def decode_block(res, peaks, md_name, sha, flush_note):
+def decode_block(res, peaks, md_name, sha, flush_note, kernel="kda_decode_kernel"):
     wl = res["wl"]
     hb = peaks["hbm_gbs"]
     out = {
         "workload": wl.name, "B": wl.B, "H": wl.H, "d": D, "calls_cycled": wl.T,
-        "state_MiB": wl.B * wl.H * D * D * 4 / 2**20, "l2": flush_note,
+        "state_MiB": wl.B * wl.H * D * D * res["state_elem_bytes"] / 2**20, "l2": flush_note,
         "initial_state": f"after {wl.warmup_tokens} warm-up tokens" if wl.warmup_tokens else
                          "N(0, 0.01) state, N(0, 1) window",
         "ms_per_call": round(res["ms"], 5), "state_gbs": round(res["state_gbs"], 1),
@@ -768,7 +777,7 @@ def decode_block(res, peaks, md_name, sha, flush_note):
         "roofline": {"bound": "hbm", "achieved": round(res["alg_gbs"], 1), "peak": hb,
                      "unit": "GB/s", "frac": round(res["alg_gbs"] / hb, 4),
                      "traffic": profile_traffic(md_name, sha),
-                     "kernel": "kda_decode_kernel", "peak_src": peaks["src"] + " hbm_gbs",
+                     "kernel": kernel, "peak_src": peaks["src"] + " hbm_gbs",
                      "alg_bytes_per_launch": res["alg_bytes"]},
     }
     if res.get("ms_graph") is not None:
@@ -827,6 +836,8 @@ def main():
                     help="profiling only: time this prefill workload alone")
     ap.add_argument("--decode-workload", default=None,
                     help="profiling only: time this decode workload alone (no e2e, no graph)")
+    ap.add_argument("--bf16-state", action="store_true",
+                    help="profiling only: with --decode-workload, the bf16-state decode")
     ap.add_argument("--lowrank-only", action="store_true",
                     help="profiling only: time the low-rank front-end decode line alone")
     ap.add_argument("--proj-only", default=None,
@@ -855,8 +866,9 @@ def main():
             r = ours.prefill(args.prefill_workload, e2e=False)
             out.update(prefill_workload=args.prefill_workload, prefill_ms=round(r["ms"], 4))
         if args.decode_workload:
-            r = ours.decode(args.decode_workload, flush=False, e2e=False)
-            out.update(decode_workload=args.decode_workload, decode_ms=round(r["ms"], 5))
+            r = ours.decode(args.decode_workload, flush=False, e2e=False, state_bf16=args.bf16_state)
+            out.update(decode_workload=args.decode_workload, decode_ms=round(r["ms"], 5),
+                       bf16_state=args.bf16_state)
         if rank == 0:
             print(json.dumps(out), flush=True)
         return
@@ -865,6 +877,7 @@ def main():
     clocks.start()
     head = None if args.no_decode else ours.decode(HEADLINE_WL, flush=False, graph=True)
     dec = None if args.no_decode else ours.decode(DECODE_WL, flush=True)
+    d16 = None if args.no_decode else ours.decode(HEADLINE_WL, flush=False, e2e=False, state_bf16=True)
     dlr = None if args.no_decode else ours.decode_lowrank(DECODE_WL)
     psteps = max(3, min(args.steps, args.prefill_steps))
     pre = None if args.no_prefill else ours.prefill(PREFILL_WL)
@@ -913,6 +926,13 @@ def main():
         line["decode_b64_h32"] = decode_block(
             dec, peaks, "decode_b64_h32_kda_decode_kernel.md", dsha,
             "state 128 MiB < L2: flushed between timed calls (256 MiB write + 256 MiB read)")
+    if d16 is not None:
+        blk = decode_block(d16, peaks, "decode_b256_h64_bf16state_kda_decode_kernel.md", dsha,
+                           "state 512 MiB > L2, calls back to back",
+                           kernel="kda_decode_kernel<bf16 state>")
+        blk["dtype"] = "bf16 state, f32 compute and I/O"
+        blk["state_bytes_per_head_step"] = STATE_BYTES // 2
+        line["decode_bf16state"] = blk
     if dlr is not None:
         w = dlr["wl"]
         fe_gbs = dlr["fe_bytes"] / (dlr["ms_frontend"] * 1e-3) / 1e9

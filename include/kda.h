@@ -140,6 +140,29 @@ KDA_API kda_status kda_decode_step(kda_ctx *ctx, int B,
                            float *o, float *o_pre, void *stream);
 
 /*
+ * kda_decode_step with the state stored as bfloat16: the same token for B
+ * sequences, reading S as bf16, running the token in fp32 (the read-out o /
+ * o_pre uses the new state as computed) and storing the new state rounded to
+ * nearest-even bf16.  Half the state bytes each way, so about half the time
+ * of kda_decode_step when the state dominates, and half the memory for the
+ * state of every layer kept resident (the model-lifetime state of the
+ * "Zero-copy state persistence" and "Wrap-once buffer cache" notes of
+ * "Metal (Apple GPU) backend for Kimi K3"; the pages give no state
+ * precision, so bf16 storage is this library's variant).  The rounding is
+ * an error of up to 2^-9 relative per element per token on top of
+ * kda_decode_step's arithmetic.
+ *   S            [B][H][d][d] bf16 (raw bit patterns), row = key channel (in/out)
+ * Every other argument, the alignment rules, B == 0 and the give-up
+ * behaviour are those of kda_decode_step.
+ */
+KDA_API kda_status kda_decode_step_bf16state(kda_ctx *ctx, int B,
+                           const float *q, const float *k, const float *v,
+                           const float *z, const float *beta_logit,
+                           const float *gate_logit,
+                           float *conv_state, uint16_t *S,
+                           float *o, float *o_pre, void *stream);
+
+/*
  * Bytes of device workspace kda_prefill needs for B sequences of T tokens
  * (0 when none is needed; the current kernels need none, callers should
  * still ask).

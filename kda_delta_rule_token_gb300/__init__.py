@@ -15,7 +15,7 @@ from . import build as _build_mod
 
 __all__ = [
     "KDAError", "load", "kda_create", "kda_destroy", "kda_strerror", "kda_last_error_detail",
-    "kda_decode_step", "kda_prefill", "kda_prefill_varlen", "kda_prefill_workspace_bytes", "kda_sync_status",
+    "kda_decode_step", "kda_decode_step_bf16state", "kda_prefill", "kda_prefill_varlen", "kda_prefill_workspace_bytes", "kda_sync_status",
     "kda_launch_count", "kda_bind_lowrank", "kda_lowrank", "kda_lowrank_workspace_bytes",
     "kda_decode_step_lowrank", "kda_decode_lowrank_workspace_bytes", "kda_lowrank_noalloc",
     "LOWRANK_NOALLOC_SCRATCH_BYTES", "kda_bind_projections", "kda_project_qkvg", "kda_project_o",
@@ -75,6 +75,8 @@ def load(path: str | None = None):
     lib.kda_last_error_detail.restype = ctypes.c_char_p
     lib.kda_decode_step.argtypes = [vp, i32] + [vp] * 11
     lib.kda_decode_step.restype = i32
+    lib.kda_decode_step_bf16state.argtypes = [vp, i32] + [vp] * 11
+    lib.kda_decode_step_bf16state.restype = i32
     lib.kda_prefill_workspace_bytes.argtypes = [vp, i32, i32]
     lib.kda_prefill_workspace_bytes.restype = sz
     lib.kda_prefill.argtypes = [vp, i32, i32] + [vp] * 10 + [sz, vp]
@@ -166,6 +168,14 @@ def kda_decode_step(ctx, B, q, k, v, z, beta_logit, gate_logit, conv_state, S, o
     _check(load().kda_decode_step(ctx, int(B), _p(q), _p(k), _p(v), _p(z), _p(beta_logit),
                                   _p(gate_logit), _p(conv_state), _p(S), _p(o), _p(o_pre),
                                   _stream(stream)), "kda_decode_step")
+
+
+def kda_decode_step_bf16state(ctx, B, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
+                              o_pre=None, stream=None) -> None:
+    """kda_decode_step with S held as bf16 (a 16-bit tensor of raw patterns)."""
+    _check(load().kda_decode_step_bf16state(ctx, int(B), _p(q), _p(k), _p(v), _p(z), _p(beta_logit),
+                                            _p(gate_logit), _p(conv_state), _p(S), _p(o), _p(o_pre),
+                                            _stream(stream)), "kda_decode_step_bf16state")
 
 
 def kda_prefill_workspace_bytes(ctx, B, T) -> int:

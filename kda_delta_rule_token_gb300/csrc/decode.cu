@@ -6,7 +6,8 @@
 // "Fused KDA token" note of "Metal (Apple GPU) backend for Kimi K3" fuses
 // them (one submission per token), laid out for GB300's HBM3e:
 //
-//  * one CTA of 256 threads per (sequence, head), three CTAs resident per SM;
+//  * one CTA of 256 threads per (sequence, head), three CTAs resident per SM
+//    (five for the bf16 state);
 //  * the 64 KiB fp32 state moves as ONE bulk TMA copy each way
 //    (cp.async.bulk global -> shared on an mbarrier, shared -> global as a
 //    bulk group), so a whole state is in flight per CTA with one instruction
@@ -20,6 +21,12 @@
 //    in-thread adds plus one 8-way shared-memory reduction;
 //  * o_pre = S_new^T q = p + (q^.k^) delta with delta = beta (v - u): the
 //    read-out needs no extra pass over the state.
+//
+// The same kernel, instantiated for a bfloat16 state, keeps the state as
+// bf16 in memory (32 KiB per head, half the bytes each way): it is widened
+// to fp32 as pass 1 and pass 2 read it, the token runs in fp32 as above (the
+// read-out uses the new state as computed), and pass 2 rounds the new state
+// to nearest-even bf16 as it stores it.
 #include <atomic>
 
 #include "kda_internal.cuh"
@@ -31,8 +38,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerWarp = kHeadDim / kWarps;           // 16
-constexpr int kStateBytes = kHeadDim * kHeadDim * 4;      // 65536
-constexpr int kDynSmem = kStateBytes;
+template <bool BF16S>
+constexpr int kStateBytes = kHeadDim * kHeadDim * (BF16S ? 2 : 4);   // 32768 or 65536
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -47,10 +54,45 @@ __device__ __forceinline__ float softplusf_(float x) {
     return x > 0.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
 }
 
-__global__ void __launch_bounds__(kThreads, 3)
+// Four consecutive state elements of row-major row `i`, columns [4 l, 4 l + 4).
+template <bool BF16S>
+__device__ __forceinline__ float4 load4(const uint8_t* sS, int i, int l) {
+    if constexpr (BF16S) {
+        const uint2 w = reinterpret_cast<const uint2*>(sS + i * kHeadDim * 2)[l];
+        return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+    } else {
+        return reinterpret_cast<const float4*>(sS + i * kHeadDim * 4)[l];
+    }
+}
+
+// bf16 pair {lo, hi} rounded to nearest even (lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <bool BF16S>
+__device__ __forceinline__ void store4(uint8_t* sS, int i, int l, float4 t) {
+    if constexpr (BF16S) {
+        reinterpret_cast<uint2*>(sS + i * kHeadDim * 2)[l] = make_uint2(pack_bf16x2(t.x, t.y), pack_bf16x2(t.z, t.w));
+    } else {
+        reinterpret_cast<float4*>(sS + i * kHeadDim * 4)[l] = t;
+    }
+}
+
+// Resident CTAs per SM: 3 for the fp32 state (3 x 75 KiB of shared memory);
+// 5 for the bf16 state (43 KiB each), which keeps as many state bytes in
+// flight per SM as the fp32 kernel does with 3 (measured on the 256 x 64
+// workload: 0.274 ms per call at 3, 0.218 at 4, 0.207 at 5; at 5 the 48
+// registers leave an 8-byte spill).
+template <bool BF16S>
+__global__ void __launch_bounds__(kThreads, BF16S ? 5 : 3)
 kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     constexpr int D = kHeadDim;
-    extern __shared__ __align__(128) float sS[];          // the 128 x 128 state
+    constexpr int kBytes = kStateBytes<BF16S>;
+    extern __shared__ __align__(128) uint8_t sS[];        // the 128 x 128 state
     __shared__ float s_q[D], s_k[D], s_v[D], s_a[D];
     __shared__ __align__(16) float s_red_u[kWarps][D];
     __shared__ __align__(16) float s_red_p[kWarps][D];
@@ -65,7 +107,8 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    float* Sg = io.S + (size_t)bh * D * D;
+    uint8_t* Sg = BF16S ? reinterpret_cast<uint8_t*>(io.S16 + (size_t)bh * D * D)
+                        : reinterpret_cast<uint8_t*>(io.S + (size_t)bh * D * D);
 
     // 1. One bulk copy brings the whole state in.
     if (tid == 0) {
@@ -74,8 +117,8 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     }
     __syncthreads();
     if (tid == 0) {
-        ptx::mbar_arrive_expect_tx(&s_bar, kStateBytes);
-        ptx::bulk_g2s(sS, Sg, kStateBytes, &s_bar);
+        ptx::mbar_arrive_expect_tx(&s_bar, kBytes);
+        ptx::bulk_g2s(sS, Sg, kBytes, &s_bar);
     }
 
     // 2. While it is in flight: conv4 + SiLU on the 3*d channels of q, k, v
@@ -144,7 +187,7 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     for (int r = 0; r < kRowsPerWarp; ++r) {
         const int i = row0 + r;
         const float ai = s_a[i], ki = s_k[i] * ai, qi = s_q[i] * ai;
-        const float4 x = reinterpret_cast<const float4*>(sS + i * D)[lane];
+        const float4 x = load4<BF16S>(sS, i, lane);
         u.x = fmaf(ki, x.x, u.x); u.y = fmaf(ki, x.y, u.y);
         u.z = fmaf(ki, x.z, u.z); u.w = fmaf(ki, x.w, u.w);
         pr.x = fmaf(qi, x.x, pr.x); pr.y = fmaf(qi, x.y, pr.y);
@@ -195,15 +238,15 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
     for (int r = 0; r < kRowsPerWarp; ++r) {
         const int i = row0 + r;
         const float ai = s_a[i], ki = s_k[i];
-        float4 t = reinterpret_cast<const float4*>(sS + i * D)[lane];
+        float4 t = load4<BF16S>(sS, i, lane);
         t.x = fmaf(ki, dl.x, t.x * ai); t.y = fmaf(ki, dl.y, t.y * ai);
         t.z = fmaf(ki, dl.z, t.z * ai); t.w = fmaf(ki, dl.w, t.w * ai);
-        reinterpret_cast<float4*>(sS + i * D)[lane] = t;
+        store4<BF16S>(sS, i, lane, t);
     }
     ptx::fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
-        ptx::bulk_s2g(Sg, sS, kStateBytes);
+        ptx::bulk_s2g(Sg, sS, kBytes);
         ptx::bulk_commit();
     }
 
@@ -223,6 +266,14 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
 // idempotent, so two host threads setting them at once is harmless).
 std::atomic<bool> g_attr_done[64];
 
+template <bool BF16S>
+cudaError_t set_attrs() {
+    cudaError_t e = cudaFuncSetAttribute(kda_decode_kernel<BF16S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kStateBytes<BF16S>);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kda_decode_kernel<BF16S>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const DeviceInfo& dev,
@@ -230,15 +281,16 @@ cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const Device
     const long long grid = (long long)io.B * p.H;
     if (grid <= 0) return cudaSuccess;
     if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(kda_decode_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kDynSmem);
+        cudaError_t e = set_attrs<false>();
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kda_decode_kernel,
-                                 cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        e = set_attrs<true>();
         if (e != cudaSuccess) return e;
         if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device].store(true, std::memory_order_release);
     }
-    kda_decode_kernel<<<(unsigned)grid, kThreads, kDynSmem, stream>>>(p, io, err_word);
+    if (io.S16)
+        kda_decode_kernel<true><<<(unsigned)grid, kThreads, kStateBytes<true>, stream>>>(p, io, err_word);
+    else
+        kda_decode_kernel<false><<<(unsigned)grid, kThreads, kStateBytes<false>, stream>>>(p, io, err_word);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -210,6 +210,28 @@ kda_status kda_decode_step(kda_ctx* ctx, int B, const float* q, const float* k, 
     return KDA_OK;
 }
 
+kda_status kda_decode_step_bf16state(kda_ctx* ctx, int B, const float* q, const float* k, const float* v,
+                                     const float* z, const float* beta_logit, const float* gate_logit,
+                                     float* conv_state, uint16_t* S, float* o, float* o_pre, void* stream) {
+    if (!ctx || B < 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !z || !beta_logit || !gate_logit || !conv_state || !S || !o)
+        return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, z, gate_logit, conv_state, S, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
+    if (!aligned4(beta_logit)) return KDA_ERR_ALIGNMENT;
+    if (o_pre && !aligned16(o_pre)) return KDA_ERR_ALIGNMENT;
+    if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
+    kda::DecodeIO io{B, q, k, v, z, beta_logit, gate_logit, conv_state, nullptr, o, o_pre, S};
+    cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectDecode, [&] {
+        return kda::launch_decode(ctx->params, io, ctx->dev, ctx->err_word, static_cast<cudaStream_t>(stream));
+    });
+    if (e != cudaSuccess) { kda::set_launch_detail(ctx, kda::kInjectDecode, "decode launch", e); return KDA_ERR_CUDA; }
+    return KDA_OK;
+}
+
 size_t kda_prefill_workspace_bytes(const kda_ctx* ctx, int B, int T) {
     if (!ctx || B <= 0 || T <= 0) return 0;
     return kda::prefill_workspace_bytes(ctx->params.H, B, T, ctx->dev);

@@ -37,6 +37,7 @@ struct DecodeIO {
     float* S;
     float* o;
     float* o_pre;  // may be null
+    uint16_t* S16; // bf16 state instead of S (then S is null), or null
 };
 
 struct PrefillIO {

@@ -33,7 +33,7 @@ def test_header_declares_the_api():
     names = declared_functions()
     for n in ("kda_create", "kda_decode_step", "kda_prefill", "kda_prefill_varlen", "kda_destroy",
               "kda_strerror", "kda_prefill_workspace_bytes", "kda_sync_status", "kda_bind_lowrank",
-              "kda_lowrank", "kda_decode_step_lowrank"):
+              "kda_lowrank", "kda_decode_step_lowrank", "kda_decode_step_bf16state"):
         assert n in names
 
 
@@ -73,6 +73,7 @@ def test_host_side_rejections(lib):
     assert out.value is None
     # calls without a context
     assert lib.kda_decode_step(null, 1, *([16] * 10), null) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_step_bf16state(null, 1, *([16] * 10), null) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_prefill(null, 1, 1, *([16] * 10), 0, null) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_prefill_varlen(null, 1, 16, 1, *([16] * 9), null) == kda.KDA_ERR_INVALID_ARG
     assert lib.kda_sync_status(null, null) == kda.KDA_ERR_INVALID_ARG
