@@ -356,7 +356,11 @@ KDA_API size_t kda_project_o_workspace_bytes(const kda_ctx *ctx, int N);
  *   o            [N][H][d] fp32 (in): the o of kda_decode_step / kda_prefill
  *   y            [N][hidden] fp32 (out)
  *   workspace    at least kda_project_o_workspace_bytes(ctx, N) bytes
- * All 16-byte aligned.  N == 0 is a no-op.
+ * All 16-byte aligned.  N == 0 is a no-op.  When the output tiles would leave
+ * most SMs idle (a few tokens), the two halves of W_o's columns run on
+ * separate CTAs and are added into y (which the call zeroes first); two
+ * addends onto zero give the same sum in either order, so y does not
+ * depend on scheduling (sums below 2^-126 in magnitude become zero).
  */
 KDA_API kda_status kda_project_o(kda_ctx *ctx, int N, const float *o, float *y, void *workspace,
                                  size_t workspace_bytes, void *stream);

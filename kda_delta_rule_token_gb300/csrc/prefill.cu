@@ -457,6 +457,17 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         tc::st32(ta, v);
     };
 
+    // DT -> tf32 in place (A operand of MMA2).
+    auto dt_to_tf32 = [&]() {
+        uint32_t v[16];
+        const uint32_t ta = tc::taddr(tm, warp, TM_DT + grp * 16);
+        tc::ld16(ta, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = tc::f2tf32(__uint_as_float(v[i]));
+        tc::st16(ta, v);
+    };
+
     for (int ci = role; ci < nchunks; ci += kStep) {
         const int t0 = ci * C;
         const int n = min(C, T - t0);
@@ -848,6 +859,10 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
         }
         if constexpr (RELAY) {
+            // MMA_T's result to tf32 while the other CTA's chain runs.
+            wtT.wait();   // MMA_T
+            if (ci + kStep < nchunks) stage_v(ci + kStep);     // the Minv^T region is free now
+            dt_to_tf32();
             // The state after chunk ci - 1 (the other CTA's) arrives; chunk 0
             // starts from the initial state in the TMEM master.
             if (ci > 0) wrx.wait();
@@ -898,19 +913,11 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             }
             tc::st32(ta, v);
         }
-        publish();
-        wtT.wait();   // MMA_T
-        if (ci + kStep < nchunks) stage_v(ci + kStep);     // the Minv^T region is free now
-
-        // ---- DT -> tf32 in place (A operand of MMA2).
-        {
-            uint32_t v[16];
-            const uint32_t ta = tc::taddr(tm, warp, TM_DT + grp * 16);
-            tc::ld16(ta, v);
-            tc::wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = tc::f2tf32(__uint_as_float(v[i]));
-            tc::st16(ta, v);
+        if constexpr (!RELAY) {
+            publish();
+            wtT.wait();   // MMA_T
+            if (ci + kStep < nchunks) stage_v(ci + kStep);     // the Minv^T region is free now
+            dt_to_tf32();
         }
         publish();
 

@@ -25,7 +25,12 @@
 //    as fp32): per token, a warp writes 32 consecutive features.
 //
 // The output projection takes o in fp32; a conversion kernel writes its bf16
-// copy into the caller's workspace first (round to nearest even).
+// copy into the caller's workspace first (round to nearest even).  When its
+// output tiles would leave more than half of the SMs idle (a few tokens: the
+// call then streams W_o), K is split in two halves on separate CTAs, each
+// adding its fp32 partial tile into y (zeroed by the conversion kernel) with
+// red.global.add: with exactly two addends onto zero, (0 + a) + b and
+// (0 + b) + a are the same float, so y does not depend on their order.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -57,6 +62,7 @@ struct ProjArgs {
     int M, N, K;            // C[N][M] = X[N][K] W[M][K]^T
     int Nt;                 // token tile: 32, 64, 128 or 256
     int mtiles, ntiles;
+    int ksplit;             // K halves per tile: 1, or 2 (fp32 output added into, zero on entry)
     int nsegs;              // outputs, each `len` consecutive features of M
     Seg seg[kMaxSegs];
 };
@@ -68,6 +74,10 @@ struct ProjMaps {
 
 __host__ __device__ constexpr uint32_t stage_bytes(int Nt) { return kATile + (uint32_t)Nt * 128; }
 constexpr uint32_t proj_smem_bytes(int Nt) { return kStages * stage_bytes(Nt) + 1024; }
+
+__device__ __forceinline__ void red_add(float* p, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
 
 __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, int* dead, int* err) {
     if (*(volatile int*)dead) return false;
@@ -103,8 +113,14 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
     int* s_issued = s_dead + 1;
 
-    const int tiles = g.mtiles * g.ntiles;
+    // Work unit u = (tile u / ksplit, K range u % ksplit): K slices [k0, k1).
+    const int units = g.mtiles * g.ntiles * g.ksplit;
     const int nk = (g.K + kKSlice - 1) / kKSlice;
+    auto krange = [&](int u, int& k0, int& k1) {
+        const int ks = u % g.ksplit;
+        k0 = ks * nk / g.ksplit;
+        k1 = (ks + 1) * nk / g.ksplit;
+    };
     const uint32_t ncols = 2u * (uint32_t)g.Nt;   // two accumulators
 
     if (tid == 0) {
@@ -130,10 +146,11 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
     if (tid == 0) {
         // TMA producer: slices of every tile of this CTA, in order.
         int it = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-            int mt, nt;
-            raster(g, t, mt, nt);
-            for (int i = 0; i < nk; ++i, ++it) {
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            int mt, nt, k0, k1;
+            raster(g, u / g.ksplit, mt, nt);
+            krange(u, k0, k1);
+            for (int i = k0; i < k1; ++i, ++it) {
                 const int s = it % kStages;
                 if (it >= kStages && !pwait(&empty[s], (uint32_t)((it / kStages - 1) & 1), s_dead, err)) goto done_p;
                 uint8_t* st = sm + s * sbytes;
@@ -149,13 +166,15 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
         // once the epilogue has read that accumulator's previous tile.
         const uint32_t id = tc::idesc_bf16(128, g.Nt);
         int it = 0, j = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
             const int b = j & 1;
             if (j >= 2 && !pwait(&acce[b], (uint32_t)(((j >> 1) - 1) & 1), s_dead, err)) break;
             tc::fence_after();
             const uint32_t d = tm + (uint32_t)(b * g.Nt);
+            int k0, k1;
+            krange(u, k0, k1);
             bool ok = true;
-            for (int i = 0; i < nk; ++i, ++it) {
+            for (int i = k0; i < k1; ++i, ++it) {
                 const int s = it % kStages;
                 if (!pwait(&full[s], (uint32_t)((it / kStages) & 1), s_dead, err)) { ok = false; break; }
                 tc::fence_after();
@@ -163,7 +182,7 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
 #pragma unroll
                 for (int kin = 0; kin < 4; ++kin)
                     tc::mma_ss_bf16(d, tc::desc_sw128(a + kin * 32), tc::desc_sw128(bb + kin * 32), id,
-                                    (i | kin) != 0 ? 1u : 0u);
+                                    (i > k0 || kin > 0) ? 1u : 0u);
                 tc::commit(&empty[s]);
             }
             tc::commit(&accf[b]);
@@ -174,12 +193,33 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
         // Epilogue: TMEM lane r = output feature mt * 128 + r, column = token.
         const int r = 32 * (warp & 3) + lane;
         int j = 0;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
             const int b = j & 1;
             if (!pwait(&accf[b], (uint32_t)((j >> 1) & 1), s_dead, err)) break;
             tc::fence_after();
+            const int t = u / g.ksplit;
             int mt, nt;
             raster(g, t, mt, nt);
+            const int n0 = nt * g.Nt;
+            if (g.ksplit > 1) {
+                // Split K: this half's fp32 partial tile added into the
+                // (single, fp32) output, token-major (a warp adds 32
+                // consecutive features per token).
+                float* out = static_cast<float*>(g.seg[0].ptr) + mt * 128 + r;
+                for (int c0 = 0; c0 < g.Nt; c0 += 32) {
+                    uint32_t v[32];
+                    tc::ld32(tc::taddr(tm, warp, b * g.Nt + c0), v);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        const int n = n0 + c0 + q;
+                        if (n < g.N) red_add(out + (size_t)n * g.M, __uint_as_float(v[q]));
+                    }
+                }
+                tc::fence_before();
+                ptx::mbar_arrive(&acce[b]);
+                continue;
+            }
             int off = mt * 128 + r;   // feature index, then the offset inside its output
             Seg sg = g.seg[0];
 #pragma unroll
@@ -188,7 +228,6 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
                     off -= sg.len;
                     sg = g.seg[i];
                 }
-            const int n0 = nt * g.Nt;
             for (int c0 = 0; c0 < g.Nt; c0 += 32) {
                 uint32_t v[32];
                 tc::ld32(tc::taddr(tm, warp, b * g.Nt + c0), v);
@@ -233,7 +272,11 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
 }
 
 // o (fp32) -> bf16, round to nearest even; n is a multiple of 4.
-__global__ void kda_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out, size_t n4) {
+// With split K it also zeroes y (nz4 float4s), which the GEMM then adds into.
+__global__ void kda_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out, size_t n4,
+                                   float4* __restrict__ zero, size_t nz4) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nz4; i += (size_t)gridDim.x * blockDim.x)
+        zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
         const float4 a = in[i];
         const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
@@ -276,8 +319,17 @@ int token_tile(int N) {
     return t;
 }
 
+// K halves per output tile: 2 when the tiles would leave more than half of
+// the SMs idle and K spans at least 16 slices of 64, else 1.
+int ksplit_for(int M, int N, int K, int sm_count) {
+    const int Nt = token_tile(N);
+    const long long tiles = (long long)(M / 128) * ((N + Nt - 1) / Nt);
+    const int nk = (K + kKSlice - 1) / kKSlice;
+    return (tiles > 0 && 2 * tiles <= sm_count && nk >= 16) ? 2 : 1;
+}
+
 cudaError_t run_proj(const CUtensorMap& wmap, int M, const void* x, int N, int K, const Seg* segs, int nsegs,
-                     const DeviceInfo& dev, int* err_word, cudaStream_t stream) {
+                     int ksplit, const DeviceInfo& dev, int* err_word, cudaStream_t stream) {
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (!g_attr_done[dev.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kda_proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -292,13 +344,14 @@ cudaError_t run_proj(const CUtensorMap& wmap, int M, const void* x, int N, int K
     g.Nt = token_tile(N);
     g.mtiles = M / 128;
     g.ntiles = (N + g.Nt - 1) / g.Nt;
+    g.ksplit = ksplit;
     g.nsegs = nsegs;
     for (int i = 0; i < nsegs; ++i) g.seg[i] = segs[i];
     ProjMaps maps{};
     maps.w = wmap;
     if (!make_map_bf16(&maps.x, x, K, N, g.Nt)) return cudaErrorInvalidValue;
-    const int tiles = g.mtiles * g.ntiles;
-    const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+    const int units = g.mtiles * g.ntiles * g.ksplit;
+    const int grid = units < dev.sm_count ? units : dev.sm_count;
     kda_proj_gemm_kernel<<<grid, kThreads, proj_smem_bytes(g.Nt), stream>>>(g, err_word, maps);
     count_launches(1);
     return cudaGetLastError();
@@ -321,7 +374,7 @@ cudaError_t launch_project_qkvg(const LayerParams& p, const Projections& pr, int
     const int HD = p.H * kHeadDim;
     const int b = qkv_f32 ? 0 : 1;
     const Seg segs[4] = {{q, HD, b}, {k, HD, b}, {v, HD, b}, {gate_logit, HD, 0}};
-    return run_proj(pr.map_qkvg, 4 * HD, x, N, pr.hidden, segs, 4, dev, err_word, stream);
+    return run_proj(pr.map_qkvg, 4 * HD, x, N, pr.hidden, segs, 4, 1, dev, err_word, stream);
 }
 
 size_t project_o_workspace_bytes(const LayerParams& p, int N) {
@@ -333,15 +386,18 @@ cudaError_t launch_project_o(const LayerParams& p, const Projections& pr, int N,
     if (N <= 0) return cudaSuccess;
     if (!pr.maps_ready) return cudaErrorInvalidValue;
     const int HD = p.H * kHeadDim;
+    const int ksplit = ksplit_for(pr.hidden, N, HD, dev.sm_count);
     const size_t n4 = (size_t)N * HD / 4;
-    const size_t want = (n4 + 255) / 256, cap = (size_t)dev.sm_count * 16;
+    const size_t nz4 = ksplit > 1 ? (size_t)N * pr.hidden / 4 : 0;
+    const size_t work = n4 > nz4 ? n4 : nz4;
+    const size_t want = (work + 255) / 256, cap = (size_t)dev.sm_count * 16;
     kda_to_bf16_kernel<<<(unsigned)(want < cap ? want : cap), 256, 0, stream>>>(
-        reinterpret_cast<const float4*>(o), static_cast<uint2*>(workspace), n4);
+        reinterpret_cast<const float4*>(o), static_cast<uint2*>(workspace), n4, reinterpret_cast<float4*>(y), nz4);
     count_launches(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const Seg segs[1] = {{y, pr.hidden, 0}};
-    return run_proj(pr.map_o, pr.hidden, workspace, N, HD, segs, 1, dev, err_word, stream);
+    return run_proj(pr.map_o, pr.hidden, workspace, N, HD, segs, 1, ksplit, dev, err_word, stream);
 }
 
 }  // namespace kda

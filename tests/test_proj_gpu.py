@@ -84,8 +84,10 @@ def test_project_qkvg_matches_oracle(N, hidden, H, qkv_f32):
     print(f"\n  N={N} hidden={hidden} H={H} qkv_f32={qkv_f32}: gate {eg:.2e}")
 
 
-@pytest.mark.parametrize("N,hidden,H", [(5, 128, 2), (64, 7168, 32), (700, 256, 4)])
+@pytest.mark.parametrize("N,hidden,H", [(5, 128, 2), (64, 7168, 32), (700, 256, 4), (1, 7168, 32), (64, 1024, 64)])
 def test_project_o_matches_oracle(N, hidden, H):
+    """Includes calls that split K in two halves across CTAs (64 and 1 tokens
+    at hidden 7168: 56 output tiles; hidden 1024 at H = 64: 8 tiles)."""
     wl = _wl(N, H)
     pr = synth.make_projections(wl, DEV, hidden=hidden)
     HD = H * 128
@@ -127,3 +129,24 @@ def test_project_argument_errors():
         assert ei.value.status == kda.KDA_ERR_INVALID_ARG
     finally:
         kda.kda_destroy(ctx)
+
+
+def test_project_o_split_is_deterministic_and_overwrites_y():
+    """Split K (64 tokens, hidden 7168, H = 32: 56 output tiles, two K halves
+    added into y): y starts as NaN and is fully overwritten; two calls give
+    the same y bit for bit (two addends onto zero commute exactly)."""
+    N, hidden, H = 64, 7168, 32
+    wl = _wl(N, H)
+    pr = synth.make_projections(wl, DEV, hidden=hidden)
+    ctx = _ctx(wl, pr)
+    try:
+        ws = torch.full((kda.kda_project_o_workspace_bytes(ctx, N),), 0x7F, dtype=torch.uint8, device=DEV)
+        y1 = torch.full((N, hidden), float("nan"), device=DEV)
+        y2 = torch.full((N, hidden), float("nan"), device=DEV)
+        kda.kda_project_o(ctx, N, pr["o_in"], y1, ws)
+        kda.kda_project_o(ctx, N, pr["o_in"], y2, ws)
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+    finally:
+        kda.kda_destroy(ctx)
+    assert bool(torch.isfinite(y1).all())
+    assert torch.equal(y1, y2)
