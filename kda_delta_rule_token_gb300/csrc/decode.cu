@@ -121,6 +121,11 @@ kda_decode_kernel(const LayerParams p, const DecodeIO io, int* err) {
         ptx::bulk_g2s(sS, Sg, kBytes, &s_bar);
     }
 
+    // Launched after the low-rank front-end (programmatic dependent launch),
+    // the state load above is already in flight while the front-end
+    // finishes; z and beta_logit are its results, read below.
+    ptx::griddep_wait();
+
     // 2. While it is in flight: conv4 + SiLU on the 3*d channels of q, k, v
     //    and the per-channel decay a = exp(gk), gk = -exp(A_log) softplus(z +
     //    dt_bias).  The shifted window is held in registers and written back
@@ -277,7 +282,7 @@ cudaError_t set_attrs() {
 }  // namespace
 
 cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const DeviceInfo& dev,
-                          int* err_word, cudaStream_t stream) {
+                          int* err_word, cudaStream_t stream, bool pdl) {
     const long long grid = (long long)io.B * p.H;
     if (grid <= 0) return cudaSuccess;
     if (dev.device < 0 || dev.device >= 64 || !g_attr_done[dev.device].load(std::memory_order_acquire)) {
@@ -287,12 +292,20 @@ cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const Device
         if (e != cudaSuccess) return e;
         if (dev.device >= 0 && dev.device < 64) g_attr_done[dev.device].store(true, std::memory_order_release);
     }
-    if (io.S16)
-        kda_decode_kernel<true><<<(unsigned)grid, kThreads, kStateBytes<true>, stream>>>(p, io, err_word);
-    else
-        kda_decode_kernel<false><<<(unsigned)grid, kThreads, kStateBytes<false>, stream>>>(p, io, err_word);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = io.S16 ? kStateBytes<true> : kStateBytes<false>;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = io.S16 ? cudaLaunchKernelEx(&cfg, kda_decode_kernel<true>, p, io, err_word)
+                                 : cudaLaunchKernelEx(&cfg, kda_decode_kernel<false>, p, io, err_word);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace kda

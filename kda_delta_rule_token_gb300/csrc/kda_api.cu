@@ -430,7 +430,7 @@ kda_status kda_decode_step_lowrank(kda_ctx* ctx, int B, const float* x, const fl
                                             ctx->err_word, st);
         if (r != cudaSuccess) return r;
         kda::DecodeIO io{B, q, k, v, z, bl, gate_logit, conv_state, S, o, o_pre};
-        return kda::launch_decode(ctx->params, io, ctx->dev, ctx->err_word, st);
+        return kda::launch_decode(ctx->params, io, ctx->dev, ctx->err_word, st, true);
     });
     if (e != cudaSuccess) {
         kda::set_launch_detail(ctx, kda::kInjectLowrank | kda::kInjectDecode, "decode_lowrank launch", e);

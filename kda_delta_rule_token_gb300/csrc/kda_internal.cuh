@@ -92,8 +92,11 @@ struct DeviceInfo {
 
 // Launchers (kernels live in decode.cu / prefill.cu).  They return the
 // cudaError_t of the launch.
+// pdl: the kernel may start while the kernel before it in the stream (the
+// low-rank front-end) finishes; it waits for that kernel before reading z and
+// beta_logit.
 cudaError_t launch_decode(const LayerParams& p, const DecodeIO& io, const DeviceInfo& dev,
-                          int* err_word, cudaStream_t stream);
+                          int* err_word, cudaStream_t stream, bool pdl = false);
 size_t prefill_workspace_bytes(int H, int B, int T, const DeviceInfo& dev);
 cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const DeviceInfo& dev,
                            int* err_word, cudaStream_t stream);

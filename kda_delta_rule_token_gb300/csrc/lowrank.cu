@@ -113,6 +113,9 @@ kda_lowrank_gemm_kernel(const GemmArgs g, int* err, const __grid_constant__ Gemm
     int* s_dead = reinterpret_cast<int*>(s_tmem + 1);
     int* s_issued = s_dead + 1;                                      // slices the producer issued
 
+    // The next kernel of the front-end (or the decode after it) may start its
+    // own set-up now; it waits for this one's results itself.
+    ptx::griddep_launch_dependents();
     const int mt = blockIdx.x, nt = blockIdx.y, ks = blockIdx.z;
     const bool second = mt >= g.tiles0;
     const int arow = (second ? mt - g.tiles0 : mt) * 128;    // first row of the tile in its matrix
@@ -142,7 +145,9 @@ kda_lowrank_gemm_kernel(const GemmArgs g, int* err, const __grid_constant__ Gemm
 
     if (tid == 0) {
         // TMA producer: slice i goes to stage i % S once the MMAs of slice
-        // i - S have released it.
+        // i - S have released it.  The B operand of GEMM C is the reduction's
+        // output: the kernel before must have completed.
+        ptx::griddep_wait();
         for (int i = 0; i < nk; ++i) {
             const int s = i % S;
             if (i >= S && !gwait(&empty[s], (uint32_t)((i / S - 1) & 1), s_dead, err)) break;
@@ -256,6 +261,8 @@ __global__ void __launch_bounds__(32 * kReduceWarps)
 kda_lowrank_reduce_kernel(const float* __restrict__ part, int splits, int N, int ldo, int M0, int M1,
                           int col1, float* __restrict__ u, float* __restrict__ beta_logit) {
     __shared__ float sp[kReduceWarps][32];
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // GEMM A's partial sums
     const size_t M = (size_t)(M0 + M1);
     const size_t total = (size_t)N * M;
     const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
@@ -358,16 +365,37 @@ size_t scratch_bytes(const Plan& pa, int N, int rank) {
     return align256((size_t)pa.splits * N * pa.ldo * 4) + align256((size_t)N * rank * 4);
 }
 
+// Launch attributes for a kernel that may start before the one ahead of it
+// in the stream has finished (programmatic dependent launch).
+cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr,
+                              bool pdl) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cfg;
+}
+
 cudaError_t run_gemm(const Plan& pl, const GemmMaps& maps, int N, int K, float* out, int* err_word,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, bool pdl) {
     GemmArgs g{pl.tiles0, N, K, pl.Nt, pl.kslice, ring_stages(pl.Nt), pl.ldo, out};
     const dim3 grid((unsigned)(pl.tiles0 + pl.tiles1), (unsigned)pl.ntiles, (unsigned)pl.splits);
-    kda_lowrank_gemm_kernel<<<grid, kThreads, gemm_smem_bytes(pl.Nt), stream>>>(g, err_word, maps);
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pdl_config(grid, dim3(kThreads), gemm_smem_bytes(pl.Nt), stream, attr, pdl);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kda_lowrank_gemm_kernel, g, err_word, maps);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // The three launches of one front-end call, with its scratch at `scratch`.
+// GEMM A starts after everything before it in the stream; the reduction and
+// GEMM C start early (programmatic dependent launch) and wait for their
+// inputs inside, and so may a kernel launched that way after GEMM C.
 cudaError_t run_frontend(const LayerParams& p, const LowRank& lr, const Plan& pa, int N, const float* x,
                          float* z, float* beta_logit, void* scratch, const DeviceInfo& dev, int* err_word,
                          cudaStream_t stream) {
@@ -387,21 +415,24 @@ cudaError_t run_frontend(const LayerParams& p, const LowRank& lr, const Plan& pa
     ma.a0 = lr.map_fa;
     ma.a1 = lr.map_bp;
     if (!make_map2d(&ma.b, x, lr.hidden, N, pa.Nt)) return cudaErrorInvalidValue;
-    cudaError_t e = run_gemm(pa, ma, N, lr.hidden, part, err_word, stream);
+    cudaError_t e = run_gemm(pa, ma, N, lr.hidden, part, err_word, stream, false);
     if (e != cudaSuccess) return e;
     // Reduce the splits.
     const size_t total = (size_t)N * (lr.rank + H);
-    kda_lowrank_reduce_kernel<<<(unsigned)((total + 31) / 32), 32 * kReduceWarps, 0, stream>>>(
-        part, pa.splits, N, pa.ldo, lr.rank, H, 128 * pa.tiles0, u, beta_logit);
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg =
+        pdl_config(dim3((unsigned)((total + 31) / 32)), dim3(32 * kReduceWarps), 0, stream, attr, true);
+    e = cudaLaunchKernelEx(&cfg, kda_lowrank_reduce_kernel, (const float*)part, pa.splits, N, pa.ldo, lr.rank, H,
+                           128 * pa.tiles0, u, beta_logit);
     count_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
     // GEMM C: z = W_fb u, one split (K = rank).
     const Plan pc = plan_gemm_c(p, lr, N, dev.sm_count);
     GemmMaps mc{};
     mc.a0 = lr.map_fb;
     mc.a1 = lr.map_fb;
     if (!make_map2d(&mc.b, u, lr.rank, N, pc.Nt)) return cudaErrorInvalidValue;
-    return run_gemm(pc, mc, N, lr.rank, z, err_word, stream);
+    return run_gemm(pc, mc, N, lr.rank, z, err_word, stream, true);
 }
 
 }  // namespace

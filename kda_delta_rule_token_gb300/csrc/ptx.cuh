@@ -83,6 +83,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* m, uint32_t parity, int* err
     return false;
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialisation attribute may start while the kernel before it in the
+// stream is still running, once every CTA of that kernel has executed
+// griddep_launch_dependents() (or exited); griddep_wait() returns once the
+// kernel before has completed and its memory operations are visible.  In a
+// kernel launched the ordinary way both are no-ops in effect (the kernel
+// before has already completed).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Thread-block clusters.  The address, in the cluster's shared window, of
 // the location at shared-memory address `saddr` of CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
