@@ -142,6 +142,9 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
     __syncthreads();
     tc::fence_after();
     const uint32_t tm = *s_tmem;
+    // Output projection (programmatic dependent launch): the conversion
+    // kernel before has written x and zeroed y once this returns.
+    ptx::griddep_wait();
 
     if (tid == 0) {
         // TMA producer: slices of every tile of this CTA, in order.
@@ -275,6 +278,7 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
 // With split K it also zeroes y (nz4 float4s), which the GEMM then adds into.
 __global__ void kda_to_bf16_kernel(const float4* __restrict__ in, uint2* __restrict__ out, size_t n4,
                                    float4* __restrict__ zero, size_t nz4) {
+    ptx::griddep_launch_dependents();   // the GEMM may set up meanwhile
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nz4; i += (size_t)gridDim.x * blockDim.x)
         zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
@@ -329,7 +333,7 @@ int ksplit_for(int M, int N, int K, int sm_count) {
 }
 
 cudaError_t run_proj(const CUtensorMap& wmap, int M, const void* x, int N, int K, const Seg* segs, int nsegs,
-                     int ksplit, const DeviceInfo& dev, int* err_word, cudaStream_t stream) {
+                     int ksplit, const DeviceInfo& dev, int* err_word, cudaStream_t stream, bool pdl) {
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (!g_attr_done[dev.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kda_proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -352,9 +356,19 @@ cudaError_t run_proj(const CUtensorMap& wmap, int M, const void* x, int N, int K
     if (!make_map_bf16(&maps.x, x, K, N, g.Nt)) return cudaErrorInvalidValue;
     const int units = g.mtiles * g.ntiles * g.ksplit;
     const int grid = units < dev.sm_count ? units : dev.sm_count;
-    kda_proj_gemm_kernel<<<grid, kThreads, proj_smem_bytes(g.Nt), stream>>>(g, err_word, maps);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = proj_smem_bytes(g.Nt);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kda_proj_gemm_kernel, g, err_word, maps);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -374,7 +388,7 @@ cudaError_t launch_project_qkvg(const LayerParams& p, const Projections& pr, int
     const int HD = p.H * kHeadDim;
     const int b = qkv_f32 ? 0 : 1;
     const Seg segs[4] = {{q, HD, b}, {k, HD, b}, {v, HD, b}, {gate_logit, HD, 0}};
-    return run_proj(pr.map_qkvg, 4 * HD, x, N, pr.hidden, segs, 4, 1, dev, err_word, stream);
+    return run_proj(pr.map_qkvg, 4 * HD, x, N, pr.hidden, segs, 4, 1, dev, err_word, stream, false);
 }
 
 size_t project_o_workspace_bytes(const LayerParams& p, int N) {
@@ -397,7 +411,7 @@ cudaError_t launch_project_o(const LayerParams& p, const Projections& pr, int N,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const Seg segs[1] = {{y, pr.hidden, 0}};
-    return run_proj(pr.map_o, pr.hidden, workspace, N, HD, segs, 1, ksplit, dev, err_word, stream);
+    return run_proj(pr.map_o, pr.hidden, workspace, N, HD, segs, 1, ksplit, dev, err_word, stream, true);
 }
 
 }  // namespace kda
