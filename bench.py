@@ -843,7 +843,7 @@ def main():
     ap.add_argument("--proj-only", default=None,
                     help="profiling only: time the projections on this workload's tokens alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-split", type=int, default=2,
+    ap.add_argument("--e2e-split", type=int, default=4,
                     help="groups of sequences the decode end-to-end step is pipelined over")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
