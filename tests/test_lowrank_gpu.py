@@ -163,6 +163,41 @@ def test_decode_lowrank_equals_frontend_then_decode():
     assert torch.equal(o, o2) and torch.equal(S, S2) and torch.equal(conv, c2)
 
 
+def test_decode_lowrank_graph_replay_equals_launches():
+    """kda_decode_step_lowrank launches its later kernels as programmatic
+    dependents (they start early and wait for their inputs); captured in a
+    CUDA graph and replayed, the calls give bit for bit what launching them
+    gives."""
+    wl = synth.shrink(synth.WORKLOADS["decode_b64_h32_x256"], B=16, H=4, T=4)
+    params, tokens = synth.make_params(wl, DEV), synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    lr = synth.make_lowrank(wl, DEV, hidden=512, rank=64)
+    S, conv = st["S"], st["conv_state"]
+    S2, c2 = S.clone(), conv.clone()
+    o = _decode_lowrank(wl, params, lr, tokens, S, conv)
+    B, H = wl.B, wl.H
+    og = torch.full((wl.T, B, H, 128), float("nan"), device=DEV)
+    ctx = _ctx(wl, params, lr)
+    try:
+        ws = torch.empty(kda.kda_decode_lowrank_workspace_bytes(ctx, B), dtype=torch.uint8, device=DEV)
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=side):
+            for t in range(wl.T):
+                kda.kda_decode_step_lowrank(ctx, B, lr["x"][t], tokens["q"][t], tokens["k"][t], tokens["v"][t],
+                                            tokens["gate_logit"][t], c2, S2, og[t], None, ws,
+                                            stream=torch.cuda.current_stream())
+        torch.cuda.current_stream().wait_stream(side)
+        assert bool(torch.isnan(og).all())   # the capture itself ran nothing
+        g.replay()
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+        del g
+    finally:
+        kda.kda_destroy(ctx)
+    assert torch.equal(o, og) and torch.equal(S, S2) and torch.equal(conv, c2)
+
+
 def test_lowrank_argument_errors():
     wl = synth.shrink(synth.WORKLOADS["decode_b64_h32_x256"], B=4, H=2, T=1)
     params = synth.make_params(wl, DEV)
