@@ -44,12 +44,16 @@
  *    is stated per call below.  A wait that gives up means the device did not
  *    complete a copy within a second, so later results on that device deserve
  *    the same suspicion.
- *  - Host-side fault injection for tests: the environment variable
- *    KDA_FAULT_INJECT, read by kda_create, names entry points ("decode",
- *    "prefill", "prefill_varlen", "lowrank", "project", "all"; comma-separated; the
- *    low-rank decode step counts as "decode" and "lowrank") whose launches that
- *    context replaces by cudaErrorLaunchFailure: nothing is launched, no
- *    buffer changes, and the call returns KDA_ERR_CUDA.
+ *  - Fault injection for tests: the environment variable KDA_FAULT_INJECT,
+ *    read by kda_create, names entry points ("decode", "prefill",
+ *    "prefill_varlen", "lowrank", "project", "all"; comma-separated; the
+ *    low-rank decode step counts as "decode" and "lowrank") whose launches
+ *    that context replaces by cudaErrorLaunchFailure: nothing is launched,
+ *    no buffer changes, and the call returns KDA_ERR_CUDA.  The name
+ *    "relay_drop" (not part of "all") makes kda_prefill's relay pairs skip
+ *    their first state hand-over: the receiving CTA's bounded wait runs out,
+ *    both CTAs of the pair give up, and kda_sync_status reports
+ *    KDA_ERR_TIMEOUT with the pair's S and window unchanged.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -191,8 +195,8 @@ KDA_API size_t kda_prefill_workspace_bytes(const kda_ctx *ctx, int B, int T);
  * as one CTA, bit for bit, so results do not depend on the split.
  * After a give-up (KDA_ERR_TIMEOUT from kda_sync_status) an affected pair
  * stops at the end of a chunk and keeps its old S and window; the o rows of
- * its chunks from the one that gave up onwards are not written (earlier rows
- * hold their results), so its o is incomplete.
+ * its chunks from the one that gave up onwards hold unspecified values
+ * (earlier rows hold their results).
  */
 KDA_API kda_status kda_prefill(kda_ctx *ctx, int B, int T,
                        const uint16_t *q, const uint16_t *k, const uint16_t *v,

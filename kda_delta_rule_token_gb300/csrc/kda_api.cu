@@ -2,12 +2,15 @@
 // device checks, launch and error reporting.  No allocation happens on the
 // per-call path; kda_create allocates the 16-byte kernel error word.
 //
-// Host-side fault injection: KDA_FAULT_INJECT, read once by kda_create, is a
+// Fault injection for tests: KDA_FAULT_INJECT, read once by kda_create, is a
 // comma-separated list of entry points ("decode", "prefill",
-// "prefill_varlen", or "all") whose launches that context replaces by the
-// error cudaErrorLaunchFailure: nothing is launched, no buffer is touched and
-// the call returns KDA_ERR_CUDA (kda_last_error_detail names the error and
-// says it was injected).  Unset or empty: no injection.
+// "prefill_varlen", "lowrank", "project", or "all") whose launches that
+// context replaces by the error cudaErrorLaunchFailure: nothing is launched,
+// no buffer is touched and the call returns KDA_ERR_CUDA
+// (kda_last_error_detail names the error and says it was injected).  The
+// name "relay_drop" (not part of "all") instead makes kda_prefill's relay
+// pairs skip their first state hand-over, so that a bounded wait inside the
+// kernel runs out.  Unset or empty: no injection.
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -60,7 +63,7 @@ kda_status check_device(const kda_ctx* ctx) {
 }
 
 constexpr unsigned kInjectDecode = 1u, kInjectPrefill = 2u, kInjectVarlen = 4u, kInjectLowrank = 8u,
-                   kInjectProject = 16u;
+                   kInjectProject = 16u, kInjectRelayDrop = 32u;
 
 // Parse KDA_FAULT_INJECT (see the top of this file).
 unsigned parse_inject(const char* v) {
@@ -77,6 +80,7 @@ unsigned parse_inject(const char* v) {
         else if (is("prefill_varlen")) m |= kInjectVarlen;
         else if (is("lowrank")) m |= kInjectLowrank;
         else if (is("project")) m |= kInjectProject;
+        else if (is("relay_drop")) m |= kInjectRelayDrop;
         else if (is("all")) m |= kInjectDecode | kInjectPrefill | kInjectVarlen | kInjectLowrank | kInjectProject;
         p = *e ? e + 1 : e;
     }
@@ -257,7 +261,7 @@ kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint
     }
     if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::PrefillIO io{B, T, nullptr, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
-                      workspace, workspace_bytes, 0};
+                      workspace, workspace_bytes, 0, (ctx->inject & kda::kInjectRelayDrop) ? 1 : 0};
     cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectPrefill, [&] {
         return kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word, static_cast<cudaStream_t>(stream));
     });

@@ -59,6 +59,10 @@ struct PrefillIO {
     // run as clusters of two CTAs that take alternate chunks and hand the
     // state over through distributed shared memory.
     int head0;
+    // Test injection (KDA_FAULT_INJECT "relay_drop"): the first CTA of every
+    // relay pair does not hand its first state over, so the second one's
+    // bounded wait runs out.
+    int drop_relay;
 };
 
 // Low-rank front-end weights bound to a context (borrowed, fp32), with

@@ -1052,7 +1052,7 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             tc::ld32(tc::taddr(tm, warp, TM_S + grp * 32), sv);
             wfree.wait();
             tc::wait_ld();
-            if (!*(volatile int*)s_dead) {
+            if (!*(volatile int*)s_dead && !(io.drop_relay && ci == 0)) {
                 const uint32_t rb = peer_st + (uint32_t)qrow * 512;
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4)

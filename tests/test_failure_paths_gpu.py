@@ -8,11 +8,19 @@
   the context's launches of it are replaced on the host by
   cudaErrorLaunchFailure; the call must return KDA_ERR_CUDA, launch nothing
   and leave every buffer as it was.
+* A relay hand-over that never comes: with KDA_FAULT_INJECT=relay_drop the
+  first CTA of each prefill relay pair skips its first state hand-over, so
+  the second CTA's bounded wait (1 s) runs out, then the first one's wait for
+  a state the second never sends; both give up, drain what they issued and
+  leave; kda_sync_status reports KDA_ERR_TIMEOUT, S and the window keep their
+  old contents, and the device keeps working.
 """
 import os
 
 import pytest
 import torch
+
+from harness import Guarded
 
 import kda_delta_rule_token_gb300 as kda
 from kda_delta_rule_token_gb300 import synth
@@ -182,5 +190,38 @@ def test_injected_lowrank_launch_failure(inject):
         torch.cuda.synchronize()
         assert bool((z == 3.0).all()) and bool((bl == 3.0).all()) and bool((o == 3.0).all())
         assert torch.equal(S, S0) and torch.equal(conv, c0)
+    finally:
+        kda.kda_destroy(ctx)
+
+
+def test_relay_hand_over_that_never_comes_times_out(inject, monkeypatch):
+    wl = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], B=1, H=2, T=192)   # relay pairs, 3 chunks
+    params, tokens = synth.make_params(wl, DEV), synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    S, conv = st["S"], st["conv_state"]
+    S.normal_(0.0, 0.01)
+    q, k, v = (tokens[n].view(torch.int16) for n in ("q", "k", "v"))
+    gS, gc = Guarded(S), Guarded(conv)
+    S0, c0 = S.clone(), conv.clone()
+    o = torch.zeros((wl.B, wl.T, wl.H, 128), device=DEV)
+    inject("relay_drop")
+    ctx = _create(wl, params)
+    try:
+        kda.kda_prefill(ctx, wl.B, wl.T, q, k, v, tokens["z"], tokens["beta_logit"], tokens["gate_logit"],
+                        gc.t, gS.t, o)
+        assert kda.kda_sync_status(ctx) == kda.KDA_ERR_TIMEOUT
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK          # reported once
+        assert torch.equal(gS.t, S0) and torch.equal(gc.t, c0)
+        assert gS.intact() and gc.intact()
+    finally:
+        kda.kda_destroy(ctx)
+    # a context without the injection computes the same call normally
+    monkeypatch.delenv("KDA_FAULT_INJECT", raising=False)
+    ctx = _create(wl, params)
+    try:
+        kda.kda_prefill(ctx, wl.B, wl.T, q, k, v, tokens["z"], tokens["beta_logit"], tokens["gate_logit"],
+                        conv, S, o)
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+        assert not torch.equal(S, S0)
     finally:
         kda.kda_destroy(ctx)
