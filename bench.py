@@ -292,13 +292,19 @@ class Ours:
             assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
             del g
 
-        # End to end through the C ABI with pinned host buffers: copy this
-        # call's inputs in, run, copy o out, all inside the timed region.  The
-        # batch is split into `--e2e-split` groups of sequences; a group's six
-        # inputs sit back to back in one pinned host buffer (each at a 16-byte
-        # multiple), so a group is one host-to-device copy, one decode call on
-        # views of the device copy and one device-to-host copy of its o, on
-        # three streams: group j's inputs arrive while group j - 1 decodes.
+        # End to end through the C ABI with pinned host buffers, the way a
+        # serving loop runs it: every step copies its inputs in from pinned
+        # host memory, decodes and copies o out, and the next step's inputs
+        # are staged while this step decodes.  The batch is split into
+        # `--e2e-split` groups of sequences; a group's six inputs sit back to
+        # back in one pinned host buffer (each at a 16-byte multiple), so a
+        # group is one host-to-device copy, one decode call on views of the
+        # device copy and one device-to-host copy of its o, on three streams.
+        # Device input packs and outputs alternate between two buffers: a
+        # step's copy-in waits for the decode two steps back that read the
+        # same pack, its decode for the copy-out two steps back of the same
+        # output.  Value: the time of Ke steps / Ke (events on the decode
+        # stream around the whole loop, the other streams wait for the start).
         ms_e2e, h2d, d2h = None, 0, 0
         if e2e:
             nh = min(8, wl.T)
@@ -323,48 +329,67 @@ class Ours:
                     for n, (a, n_el, _s) in ent.items():
                         hb[a:a + n_el].copy_(tk[n][t][b0:b1].reshape(-1))
                 host.append(hb)
-            dpack = torch.empty(total, dtype=torch.float32, device=self.dev)
-            seg = []                                        # (start, end) of each group in the pack
-            dv = []
+            dpack = [torch.empty(total, dtype=torch.float32, device=self.dev) for _ in range(2)]
+            seg = []                                        # (start, end) of each group in a pack
             start = 0
-            for (end, ent) in layout:
+            for (end, _ent) in layout:
                 seg.append((start, end))
-                dv.append({n: dpack[a:a + n_el].view(shp) for n, (a, n_el, shp) in ent.items()})
                 start = end
-            o_host = torch.empty((B, H, D), pin_memory=True)
+            dv = [[{n: dp[a:a + n_el].view(shp) for n, (a, n_el, shp) in ent.items()} for (_e, ent) in layout]
+                  for dp in dpack]
+            od = [torch.empty((B, H, D), device=self.dev) for _ in range(2)]
+            o_host = [torch.empty((B, H, D), pin_memory=True) for _ in range(2)]
             h2d = total * 4
-            d2h = o_host.numel() * 4
+            d2h = B * H * D * 4
             s_in = torch.cuda.Stream(device=self.dev)
             s_out = torch.cuda.Stream(device=self.dev)
+            ev_dec, ev_out = {}, {}
+
+            def steps(i0, n):
+                for i in range(i0, i0 + n):
+                    p = i % 2
+                    hb = host[i % nh]
+                    if flush:
+                        self.flush_l2()
+                    for j, (b0, b1) in enumerate(groups):
+                        a0, a1 = seg[j]
+                        if (i - 2, j) in ev_dec:
+                            s_in.wait_event(ev_dec.pop((i - 2, j)))
+                        with torch.cuda.stream(s_in):
+                            dpack[p][a0:a1].copy_(hb[a0:a1], non_blocking=True)
+                        e_in = torch.cuda.Event()
+                        e_in.record(s_in)
+                        self.stream.wait_event(e_in)
+                        if (i - 2, j) in ev_out:
+                            self.stream.wait_event(ev_out.pop((i - 2, j)))
+                        g_ = dv[p][j]
+                        kda.kda_decode_step(ctx, b1 - b0, g_["q"], g_["k"], g_["v"], g_["z"],
+                                            g_["beta_logit"], g_["gate_logit"], cs[b0:b1], S[b0:b1],
+                                            od[p][b0:b1], None, self.stream)
+                        e_d = torch.cuda.Event()
+                        e_d.record(self.stream)
+                        ev_dec[(i, j)] = e_d
+                        s_out.wait_event(e_d)
+                        with torch.cuda.stream(s_out):
+                            o_host[p][b0:b1].copy_(od[p][b0:b1], non_blocking=True)
+                        e_o = torch.cuda.Event()
+                        e_o.record(s_out)
+                        ev_out[(i, j)] = e_o
+
             Ke = max(3, min(K, 200))
-            eve = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(W + Ke)]
-            for i in range(W + Ke):
-                if flush:
-                    self.flush_l2()
-                eve[i][0].record(self.stream)
-                s_in.wait_event(eve[i][0])
-                s_out.wait_event(eve[i][0])
-                hb = host[i % nh]
-                for j, (b0, b1) in enumerate(groups):
-                    a0, a1 = seg[j]
-                    with torch.cuda.stream(s_in):
-                        dpack[a0:a1].copy_(hb[a0:a1], non_blocking=True)
-                    self.stream.wait_stream(s_in)
-                    g_ = dv[j]
-                    kda.kda_decode_step(ctx, b1 - b0, g_["q"], g_["k"], g_["v"], g_["z"],
-                                        g_["beta_logit"], g_["gate_logit"], cs[b0:b1], S[b0:b1],
-                                        o[b0:b1], None, self.stream)
-                    s_out.wait_stream(self.stream)
-                    with torch.cuda.stream(s_out):
-                        o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
-                self.stream.wait_stream(s_out)
-                eve[i][1].record(self.stream)
+            steps(0, W)
             self.barrier_sync()
-            eve = eve[W:]
-            ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            s_in.wait_event(e0)
+            s_out.wait_event(e0)
+            steps(W, Ke)
+            self.stream.wait_stream(s_out)
+            e1.record(self.stream)
+            self.barrier_sync()
+            ms_e2e = self.max_over_ranks(e0.elapsed_time(e1) / Ke)
             assert kda.kda_sync_status(ctx, self.stream) == kda.KDA_OK
-            del host, dpack, dv, o_host
+            del host, dpack, dv, od, o_host
         kda.kda_destroy(ctx)
 
         units = B * H                                   # (sequence, head) pairs per call
@@ -843,7 +868,7 @@ def main():
     ap.add_argument("--proj-only", default=None,
                     help="profiling only: time the projections on this workload's tokens alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-split", type=int, default=4,
+    ap.add_argument("--e2e-split", type=int, default=1,
                     help="groups of sequences the decode end-to-end step is pipelined over")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
@@ -876,7 +901,7 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     head = None if args.no_decode else ours.decode(HEADLINE_WL, flush=False, graph=True)
-    dec = None if args.no_decode else ours.decode(DECODE_WL, flush=True)
+    dec = None if args.no_decode else ours.decode(DECODE_WL, flush=True, e2e=False)
     d16 = None if args.no_decode else ours.decode(HEADLINE_WL, flush=False, e2e=False, state_bf16=True)
     dlr = None if args.no_decode else ours.decode_lowrank(DECODE_WL)
     psteps = max(3, min(args.steps, args.prefill_steps))
