@@ -572,47 +572,72 @@ class Ours:
 
         ms_e2e, h2d, d2h = None, 0, 0
         if e2e:
-            # End to end with pinned host buffers (inputs in, o out, per call),
-            # pipelined over groups of sequences: group j's inputs are copied in on
-            # one stream while group j - 1 runs (one kda_prefill call per group, on
-            # the group's slices of the same buffers) and group j - 2's output is
-            # copied out on a third stream.
+            # End to end with pinned host buffers (inputs in, o out, every
+            # call), as a serving loop runs it: within a call, group j's inputs
+            # are copied in on one stream while group j - 1 runs (one
+            # kda_prefill call per group of sequences) and finished groups'
+            # outputs are copied out on a third stream; across calls, the next
+            # call's copies overlap this call's kernels and copy-out.  Device
+            # inputs and outputs alternate between two sets: a copy-in waits
+            # for the kernel two calls back that read its buffers, a kernel
+            # for the copy-out two calls back of its output.  Value: the time
+            # of Ke calls / Ke (events on the kernel stream around the loop).
             names = ("q", "k", "v", "z", "beta_logit", "gate_logit")
             host = {n: tk[n].to("cpu").pin_memory() for n in names}
             o_host = torch.empty((B, T, H, D), pin_memory=True)
             h2d = sum(x.numel() * x.element_size() for x in host.values())
             d2h = o_host.numel() * 4
-            dbuf = tk                                       # reuse the device input buffers
+            dbuf = [tk, {n: torch.empty_like(tk[n]) for n in names}]
+            obuf = [o, torch.empty_like(o)]
             groups = [(b, min(B, b + max(1, B // 4))) for b in range(0, B, max(1, B // 4))]
             s_in = torch.cuda.Stream(device=self.dev)
             s_out = torch.cuda.Stream(device=self.dev)
+            ev_k, ev_o = {}, {}
+
+            def calls(i0, n):
+                for i in range(i0, i0 + n):
+                    p = i % 2
+                    db, ob = dbuf[p], obuf[p]
+                    S.zero_()
+                    cs.zero_()
+                    for j, (b0, b1) in enumerate(groups):
+                        if (i - 2, j) in ev_k:
+                            s_in.wait_event(ev_k.pop((i - 2, j)))
+                        with torch.cuda.stream(s_in):
+                            for nm in names:
+                                db[nm][b0:b1].copy_(host[nm][b0:b1], non_blocking=True)
+                        e_in = torch.cuda.Event()
+                        e_in.record(s_in)
+                        self.stream.wait_event(e_in)
+                        if (i - 2, j) in ev_o:
+                            self.stream.wait_event(ev_o.pop((i - 2, j)))
+                        kda.kda_prefill(ctx, b1 - b0, T, db["q"][b0:b1].view(torch.int16),
+                                        db["k"][b0:b1].view(torch.int16), db["v"][b0:b1].view(torch.int16),
+                                        db["z"][b0:b1], db["beta_logit"][b0:b1], db["gate_logit"][b0:b1],
+                                        cs[b0:b1], S[b0:b1], ob[b0:b1], ws, nws, self.stream)
+                        e_k = torch.cuda.Event()
+                        e_k.record(self.stream)
+                        ev_k[(i, j)] = e_k
+                        s_out.wait_event(e_k)
+                        with torch.cuda.stream(s_out):
+                            o_host[b0:b1].copy_(ob[b0:b1], non_blocking=True)
+                        e_o = torch.cuda.Event()
+                        e_o.record(s_out)
+                        ev_o[(i, j)] = e_o
+
             Ke = 3
-            eve = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-                   for _ in range(1 + Ke)]
-            for i in range(1 + Ke):
-                S.zero_()
-                cs.zero_()
-                t0 = eve[i][0]
-                t0.record(self.stream)
-                s_in.wait_event(t0)
-                s_out.wait_event(t0)
-                for (b0, b1) in groups:
-                    with torch.cuda.stream(s_in):
-                        for n in names:
-                            dbuf[n][b0:b1].copy_(host[n][b0:b1], non_blocking=True)
-                    self.stream.wait_stream(s_in)
-                    kda.kda_prefill(ctx, b1 - b0, T, dbuf["q"][b0:b1].view(torch.int16),
-                                    dbuf["k"][b0:b1].view(torch.int16), dbuf["v"][b0:b1].view(torch.int16),
-                                    dbuf["z"][b0:b1], dbuf["beta_logit"][b0:b1], dbuf["gate_logit"][b0:b1],
-                                    cs[b0:b1], S[b0:b1], o[b0:b1], ws, nws, self.stream)
-                    s_out.wait_stream(self.stream)
-                    with torch.cuda.stream(s_out):
-                        o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
-                self.stream.wait_stream(s_out)
-                eve[i][1].record(self.stream)
+            calls(0, 1)                                     # warm-up
             self.barrier_sync()
-            eve = eve[1:]                                   # the first pass is the warm-up
-            ms_e2e = self.max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in eve))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            s_in.wait_event(e0)
+            s_out.wait_event(e0)
+            calls(1, Ke)
+            self.stream.wait_stream(s_out)
+            e1.record(self.stream)
+            self.barrier_sync()
+            ms_e2e = self.max_over_ranks(e0.elapsed_time(e1) / Ke)
+            del dbuf, obuf, host, o_host
         kda.kda_destroy(ctx)
         th = B * T * H
         io_bytes = th * (3 * D * 2 + 3 * D * 4 + 4) + B * H * (STATE_BYTES + 2 * 9 * D * 4) \
