@@ -91,8 +91,10 @@ SMALL = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], B=2, H=3, T=130,
                      s0_std=0.05, win_std=1.0)
 
 
-@pytest.mark.parametrize("T", [1, 2, 16, 63, 64, 65, 100, 130])
+@pytest.mark.parametrize("T", [1, 2, 16, 63, 64, 65, 100, 128, 130, 192])
 def test_small_prefill_every_output(T):
+    """6 heads: one CTA per head for T <= 64, relay pairs (two CTAs taking
+    alternate chunks) from two chunks on; nonzero initial state and window."""
     wl = synth.shrink(SMALL, T=T)
     params, tokens, S, conv = _setup(wl)
     S0, c0 = S.clone(), conv.clone()
