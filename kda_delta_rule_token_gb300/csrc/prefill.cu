@@ -229,11 +229,12 @@ constexpr int kIssuerB = 480, kIssuer1 = 320, kStager = 384, kOStore = 96;
 // 16 warps: warp w reaches TMEM lanes [32 (w % 4), +32) and takes column group
 // w / 4 of every TMEM pass; in the thread-per-channel passes the same thread
 // owns channel c = its TMEM lane and group grp = w / 4.
-// RELAY: two CTAs per (sequence, head) take alternate chunks (CTA role r
-// does the chunks r, r + 2, ...); each builds the state-independent part of
-// its chunk (conv, norms, L/R, MMA0, the inverse, MMA_T) while the other
-// runs the state chain of the chunk before, then takes the state over from
-// it through the relay buffer, runs the chain and hands the state on.
+// RELAY: two CTAs per (sequence, head), one cluster, take alternate chunks
+// (CTA role r does the chunks r, r + 2, ...); each builds the
+// state-independent part of its chunk (conv, norms, L/R, MMA0, the inverse,
+// MMA_T, DT) while the other runs the state chain of the chunk before, then
+// takes the state over from it through distributed shared memory, runs the
+// chain and hands the state on.
 template <bool RELAY>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __grid_constant__ Maps maps) {
