@@ -517,4 +517,14 @@ kda_status kda_testing_bounded_wait(kda_ctx* ctx, unsigned limit_us, void* strea
     return KDA_OK;
 }
 
+long long kda_testing_prefill_relay_heads(long long heads, int T, int sm_count) {
+    if (heads < 0 || T < 0 || sm_count < 0) return -1;
+    return kda::prefill_relay_heads(heads, T, sm_count);
+}
+
+int kda_testing_project_o_ksplit(int hidden, int N, int HD, int sm_count) {
+    if (hidden < 0 || N <= 0 || HD < 0 || sm_count < 0) return -1;
+    return kda::project_o_ksplit(hidden, N, HD, sm_count);
+}
+
 }  // extern "C"

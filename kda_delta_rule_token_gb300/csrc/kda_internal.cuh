@@ -136,6 +136,13 @@ cudaError_t launch_project_o(const LayerParams& p, const Projections& pr, int N,
 // Test hook (csrc/testing.cu): a kernel whose bounded wait runs out.
 cudaError_t launch_testing_wait(int* err_word, unsigned long long limit_ns, cudaStream_t stream);
 
+// Launch policies (exported through the test hooks): how many of `heads`
+// (sequence, head) pairs of a T-token prefill run as relay pairs on a
+// device of sm_count SMs, and into how many K ranges the output projection
+// of N tokens (hidden outputs, HD inputs) is split.
+long long prefill_relay_heads(long long heads, int T, int sm_count);
+int project_o_ksplit(int hidden, int N, int HD, int sm_count);
+
 // Counts kernel launches made by the library (for benchmark accounting).
 void count_launches(uint64_t n);
 

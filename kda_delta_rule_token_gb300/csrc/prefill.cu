@@ -1173,6 +1173,10 @@ long long relay_heads(long long heads, int nchunks, int sm_count) {
 
 }  // namespace
 
+long long prefill_relay_heads(long long heads, int T, int sm_count) {
+    return relay_heads(heads, (T + C - 1) / C, sm_count);
+}
+
 size_t prefill_workspace_bytes(int, int, int, const DeviceInfo&) { return 0; }
 
 cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const DeviceInfo& dev,

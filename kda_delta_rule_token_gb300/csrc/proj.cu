@@ -391,6 +391,8 @@ cudaError_t launch_project_qkvg(const LayerParams& p, const Projections& pr, int
     return run_proj(pr.map_qkvg, 4 * HD, x, N, pr.hidden, segs, 4, 1, dev, err_word, stream, false);
 }
 
+int project_o_ksplit(int hidden, int N, int HD, int sm_count) { return ksplit_for(hidden, N, HD, sm_count); }
+
 size_t project_o_workspace_bytes(const LayerParams& p, int N) {
     return N <= 0 ? 0 : (size_t)N * p.H * kHeadDim * 2;
 }
