@@ -888,6 +888,8 @@ def main():
                     help="profiling only: time this decode workload alone (no e2e, no graph)")
     ap.add_argument("--bf16-state", action="store_true",
                     help="profiling only: with --decode-workload, the bf16-state decode")
+    ap.add_argument("--varlen-only", action="store_true",
+                    help="profiling only: time the packed-sequence prefill alone")
     ap.add_argument("--lowrank-only", action="store_true",
                     help="profiling only: time the low-rank front-end decode line alone")
     ap.add_argument("--proj-only", default=None,
@@ -904,7 +906,8 @@ def main():
 
     ours = Ours(args, world, rank, local)
     peaks = load_peaks()
-    if args.prefill_workload or args.decode_workload or args.lowrank_only or args.proj_only:   # profiling runs
+    if args.prefill_workload or args.decode_workload or args.lowrank_only or args.proj_only or args.varlen_only:
+        # profiling runs
         out = {"profiling_only": True}
         if args.proj_only:
             r = ours.projections(args.proj_only, with_cublas=False)
@@ -912,6 +915,9 @@ def main():
         if args.lowrank_only:
             r = ours.decode_lowrank(DECODE_WL)
             out.update(lowrank_step_ms=round(r["ms_step"], 5), lowrank_frontend_ms=round(r["ms_frontend"], 5))
+        if args.varlen_only:
+            r = ours.prefill_varlen()
+            out.update(varlen_ms=round(r["ms"], 4), varlen_tokens=r["total_tokens"])
         if args.prefill_workload:
             r = ours.prefill(args.prefill_workload, e2e=False)
             out.update(prefill_workload=args.prefill_workload, prefill_ms=round(r["ms"], 4))
@@ -1014,7 +1020,8 @@ def main():
             "gpu_launches": pvl["launches"],
             "roofline": {"bound": "hbm", "achieved": round(pvl["alg_gbs"], 1), "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": round(pvl["alg_gbs"] / peaks["hbm_gbs"], 4),
-                         "traffic": None, "kernel": "kda_prefill_kernel",
+                         "traffic": profile_traffic("prefill_varlen_kernel.md", psha),
+                         "kernel": "kda_prefill_kernel",
                          "alg_bytes_per_launch": pvl["alg_bytes"]},
         }
     for key, r in (("projections", prj), ("projections_decode", prd)):
