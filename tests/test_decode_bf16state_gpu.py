@@ -120,10 +120,24 @@ def _setup(wl, T=None):
     return params, tokens, bf16_of(st["S"]), st["conv_state"]
 
 
-@pytest.mark.parametrize("shape", [dict(B=1, H=2, T=16), dict(B=3, H=5, T=9)], ids=["tiny", "ragged"])
+def _extreme(params, tokens):
+    """Strong decay (gk about -30 per token: the state walks down into the
+    subnormal range), saturated beta, a zero q, large v."""
+    params["A_log"][0].fill_(0.0)
+    tokens["z"][:, 0, 0].fill_(30.0)
+    tokens["beta_logit"][:, 1, 0] = 40.0
+    tokens["beta_logit"][:, 1, 1] = -40.0
+    tokens["q"][2, 0].zero_()
+    tokens["v"][3].mul_(1e3)
+
+
+@pytest.mark.parametrize("shape", [dict(B=1, H=2, T=16), dict(B=3, H=5, T=9), dict(B=2, H=2, T=8)],
+                         ids=["tiny", "ragged", "extreme"])
 def test_each_call_is_a_valid_rounding(shape):
     wl = synth.shrink(synth.WORKLOADS["decode_b64_h32_x256"], **shape)
     params, tokens, S16, conv = _setup(wl)
+    if shape["T"] == 8:
+        _extreme(params, tokens)
     # a nonzero starting state (from fp32 warm tokens) so that decay, erase and write all matter
     warm = synth.make_tokens(wl, DEV, T=6, warm=True)
     run_calls(wl, params, warm, S16, conv)
