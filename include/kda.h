@@ -53,7 +53,10 @@
  *    "relay_drop" (not part of "all") makes kda_prefill's relay pairs skip
  *    their first state hand-over: the receiving CTA's bounded wait runs out,
  *    both CTAs of the pair give up, and kda_sync_status reports
- *    KDA_ERR_TIMEOUT with the pair's S and window unchanged.
+ *    KDA_ERR_TIMEOUT with the pair's S and window unchanged.  The name
+ *    "split_drop" (not part of "all") makes the producers of kda_prefill's
+ *    split schedule skip publishing their first chunk: the consumers' bounded
+ *    waits run out, with the same report and S and window unchanged.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -167,9 +170,9 @@ KDA_API kda_status kda_decode_step_bf16state(kda_ctx *ctx, int B,
                            float *o, float *o_pre, void *stream);
 
 /*
- * Bytes of device workspace kda_prefill needs for B sequences of T tokens
- * (0 when none is needed; the current kernels need none, callers should
- * still ask).
+ * Bytes of device workspace with which kda_prefill runs B sequences of T
+ * tokens on its split schedule (0 when the call has none: one chunk per
+ * sequence, or enough sequence-heads to fill the SMs in whole waves).
  */
 KDA_API size_t kda_prefill_workspace_bytes(const kda_ctx *ctx, int B, int T);
 
@@ -184,15 +187,21 @@ KDA_API size_t kda_prefill_workspace_bytes(const kda_ctx *ctx, int B, int T);
  *   conv_state   [B][3][3*H*d] fp32 (in/out), as for kda_decode_step
  *   S            [B][H][d][d] fp32 (in/out)
  *   o            [B][T][H][d] fp32 (out)
- *   workspace    device buffer of at least kda_prefill_workspace_bytes(ctx,B,T)
- *                bytes, 16-byte aligned (may be NULL when that is 0);
- *                workspace_bytes is its size.  A smaller buffer gives
- *                KDA_ERR_INVALID_ARG.
- * B == 0 or T == 0 is a no-op returning KDA_OK.  Sequence-head pairs that
- * would leave SMs idle (all of them when two CTAs per pair fit on the device,
- * else those of a last partial wave) run as two CTAs that take alternate
- * chunks and hand the state to each other; they compute the same arithmetic
- * as one CTA, bit for bit, so results do not depend on the split.
+ *   workspace    optional device buffer, 16-byte aligned, of workspace_bytes
+ *                bytes (NULL: none); the library's scratch for the call,
+ *                ordered on the stream like the call itself.
+ * B == 0 or T == 0 is a no-op returning KDA_OK.  Sequence-head pairs fill the
+ * SMs one CTA each; those that would leave SMs idle (all of them when two
+ * CTAs per pair fit on the device, else those of a last partial wave) run on
+ * one of two few-head schedules.  With a workspace of at least
+ * kda_prefill_workspace_bytes(ctx, B, T) bytes, producer CTAs build every
+ * chunk's state-independent operands in parallel and pass them through the
+ * workspace to one consumer CTA per pair, which keeps the state and runs the
+ * sequential part (one cooperative launch: all its CTAs are resident at once;
+ * it needs the device's SMs free of other work to start); with less, or none,
+ * two CTAs per pair take alternate chunks and hand the state to each other.
+ * All schedules compute the same arithmetic in the same order, so results are
+ * bit for bit the same whichever runs.
  * After a give-up (KDA_ERR_TIMEOUT from kda_sync_status) an affected pair
  * stops at the end of a chunk and keeps its old S and window; the o rows of
  * its chunks from the one that gave up onwards hold unspecified values

@@ -9,8 +9,10 @@
 // no buffer is touched and the call returns KDA_ERR_CUDA
 // (kda_last_error_detail names the error and says it was injected).  The
 // name "relay_drop" (not part of "all") instead makes kda_prefill's relay
-// pairs skip their first state hand-over, so that a bounded wait inside the
-// kernel runs out.  Unset or empty: no injection.
+// pairs skip their first state hand-over, and "split_drop" (not part of
+// "all") makes the producers of its split schedule skip publishing their
+// first chunk, so that a bounded wait inside the kernel runs out.  Unset or
+// empty: no injection.
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -63,7 +65,8 @@ kda_status check_device(const kda_ctx* ctx) {
 }
 
 constexpr unsigned kInjectDecode = 1u, kInjectPrefill = 2u, kInjectVarlen = 4u, kInjectLowrank = 8u,
-                   kInjectProject = 16u, kInjectRelayDrop = 32u;
+                   kInjectProject = 16u, kInjectRelayDrop = 32u,
+                   kInjectSplitDrop = 64u;
 
 // Parse KDA_FAULT_INJECT (see the top of this file).
 unsigned parse_inject(const char* v) {
@@ -81,6 +84,7 @@ unsigned parse_inject(const char* v) {
         else if (is("lowrank")) m |= kInjectLowrank;
         else if (is("project")) m |= kInjectProject;
         else if (is("relay_drop")) m |= kInjectRelayDrop;
+        else if (is("split_drop")) m |= kInjectSplitDrop;
         else if (is("all")) m |= kInjectDecode | kInjectPrefill | kInjectVarlen | kInjectLowrank | kInjectProject;
         p = *e ? e + 1 : e;
     }
@@ -254,14 +258,14 @@ kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint
         if (!aligned16(p)) return KDA_ERR_ALIGNMENT;
     if (!aligned4(beta_logit)) return KDA_ERR_ALIGNMENT;
     if ((long long)B * ctx->params.H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
-    const size_t need = kda::prefill_workspace_bytes(ctx->params.H, B, T, ctx->dev);
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
-        if (!aligned16(workspace)) return KDA_ERR_ALIGNMENT;
-    }
+    // The workspace is optional: with kda_prefill_workspace_bytes of it the
+    // few-head schedule splits producers from consumers, else it runs relay pairs.
+    if (workspace && !aligned16(workspace)) return KDA_ERR_ALIGNMENT;
+    if (!workspace) workspace_bytes = 0;
     if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::PrefillIO io{B, T, nullptr, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
-                      workspace, workspace_bytes, 0, (ctx->inject & kda::kInjectRelayDrop) ? 1 : 0};
+                      workspace, workspace_bytes, 0, (ctx->inject & kda::kInjectRelayDrop) ? 1 : 0,
+                      (ctx->inject & kda::kInjectSplitDrop) ? 1 : 0};
     cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectPrefill, [&] {
         return kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word, static_cast<cudaStream_t>(stream));
     });

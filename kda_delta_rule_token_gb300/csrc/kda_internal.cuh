@@ -63,6 +63,10 @@ struct PrefillIO {
     // relay pair does not hand its first state over, so the second one's
     // bounded wait runs out.
     int drop_relay;
+    // Test injection (KDA_FAULT_INJECT "split_drop"): the producers of the
+    // split schedule do not publish their first chunk, so its consumer's
+    // bounded wait runs out.
+    int drop_split;
 };
 
 // Low-rank front-end weights bound to a context (borrowed, fp32), with

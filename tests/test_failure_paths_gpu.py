@@ -14,6 +14,10 @@
   a state the second never sends; both give up, drain what they issued and
   leave; kda_sync_status reports KDA_ERR_TIMEOUT, S and the window keep their
   old contents, and the device keeps working.
+* A chunk that is never published: with KDA_FAULT_INJECT=split_drop the
+  producers of the split schedule skip publishing their first chunk, so each
+  consumer's bounded wait for its head's first chunk runs out; the same
+  report, S and the window unchanged, the device still working.
 """
 import os
 
@@ -221,6 +225,42 @@ def test_relay_hand_over_that_never_comes_times_out(inject, monkeypatch):
     try:
         kda.kda_prefill(ctx, wl.B, wl.T, q, k, v, tokens["z"], tokens["beta_logit"], tokens["gate_logit"],
                         conv, S, o)
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+        assert not torch.equal(S, S0)
+    finally:
+        kda.kda_destroy(ctx)
+
+
+def test_split_chunk_that_is_never_published_times_out(inject, monkeypatch):
+    wl = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], B=1, H=2, T=192)   # split schedule, 3 chunks
+    params, tokens = synth.make_params(wl, DEV), synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    S, conv = st["S"], st["conv_state"]
+    S.normal_(0.0, 0.01)
+    q, k, v = (tokens[n].view(torch.int16) for n in ("q", "k", "v"))
+    gS, gc = Guarded(S), Guarded(conv)
+    S0, c0 = S.clone(), conv.clone()
+    o = torch.zeros((wl.B, wl.T, wl.H, 128), device=DEV)
+    inject("split_drop")
+    ctx = _create(wl, params)
+    try:
+        nws = kda.kda_prefill_workspace_bytes(ctx, wl.B, wl.T)
+        assert nws > 0
+        ws = torch.empty(nws, dtype=torch.uint8, device=DEV)
+        kda.kda_prefill(ctx, wl.B, wl.T, q, k, v, tokens["z"], tokens["beta_logit"], tokens["gate_logit"],
+                        gc.t, gS.t, o, ws, nws)
+        assert kda.kda_sync_status(ctx) == kda.KDA_ERR_TIMEOUT
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK          # reported once
+        assert torch.equal(gS.t, S0) and torch.equal(gc.t, c0)
+        assert gS.intact() and gc.intact()
+    finally:
+        kda.kda_destroy(ctx)
+    # a context without the injection computes the same call normally
+    monkeypatch.delenv("KDA_FAULT_INJECT", raising=False)
+    ctx = _create(wl, params)
+    try:
+        kda.kda_prefill(ctx, wl.B, wl.T, q, k, v, tokens["z"], tokens["beta_logit"], tokens["gate_logit"],
+                        conv, S, o, ws, nws)
         assert kda.kda_sync_status(ctx) == kda.KDA_OK
         assert not torch.equal(S, S0)
     finally:

@@ -32,8 +32,11 @@ def bits(x: torch.Tensor) -> torch.Tensor:
     return x.view(torch.int16)
 
 
-def gpu_prefill(wl, params, tokens, S, conv, T=None, t0=0, stream=None):
-    """Prefill tokens [t0, t0+T) of ``tokens`` ([B, T, H, d]) in place on S / conv."""
+def gpu_prefill(wl, params, tokens, S, conv, T=None, t0=0, stream=None, schedule="split"):
+    """Prefill tokens [t0, t0+T) of ``tokens`` ([B, T, H, d]) in place on S / conv.
+    schedule "split": with the workspace kda_prefill_workspace_bytes asks for
+    (few-head calls split producers from consumers); "relay": without one
+    (those heads run as relay pairs)."""
     B, Tall, H, d = tokens["q"].shape
     T = Tall - t0 if T is None else T
     sl = lambda x: x[:, t0:t0 + T].contiguous()
@@ -45,6 +48,8 @@ def gpu_prefill(wl, params, tokens, S, conv, T=None, t0=0, stream=None):
     ctx = kda.kda_create(H, params["conv_w"], params["dt_bias"], params["A_log"], params["gamma"])
     try:
         nws = kda.kda_prefill_workspace_bytes(ctx, B, T)
+        if schedule == "relay":
+            nws = 0
         ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=DEV) if nws else None
         kda.kda_prefill(ctx, B, T, q, k, v, z, bl, g, gc.t, gS.t, go.t, ws, nws, stream=stream)
         assert kda.kda_sync_status(ctx, stream) == kda.KDA_OK
@@ -91,14 +96,17 @@ SMALL = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], B=2, H=3, T=130,
                      s0_std=0.05, win_std=1.0)
 
 
-@pytest.mark.parametrize("T", [1, 2, 16, 63, 64, 65, 100, 128, 130, 192])
-def test_small_prefill_every_output(T):
-    """6 heads: one CTA per head for T <= 64, relay pairs (two CTAs taking
-    alternate chunks) from two chunks on; nonzero initial state and window."""
+@pytest.mark.parametrize("schedule", ["split", "relay"])
+@pytest.mark.parametrize("T", [1, 2, 16, 63, 64, 65, 100, 128, 130, 192, 320])
+def test_small_prefill_every_output(T, schedule):
+    """6 heads: one CTA per head for T <= 64; from two chunks on, producers
+    and one consumer per head (split) or two CTAs per head taking alternate
+    chunks (relay); nonzero initial state and window.  T = 320 (five chunks)
+    wraps the split schedule's ring of four slots per head."""
     wl = synth.shrink(SMALL, T=T)
     params, tokens, S, conv = _setup(wl)
     S0, c0 = S.clone(), conv.clone()
-    o = gpu_prefill(wl, params, tokens, S, conv)
+    o = gpu_prefill(wl, params, tokens, S, conv, schedule=schedule)
     pairs = [(b, h) for b in range(wl.B) for h in range(wl.H)]
     ref = oracle_pairs(params, tokens, S0, c0, pairs, call_major=False)
     check(ref, o, S, conv, pairs)
@@ -231,15 +239,47 @@ def test_graph_replay_equals_launch():
     assert torch.equal(c2, conv)
 
 
-def test_relay_pairs_match_oracle_and_tail_split():
-    """Heads run as CTA pairs that alternate chunks and relay the state
-    (few heads: every head; more heads than SMs: the last partial wave's).
-    200 heads = one full wave of single CTAs plus a 48-head tail of pairs on
-    152 SMs; sampled heads from both parts against the oracle."""
+@pytest.mark.parametrize("schedule", ["split", "relay"])
+def test_tail_wave_matches_oracle(schedule):
+    """More heads than SMs: the last partial wave runs on the few-head
+    schedule (split, or relay pairs without a workspace).  200 heads = one
+    full wave of single CTAs plus a 48-head tail on 152 SMs; sampled heads
+    from both parts against the oracle."""
     wl = synth.shrink(synth.WORKLOADS["prefill_b8_h64_t8192"], B=2, H=100, T=200)
     params, tokens, S, conv = _setup(wl)
     S0, c0 = S.clone(), conv.clone()
-    o = gpu_prefill(wl, params, tokens, S, conv)
+    o = gpu_prefill(wl, params, tokens, S, conv, schedule=schedule)
     pairs = [(0, 0), (0, 57), (1, 51), (1, 52), (1, 99)]
     ref = oracle_pairs(params, tokens, S0, c0, pairs, call_major=False)
     check(ref, o, S, conv, pairs)
+
+
+@pytest.mark.parametrize("shape", [dict(B=1, H=32, T=4096), dict(B=2, H=100, T=333)], ids=["single_seq", "tail"])
+def test_schedules_agree_bit_for_bit(shape):
+    """The split schedule, the relay pairs and single CTAs (the packed entry
+    point runs one CTA per sequence-head) compute the same arithmetic in the
+    same order: o, S and the window agree bit for bit, at the single-sequence
+    workload's full size and on a tail wave with a ragged last chunk."""
+    wl = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], **shape)
+    params, tokens, S, conv = _setup(wl)
+    S0, c0 = S.clone(), conv.clone()
+    res = {}
+    for schedule in ("split", "relay"):
+        S1, c1 = S0.clone(), c0.clone()
+        res[schedule] = (gpu_prefill(wl, params, tokens, S1, c1, schedule=schedule), S1, c1)
+    B, T, H, d = tokens["q"].shape
+    cu = torch.arange(0, (B + 1) * T, T, dtype=torch.int32, device=DEV)
+    flat = {n: tokens[n].reshape((B * T,) + tuple(tokens[n].shape[2:])).contiguous() for n in tokens}
+    o_v = torch.zeros((B * T, H, d), device=DEV)
+    S_v, c_v = S0.clone(), c0.clone()
+    ctx = kda.kda_create(H, params["conv_w"], params["dt_bias"], params["A_log"], params["gamma"])
+    try:
+        kda.kda_prefill_varlen(ctx, B, cu, B * T, bits(flat["q"]), bits(flat["k"]), bits(flat["v"]), flat["z"],
+                               flat["beta_logit"], flat["gate_logit"], c_v, S_v, o_v)
+        assert kda.kda_sync_status(ctx) == kda.KDA_OK
+    finally:
+        kda.kda_destroy(ctx)
+    for schedule, (o, S1, c1) in res.items():
+        assert torch.equal(o.reshape(B * T, H, d), o_v), schedule
+        assert torch.equal(S1, S_v), schedule
+        assert torch.equal(c1, c_v), schedule
