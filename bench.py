@@ -533,6 +533,9 @@ class Ours:
     def prefill(self, wl_name, e2e=True):
         torch, kda, synth = self.torch, self.kda, self.synth
         wl = synth.WORKLOADS[wl_name]
+        if self.args.prefill_shape:   # profiling: a smaller case of the workload
+            sB, sH, sT = (int(x) for x in self.args.prefill_shape.split(","))
+            wl = synth.shrink(wl, B=sB, H=sH, T=sT)
         p = synth.make_params(wl, self.dev)
         tk = synth.make_tokens(wl, self.dev)
         st = synth.make_state(wl, self.dev)
@@ -642,7 +645,11 @@ class Ours:
         th = B * T * H
         io_bytes = th * (3 * D * 2 + 3 * D * 4 + 4) + B * H * (STATE_BYTES + 2 * 9 * D * 4) \
             + H * 7680
-        res = {"wl": wl, "ms": ms, "launches": launches,
+        per_call = launches // K
+        kernels = ("kda_prefill_kernel" if nws == 0 else
+                   "kda_prefill_split_kernel" if per_call == 1 else
+                   "kda_prefill_kernel + kda_prefill_split_kernel (last partial wave)")
+        res = {"wl": wl, "ms": ms, "launches": launches, "kernels": kernels, "workspace_bytes": nws,
                "tokens_s": self.world * B * T / (ms * 1e-3),
                "e2e_tokens_s": None if ms_e2e is None else self.world * B * T / (ms_e2e * 1e-3),
                "ms_e2e": ms_e2e, "h2d": h2d, "d2h": d2h, "alg_bytes": io_bytes,
@@ -856,8 +863,9 @@ def prefill_block(pre, peaks, steps, md_name, sha, cpu=None):
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(pre["alg_gbs"] / peaks["hbm_gbs"], 4),
                      "traffic": profile_traffic(md_name, sha),
-                     "kernel": "kda_prefill_kernel", "peak_src": peaks["src"] + " hbm_gbs",
+                     "kernel": pre["kernels"], "peak_src": peaks["src"] + " hbm_gbs",
                      "alg_bytes_per_launch": pre["alg_bytes"]},
+        "workspace_bytes": pre["workspace_bytes"],
         "tensor": {"achieved_tflops": round(pre["alg_tflops"], 2),
                    "pct_of_bf16_peak": round(100 * pre["alg_tflops"] / peaks["bf16_tflops"], 2),
                    "pct_of_tf32_peak": round(100 * pre["alg_tflops"] / tf32_peak, 2),
@@ -884,6 +892,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip every decode line (profiling only)")
     ap.add_argument("--prefill-workload", default=None,
                     help="profiling only: time this prefill workload alone")
+    ap.add_argument("--prefill-shape", default=None,
+                    help="profiling only: with --prefill-workload, 'B,H,T' of a smaller case of it")
     ap.add_argument("--decode-workload", default=None,
                     help="profiling only: time this decode workload alone (no e2e, no graph)")
     ap.add_argument("--bf16-state", action="store_true",

@@ -1306,6 +1306,9 @@ constexpr uint32_t kSlotBytes = SL_SMALL + kSmallBytes;
 // operand (lower half) and the U operand (upper half); L; the gate / o tile
 // in the R region; V; the small records (two, by chunk parity) in the Minv^T region.
 constexpr uint32_t CON_X = OFF_ST, CON_U = OFF_ST + 32768, CON_OG = OFF_R, CON_SMALL = OFF_MT;
+// The consumer's operand copies come from warp 14 (lane quadrant 2: idle in
+// the X epilogue, so a wait for the next chunk's slot does not hold up the chain).
+constexpr int kCStager = 448;
 
 struct SplitIO {
     uint8_t* ring;   // [heads][kRing] slots of kSlotBytes
@@ -1536,7 +1539,7 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
         };
         if (tid < D) t.s_gam[tid] = 0.5f * p.gamma[h * D + tid];
         bool have_next = false;   // stager: the next chunk's slot is published (and its loads issued)
-        if (tid == kStager) {
+        if (tid == kCStager) {
             load_gate(0);
             if (flag_wait(sp.ready + hh * kRing, 1, s_dead, err)) {
                 fence_proxy_async_global();
@@ -1562,7 +1565,22 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
             const bool fb = reinterpret_cast<const int*>(small)[C + D] != 0;
             const float gl = small[C + t.qrow];
             state_pass(t, esc_prev, false, fb, gl, nullptr);
-            {
+            publish();   // S^T operand, rescaled master
+            if (tid == kIssuer1) {
+                mma1_part(t, 0, s_bar1);
+                mma1_part(t, 1, s_bar1);
+            }
+            // under MMA1: is the next chunk published?
+            if (tid == kCStager)
+                have_next = ci + 1 < nchunks && flag_wait(sp.ready + hh * kRing + (ci + 1) % kRing, ci + 2, s_dead, err);
+            wt1.wait();   // MMA1: L and S^T are free
+            if (tid == kCStager && have_next) {
+                fence_proxy_async_global();
+                load_a(ci + 1);
+            }
+            wV.wait();   // V
+            if ((warp & 3) < 2) x_epilogue(t, small, CON_X);
+            {   // DT and R^T (loaded at the chunk's start) into TMEM
                 uint32_t v[16];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) { v[4 * k] = dtr[k].x; v[4 * k + 1] = dtr[k].y; v[4 * k + 2] = dtr[k].z; v[4 * k + 3] = dtr[k].w; }
@@ -1571,23 +1589,8 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
                 for (int k = 0; k < 4; ++k) { v[4 * k] = rtr[k].x; v[4 * k + 1] = rtr[k].y; v[4 * k + 2] = rtr[k].z; v[4 * k + 3] = rtr[k].w; }
                 tc::st16(tc::taddr(t.tm, warp, TM_RT + t.grp * 16), v);
             }
-            publish();   // S^T operand, rescaled master, DT and R^T
-            if (tid == kIssuer1) {
-                mma1_part(t, 0, s_bar1);
-                mma1_part(t, 1, s_bar1);
-            }
-            wt1.wait();   // MMA1: L and S^T are free
-            if (tid == kStager) {
-                have_next = ci + 1 < nchunks && flag_wait(sp.ready + hh * kRing + (ci + 1) % kRing, ci + 2, s_dead, err);
-                if (have_next) {
-                    fence_proxy_async_global();
-                    load_a(ci + 1);
-                }
-            }
-            wV.wait();   // V
-            if ((warp & 3) < 2) x_epilogue(t, small, CON_X);
             publish();
-            if (tid == kStager) {
+            if (tid == kCStager) {
                 // every read of chunk ci's slot is done: its producer may refill it
                 st_release(sp.consumed + hh, ci + 1);
                 if (have_next) load_v(ci + 1);
@@ -1607,7 +1610,7 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
             const bool stop = __syncthreads_or(*(volatile int*)s_dead) != 0;
             tc::fence_after();
             if (stop) break;
-            if (tid == kStager && ci + 1 < nchunks) load_gate(ci + 1);
+            if (tid == kCStager && ci + 1 < nchunks) load_gate(ci + 1);
         }
         const bool dead = __syncthreads_or(*(volatile int*)s_dead) != 0;
         if (!dead) {
@@ -1619,7 +1622,7 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
         if (tid == kOStore) ptx::bulk_wait_all();
         if (dead) {
             if (tid == 0 || tid == kIssuer1) tc::commit(s_drain);
-            if (tid == kStager) {
+            if (tid == kCStager) {
                 if (*s_na > 0) ptx::mbar_wait_timed(s_ldA, (uint32_t)((*s_na - 1) & 1));
                 if (*s_nv > 0) ptx::mbar_wait_timed(s_ldV, (uint32_t)((*s_nv - 1) & 1));
                 if (*s_nt > 0) ptx::mbar_wait_timed(s_gbar, (uint32_t)((*s_nt - 1) & 1));
