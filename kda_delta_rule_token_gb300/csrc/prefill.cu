@@ -1536,6 +1536,10 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
             ptx::mbar_arrive_expect_tx(s_gbar, C * D * 4);
 #pragma unroll
             for (int j = 0; j < 4; ++j) ptx::tma_load_4d(sm + CON_OG + j * kOGBox, &maps.g, j * 32, h, ci * C, b, s_gbar);
+            if (ci + 1 < nchunks) {   // the next chunk's gate tile into L2 a chunk ahead
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ptx::tma_prefetch_4d(&maps.g, j * 32, h, (ci + 1) * C, b);
+            }
         };
         if (tid < D) t.s_gam[tid] = 0.5f * p.gamma[h * D + tid];
         bool have_next = false;   // stager: the next chunk's slot is published (and its loads issued)
@@ -1570,6 +1574,9 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
                 mma1_part(t, 0, s_bar1);
                 mma1_part(t, 1, s_bar1);
             }
+            // under MMA1: the gate tile becomes gamma sigmoid(gate) (warps 1..15)
+            wgate.wait();
+            gate_pass(t, CON_OG);
             // under MMA1: is the next chunk published?
             if (tid == kCStager)
                 have_next = ci + 1 < nchunks && flag_wait(sp.ready + hh * kRing + (ci + 1) % kRing, ci + 2, s_dead, err);
@@ -1596,21 +1603,19 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
                 if (have_next) load_v(ci + 1);
             }
             if (tid == 0) mma2(t, CON_X, s_bar2);
-            wgate.wait();
-            gate_pass(t, CON_OG);
-            if ((warp & 3) < 2) named_barrier_arrive(4, kThreads);
-            else named_barrier_sync(4, kThreads);
             wt2.wait();   // MMA2
             if ((warp & 3) < 2) u_operand_mma3(t, CON_U, s_bar3);
             else out_epilogue(t, CON_OG, p.rms_eps, n, false, nullptr, 0, maps, h, t0, b);
             wt3.wait();   // MMA3
-            if (tid == kOStore) ptx::bulk_wait_read_all();   // the o tile has left shared memory
             esc_prev = __expf(fb ? 0.f : 0.5f * gl);   // e^{G_last - rho_R}
             tc::fence_before();
             const bool stop = __syncthreads_or(*(volatile int*)s_dead) != 0;
             tc::fence_after();
             if (stop) break;
-            if (tid == kCStager && ci + 1 < nchunks) load_gate(ci + 1);
+            if (tid == kOStore) {
+                ptx::bulk_wait_read_all();   // the o tile has left shared memory
+                if (ci + 1 < nchunks) load_gate(ci + 1);
+            }
         }
         const bool dead = __syncthreads_or(*(volatile int*)s_dead) != 0;
         if (!dead) {
