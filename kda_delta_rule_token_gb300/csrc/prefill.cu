@@ -1553,18 +1553,32 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
         }
         state_in(t, io.S + (size_t)bh * D * D);
         sync_tc();   // the stager's acquire of chunk 0 comes before every thread's reads of its slot
+        // DT and R^T of a chunk: loaded into registers while MMA2 of the chunk
+        // before runs, written into TMEM once MMA2 (DT) and MMA3 (R^T) of that
+        // chunk have read the previous ones.
+        uint4 dtr[4], rtr[4];
+        auto load_dtrt = [&](int cj) {
+            const float* dti = reinterpret_cast<const float*>(slot_of(cj) + SL_DT);
+            const float* rti = reinterpret_cast<const float*>(slot_of(cj) + SL_RT);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                dtr[k] = *reinterpret_cast<const uint4*>(dti + img_at(t, k));
+                rtr[k] = *reinterpret_cast<const uint4*>(rti + img_at(t, k));
+            }
+        };
+        auto store_tm = [&](const uint4 (&r)[4], int col) {
+            uint32_t v[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) { v[4 * k] = r[k].x; v[4 * k + 1] = r[k].y; v[4 * k + 2] = r[k].z; v[4 * k + 3] = r[k].w; }
+            tc::st16(tc::taddr(t.tm, warp, col + t.grp * 16), v);
+        };
+        load_dtrt(0);
+        store_tm(dtr, TM_DT);
+        store_tm(rtr, TM_RT);
         float esc_prev = 1.0f;
         for (int ci = 0; ci < nchunks; ++ci) {
             const int t0 = ci * C, n = min(C, T - t0);
-            const uint8_t* slot = slot_of(ci);
             const float* small = reinterpret_cast<const float*>(sm + CON_SMALL + (ci & 1) * kSmallBytes);
-            // DT and R^T of the chunk: into registers now, into TMEM after the state pass.
-            uint4 dtr[4], rtr[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                dtr[k] = *reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(slot + SL_DT) + img_at(t, k));
-                rtr[k] = *reinterpret_cast<const uint4*>(reinterpret_cast<const float*>(slot + SL_RT) + img_at(t, k));
-            }
             wA.wait();   // L and the small record
             const bool fb = reinterpret_cast<const int*>(small)[C + D] != 0;
             const float gl = small[C + t.qrow];
@@ -1587,15 +1601,6 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
             }
             wV.wait();   // V
             if ((warp & 3) < 2) x_epilogue(t, small, CON_X);
-            {   // DT and R^T (loaded at the chunk's start) into TMEM
-                uint32_t v[16];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) { v[4 * k] = dtr[k].x; v[4 * k + 1] = dtr[k].y; v[4 * k + 2] = dtr[k].z; v[4 * k + 3] = dtr[k].w; }
-                tc::st16(tc::taddr(t.tm, warp, TM_DT + t.grp * 16), v);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) { v[4 * k] = rtr[k].x; v[4 * k + 1] = rtr[k].y; v[4 * k + 2] = rtr[k].z; v[4 * k + 3] = rtr[k].w; }
-                tc::st16(tc::taddr(t.tm, warp, TM_RT + t.grp * 16), v);
-            }
             publish();
             if (tid == kCStager) {
                 // every read of chunk ci's slot is done: its producer may refill it
@@ -1603,10 +1608,14 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
                 if (have_next) load_v(ci + 1);
             }
             if (tid == 0) mma2(t, CON_X, s_bar2);
+            const bool more = ci + 1 < nchunks;
+            if (more) load_dtrt(ci + 1);   // its slot was acquired before the barrier above
             wt2.wait();   // MMA2
+            if (more) store_tm(dtr, TM_DT);
             if ((warp & 3) < 2) u_operand_mma3(t, CON_U, s_bar3);
             else out_epilogue(t, CON_OG, p.rms_eps, n, false, nullptr, 0, maps, h, t0, b);
             wt3.wait();   // MMA3
+            if (more) store_tm(rtr, TM_RT);
             esc_prev = __expf(fb ? 0.f : 0.5f * gl);   // e^{G_last - rho_R}
             tc::fence_before();
             const bool stop = __syncthreads_or(*(volatile int*)s_dead) != 0;
