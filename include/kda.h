@@ -57,6 +57,10 @@
  *    "split_drop" (not part of "all") makes the producers of kda_prefill's
  *    split schedule skip publishing their first chunk: the consumers' bounded
  *    waits run out, with the same report and S and window unchanged.
+ *    "split_nofit" (not part of "all") makes kda_prefill treat the split
+ *    schedule's launch as not fitting on the device, as when fewer SMs are
+ *    available to the process than the device has: the relay pairs run
+ *    instead, with the same results.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -199,7 +203,8 @@ KDA_API size_t kda_prefill_workspace_bytes(const kda_ctx *ctx, int B, int T);
  * workspace to one consumer CTA per pair, which keeps the state and runs the
  * sequential part (one cooperative launch: all its CTAs are resident at once;
  * it needs the device's SMs free of other work to start); with less, or none,
- * two CTAs per pair take alternate chunks and hand the state to each other.
+ * or when that launch cannot be resident at once on the device, two CTAs per
+ * pair take alternate chunks and hand the state to each other.
  * All schedules compute the same arithmetic in the same order, so results are
  * bit for bit the same whichever runs.
  * After a give-up (KDA_ERR_TIMEOUT from kda_sync_status) an affected pair

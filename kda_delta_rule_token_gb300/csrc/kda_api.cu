@@ -11,8 +11,10 @@
 // name "relay_drop" (not part of "all") instead makes kda_prefill's relay
 // pairs skip their first state hand-over, and "split_drop" (not part of
 // "all") makes the producers of its split schedule skip publishing their
-// first chunk, so that a bounded wait inside the kernel runs out.  Unset or
-// empty: no injection.
+// first chunk, so that a bounded wait inside the kernel runs out;
+// "split_nofit" makes kda_prefill treat the split schedule's cooperative
+// launch as not fitting on the device (it then runs the relay pairs).  Unset
+// or empty: no injection.
 #include <atomic>
 #include <cmath>
 #include <cstdio>
@@ -66,7 +68,7 @@ kda_status check_device(const kda_ctx* ctx) {
 
 constexpr unsigned kInjectDecode = 1u, kInjectPrefill = 2u, kInjectVarlen = 4u, kInjectLowrank = 8u,
                    kInjectProject = 16u, kInjectRelayDrop = 32u,
-                   kInjectSplitDrop = 64u;
+                   kInjectSplitDrop = 64u, kInjectSplitNofit = 128u;
 
 // Parse KDA_FAULT_INJECT (see the top of this file).
 unsigned parse_inject(const char* v) {
@@ -85,6 +87,7 @@ unsigned parse_inject(const char* v) {
         else if (is("project")) m |= kInjectProject;
         else if (is("relay_drop")) m |= kInjectRelayDrop;
         else if (is("split_drop")) m |= kInjectSplitDrop;
+        else if (is("split_nofit")) m |= kInjectSplitNofit;
         else if (is("all")) m |= kInjectDecode | kInjectPrefill | kInjectVarlen | kInjectLowrank | kInjectProject;
         p = *e ? e + 1 : e;
     }
@@ -265,7 +268,7 @@ kda_status kda_prefill(kda_ctx* ctx, int B, int T, const uint16_t* q, const uint
     if (const kda_status d = check_device(ctx); d != KDA_OK) return d;
     kda::PrefillIO io{B, T, nullptr, q, k, v, z, beta_logit, gate_logit, conv_state, S, o,
                       workspace, workspace_bytes, 0, (ctx->inject & kda::kInjectRelayDrop) ? 1 : 0,
-                      (ctx->inject & kda::kInjectSplitDrop) ? 1 : 0};
+                      (ctx->inject & kda::kInjectSplitDrop) ? 1 : 0, (ctx->inject & kda::kInjectSplitNofit) ? 1 : 0};
     cudaError_t e = kda::launch_or_inject(ctx, kda::kInjectPrefill, [&] {
         return kda::launch_prefill(ctx->params, io, ctx->dev, ctx->err_word, static_cast<cudaStream_t>(stream));
     });

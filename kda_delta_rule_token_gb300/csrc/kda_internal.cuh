@@ -67,6 +67,10 @@ struct PrefillIO {
     // split schedule do not publish their first chunk, so its consumer's
     // bounded wait runs out.
     int drop_split;
+    // Test injection (KDA_FAULT_INJECT "split_nofit"): the split schedule's
+    // cooperative launch is treated as not fitting on the device, so the
+    // relay pairs run instead.
+    int nofit_split;
 };
 
 // Low-rank front-end weights bound to a context (borrowed, fp32), with

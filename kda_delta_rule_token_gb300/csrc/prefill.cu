@@ -1771,10 +1771,17 @@ cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const Devi
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, kda_prefill_split_kernel, p, io, err_word, maps, sp);
-        count_launches(1);
-        if (e != cudaSuccess) return e;
-        return cudaGetLastError();
+        cudaError_t e = io.nofit_split ? cudaErrorCooperativeLaunchTooLarge
+                                       : cudaLaunchKernelEx(&cfg, kda_prefill_split_kernel, p, io, err_word, maps, sp);
+        if (e == cudaSuccess) {
+            count_launches(1);
+            return cudaGetLastError();
+        }
+        if (e != cudaErrorCooperativeLaunchTooLarge) return e;
+        // The launch cannot be resident all at once on the device as this
+        // process sees it (fewer SMs than the device has): the same heads run
+        // as relay pairs instead, with the same results.
+        (void)cudaGetLastError();
     }
     if (rh > 0) {
         // The heads [single, grid) as CTA pairs, each pair one cluster of two

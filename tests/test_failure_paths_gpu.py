@@ -14,6 +14,10 @@
   a state the second never sends; both give up, drain what they issued and
   leave; kda_sync_status reports KDA_ERR_TIMEOUT, S and the window keep their
   old contents, and the device keeps working.
+* A split launch that does not fit: with KDA_FAULT_INJECT=split_nofit the
+  split schedule's cooperative launch is treated as not fitting on the
+  device; the call runs the relay pairs instead, one launch, and gives the
+  same results bit for bit.
 * A chunk that is never published: with KDA_FAULT_INJECT=split_drop the
   producers of the split schedule skip publishing their first chunk, so each
   consumer's bounded wait for its head's first chunk runs out; the same
@@ -265,3 +269,34 @@ def test_split_chunk_that_is_never_published_times_out(inject, monkeypatch):
         assert not torch.equal(S, S0)
     finally:
         kda.kda_destroy(ctx)
+
+
+def test_split_launch_that_does_not_fit_falls_back_to_relay_pairs(inject, monkeypatch):
+    wl = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], B=2, H=8, T=300)   # 16 heads, split schedule
+    params, tokens = synth.make_params(wl, DEV), synth.make_tokens(wl, DEV)
+    st = synth.make_state(wl, DEV)
+    S0, c0 = st["S"].normal_(0.0, 0.01).clone(), st["conv_state"].clone()
+    q, k, v = (tokens[n].view(torch.int16) for n in ("q", "k", "v"))
+    res = {}
+    for what in ("", "split_nofit"):
+        if what:
+            inject(what)
+        else:
+            monkeypatch.delenv("KDA_FAULT_INJECT", raising=False)
+        S, conv = S0.clone(), c0.clone()
+        o = torch.zeros((wl.B, wl.T, wl.H, 128), device=DEV)
+        ctx = _create(wl, params)
+        try:
+            nws = kda.kda_prefill_workspace_bytes(ctx, wl.B, wl.T)
+            assert nws > 0
+            ws = torch.empty(nws, dtype=torch.uint8, device=DEV)
+            n0 = kda.kda_launch_count()
+            kda.kda_prefill(ctx, wl.B, wl.T, q, k, v, tokens["z"], tokens["beta_logit"], tokens["gate_logit"],
+                            conv, S, o, ws, nws)
+            assert kda.kda_sync_status(ctx) == kda.KDA_OK
+            assert kda.kda_launch_count() == n0 + 1
+        finally:
+            kda.kda_destroy(ctx)
+        res[what] = (o, S, conv)
+    for a, b in zip(res[""], res["split_nofit"]):
+        assert torch.equal(a, b)
