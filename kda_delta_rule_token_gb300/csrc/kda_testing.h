@@ -23,10 +23,10 @@ KDA_API kda_status kda_testing_bounded_wait(kda_ctx *ctx, unsigned limit_us, voi
 /*
  * Launch policies, computed on the host without a device:
  * kda_testing_prefill_relay_heads: how many of `heads` (sequence, head)
- * pairs of a T-token kda_prefill run as relay pairs (two CTAs, alternate
- * chunks) on sm_count SMs: all when twice their number fits, else those of a
- * last partial wave that fills at most half of the SMs, none for a single
- * chunk.  kda_testing_project_o_ksplit: the K ranges of kda_project_o on N
+ * pairs of a T-token kda_prefill run on the few-head schedule (the split
+ * schedule with a workspace, else relay pairs) on sm_count SMs: all when
+ * twice their number fits, else those of a last partial wave that fills at
+ * most half of the SMs, none for a single chunk.  kda_testing_project_o_ksplit: the K ranges of kda_project_o on N
  * tokens (2 when its hidden / 128 x token-tile output tiles fill at most half
  * of the SMs and HD spans at least 16 slices of 64, else 1).  -1 on a
  * negative argument.
