@@ -1291,10 +1291,13 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
 // a ring of slots in the caller's workspace, to one consumer CTA per
 // (sequence, head), which keeps the state in TMEM and runs only the chain
 // (state pass, MMA1, X epilogue, MMA2, U operand, MMA3, output epilogue).
-// All CTAs of the launch are resident at once (cooperative launch), producers
-// take the chunk-major item list in a fixed stride, and every wait on another
-// CTA is bounded, so a chunk's producer never waits on a consumer that waits
-// on a later chunk (the lowest unfinished item can always finish).
+// All CTAs of the launch are resident at once (cooperative launch).  Each
+// producer takes every nprod-th item of the chunk-major list (chunk c of head
+// h is item c * heads + h) in increasing order and waits for a free slot only
+// at an item's start, when it holds no unpublished item: the lowest
+// unfinished item then always finishes (what it waits for belongs to lower
+// items), so the schedule makes progress.  Every wait on another CTA is also
+// bounded, so a lost item ends as a timeout, not a hang.
 // ---------------------------------------------------------------------------
 constexpr int kRing = 4;   // slots per head
 // A slot: L (tf32, SW128 as in shared memory), V (fp32, SW128), DT and R^T
