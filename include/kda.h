@@ -239,9 +239,12 @@ KDA_API kda_status kda_prefill(kda_ctx *ctx, int B, int T,
  *   o            [total_T][H][d] fp32 (out)
  * Alignment as for kda_prefill; cu_seqlens 4-byte aligned.  A sequence of
  * length 0 leaves its state and window unchanged; B == 0 or total_T == 0 is a
- * no-op returning KDA_OK.  Needs no workspace.  Sequences are isolated: no
- * value of one sequence's inputs, not even a NaN or an infinity, changes
- * another sequence's o, S or window.  Give-ups behave as for kda_prefill.
+ * no-op returning KDA_OK.  Needs no workspace.  When twice the number of
+ * sequence-heads (B x H) fits on the device's SMs, each runs as two CTAs
+ * that take alternate chunks (the relay pairs of kda_prefill); else one CTA
+ * each.  Sequences are isolated: no value of one sequence's inputs, not
+ * even a NaN or an infinity, changes another sequence's o, S or window.
+ * Give-ups behave as for kda_prefill.
  */
 KDA_API kda_status kda_prefill_varlen(kda_ctx *ctx, int B, const int32_t *cu_seqlens, int total_T,
                        const uint16_t *q, const uint16_t *k, const uint16_t *v,

@@ -1687,8 +1687,10 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esiz
 // Heads that would leave SMs idle as single CTAs: all of them when twice
 // their number fits on the SMs (few-head workloads: otherwise most SMs
 // idle), else the heads of a last, partial wave when it fills at most half
-// of the SMs; none for single-chunk sequences or packed ones.  They run on
-// the split schedule when the caller gives its workspace, else as relay pairs.
+// of the SMs; none for single-chunk sequences.  They run on the split
+// schedule when the caller gives its workspace, else as relay pairs.  (Packed
+// calls, whose lengths only the device knows, use relay pairs for all their
+// sequence-heads when twice their number fits, else none; see launch_prefill.)
 long long relay_heads(long long heads, int nchunks, int sm_count) {
     if (nchunks < 2 || sm_count < 2) return 0;
     if (2 * heads <= sm_count) return heads;
@@ -1740,7 +1742,10 @@ cudaError_t launch_prefill(const LayerParams& p, const PrefillIO& io, const Devi
                   CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int nchunks = (io.T + C - 1) / C;
-    const long long rh = io.cu_seqlens ? 0 : relay_heads(grid, nchunks, dev.sm_count);
+    // Packed sequences (their lengths are on the device): relay pairs for all
+    // sequence-heads when twice their number fits on the SMs, else none.
+    const long long rh = io.cu_seqlens ? (2 * grid <= dev.sm_count ? grid : 0)
+                                       : relay_heads(grid, nchunks, dev.sm_count);
     const long long single = grid - rh;
     const bool split = rh > 0 && rh < dev.sm_count && io.workspace != nullptr && io.workspace_bytes >= split_bytes(rh);
     if (single > 0) {
