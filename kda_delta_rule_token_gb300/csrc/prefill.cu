@@ -599,29 +599,38 @@ __device__ __forceinline__ void lr_build(const Thr& t, bool fb, float* rt_img) {
     }
 }
 
+// The MMA issue loops below are fully unrolled and add constant offsets to
+// one base descriptor per operand: a rolled loop, or a descriptor rebuilt
+// from the address per instruction, roughly halves the issue rate.
+
 // ---- MMA0: [A'; P] = L R^T (one thread issues).
 __device__ __forceinline__ void mma0(const Thr& t, uint64_t* bar) {
     constexpr uint32_t id = tc::idesc_tf32(128, 64);
-#pragma unroll 1
+    const uint64_t da = tc::desc_sw128(ptx::smem_u32(t.sm + OFF_L));
+    const uint64_t db = tc::desc_sw128(ptx::smem_u32(t.sm + OFF_R));
+#pragma unroll
     for (int ks = 0; ks < D / 8; ++ks) {
         const int kb = ks >> 2, kin = ks & 3;
-        tc::mma_ss(t.tm + TM_D0, tc::desc_sw128(ptx::smem_u32(t.sm + OFF_L + kb * 16384 + kin * 32)),
-                   tc::desc_sw128(ptx::smem_u32(t.sm + OFF_R + kb * 8192 + kin * 32)), id, ks > 0);
+        tc::mma_ss(t.tm + TM_D0, tc::desc_add(da, kb * 16384 + kin * 32), tc::desc_add(db, kb * 8192 + kin * 32), id,
+                   ks > 0);
     }
     tc::commit(bar);
 }
 
 // ---- MMA1: D1 = L (Diag(e^rho_L) S0) = [K_g S0; Q_g S0], K blocks
-//      [2 half, 2 half + 2) (one thread issues; half 1 commits to bar1).
-__device__ __forceinline__ void mma1_part(const Thr& t, int half, uint64_t* bar1) {
+//      [2 HALF, 2 HALF + 2) (one thread issues; half 1 commits to bar1).
+template <int HALF>
+__device__ __forceinline__ void mma1_part(const Thr& t, uint64_t* bar1) {
     constexpr uint32_t id = tc::idesc_tf32(128, 128);
-#pragma unroll 1
-    for (int ks = half * 8; ks < half * 8 + 8; ++ks) {
+    const uint64_t da = tc::desc_sw128(ptx::smem_u32(t.sm + OFF_L));
+    const uint64_t db = tc::desc_sw128(ptx::smem_u32(t.sm + OFF_ST));
+#pragma unroll
+    for (int ks = HALF * 8; ks < HALF * 8 + 8; ++ks) {
         const int kb = ks >> 2, kin = ks & 3;
-        tc::mma_ss(t.tm + TM_D1, tc::desc_sw128(ptx::smem_u32(t.sm + OFF_L + kb * 16384 + kin * 32)),
-                   tc::desc_sw128(ptx::smem_u32(t.sm + OFF_ST + kb * 16384 + kin * 32)), id, ks > 0);
+        tc::mma_ss(t.tm + TM_D1, tc::desc_add(da, kb * 16384 + kin * 32), tc::desc_add(db, kb * 16384 + kin * 32), id,
+                   ks > 0);
     }
-    if (half == 1) tc::commit(bar1);
+    if (HALF == 1) tc::commit(bar1);
 }
 
 // ---- C1: N = Diag(beta) A' to shared memory as N^T (row b holds column b
@@ -758,11 +767,11 @@ __device__ __forceinline__ void inverse_mma_t(const Thr& t, uint64_t* barT) {
         if (tid == kIssuerB) {
             tc::fence_after();
             constexpr uint32_t id = tc::idesc_tf32(128, 64);
-#pragma unroll 1
+            const uint64_t db = tc::desc_sw128(ptx::smem_u32(sm + OFF_MT));
+#pragma unroll
             for (int ks = 0; ks < C / 8; ++ks) {
                 const int kb = ks >> 2, kin = ks & 3;
-                tc::mma_ts(t.tm + TM_DT, t.tm + TM_D0 + ks * 8,
-                           tc::desc_sw128(ptx::smem_u32(sm + OFF_MT + kb * 8192 + kin * 32)), id, ks > 0);
+                tc::mma_ts(t.tm + TM_DT, t.tm + TM_D0 + ks * 8, tc::desc_add(db, kb * 8192 + kin * 32), id, ks > 0);
             }
             tc::commit(barT);
         }
@@ -822,11 +831,11 @@ __device__ __forceinline__ void x_epilogue(const Thr& t, const float* beta, uint
 //      MMA costs about the same per instruction at N = 64 and 128).
 __device__ __forceinline__ void mma2(const Thr& t, uint32_t x_off, uint64_t* bar2) {
     constexpr uint32_t id = tc::idesc_tf32(128, 128);
-#pragma unroll 1
+    const uint64_t db = tc::desc_sw128(ptx::smem_u32(t.sm + x_off));
+#pragma unroll
     for (int ks = 0; ks < C / 8; ++ks) {
         const int kb = ks >> 2, kin = ks & 3;
-        tc::mma_ts(t.tm + TM_D1, t.tm + TM_DT + ks * 8,
-                   tc::desc_sw128(ptx::smem_u32(t.sm + x_off + kb * 16384 + kin * 32)), id, 1u);
+        tc::mma_ts(t.tm + TM_D1, t.tm + TM_DT + ks * 8, tc::desc_add(db, kb * 16384 + kin * 32), id, 1u);
     }
     tc::commit(bar2);
 }
@@ -868,11 +877,11 @@ __device__ __forceinline__ void u_operand_mma3(const Thr& t, uint32_t u_off, uin
     if (t.tid == 0) {
         tc::fence_after();
         constexpr uint32_t id = tc::idesc_tf32(128, 128);
-#pragma unroll 1
+        const uint64_t db = tc::desc_sw128(ptx::smem_u32(sm + u_off));
+#pragma unroll
         for (int ks = 0; ks < C / 8; ++ks) {
             const int kb = ks >> 2, kin = ks & 3;
-            tc::mma_ts(t.tm + TM_S, t.tm + TM_RT + ks * 8,
-                       tc::desc_sw128(ptx::smem_u32(sm + u_off + kb * 16384 + kin * 32)), id, 1u);
+            tc::mma_ts(t.tm + TM_S, t.tm + TM_RT + ks * 8, tc::desc_add(db, kb * 16384 + kin * 32), id, 1u);
         }
         tc::commit(bar3);
     }
@@ -1154,14 +1163,14 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // MMA1 (runs under the inverse) is issued by warp 10 in two halves: K
         // blocks 0, 1 before C1 and 2, 3 after it (warp 10 has little work in
         // C1 and C2).
-        if (!RELAY && tid == kIssuer1) mma1_part(t, 0, s_bar1);
+        if (!RELAY && tid == kIssuer1) mma1_part<0>(t, s_bar1);
         if (!fb) wt.wait();   // MMA0
 
         c1_pass(t);
         tc::wait_st();
         sync_tc();
 
-        if (!RELAY && tid == kIssuer1) mma1_part(t, 1, s_bar1);
+        if (!RELAY && tid == kIssuer1) mma1_part<1>(t, s_bar1);
 
         inverse_mma_t(t, s_tbarT);
         if constexpr (RELAY) {
@@ -1175,8 +1184,8 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
             state_pass(t, esc_prev, ci > 0, fb, t.s_gh0[qrow] + t.s_gh1[qrow], s_rxesc);
             publish();
             if (tid == kIssuer1) {
-                mma1_part(t, 0, s_bar1);
-                mma1_part(t, 1, s_bar1);
+                mma1_part<0>(t, s_bar1);
+                mma1_part<1>(t, s_bar1);
             }
         }
         wt1.wait();   // MMA1
@@ -1588,8 +1597,8 @@ kda_prefill_split_kernel(const LayerParams p, const PrefillIO io, int* err, cons
             state_pass(t, esc_prev, false, fb, gl, nullptr);
             publish();   // S^T operand, rescaled master
             if (tid == kIssuer1) {
-                mma1_part(t, 0, s_bar1);
-                mma1_part(t, 1, s_bar1);
+                mma1_part<0>(t, s_bar1);
+                mma1_part<1>(t, s_bar1);
             }
             // under MMA1: the gate tile becomes gamma sigmoid(gate) (warps 1..15)
             wgate.wait();

@@ -37,6 +37,16 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// The descriptor of the operand `off` bytes (a multiple of 16) past the one
+// `d` describes.  The start-address field holds bits 4..17 of the
+// shared-memory address and every operand lies below 256 KiB, so the sum
+// never carries out of the field.  Issue loops that add constant offsets to
+// one base descriptor and are fully unrolled issue an MMA every 45-64 cycles
+// (the tensor pipe's own rate for tf32 at N = 64..128); the same loop kept
+// rolled, or rebuilding the descriptor from the address each time, issues
+// one every 87-127 cycles, and a single issuing thread then sets the pace.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); }
+
 // Instruction descriptor: kind::tf32, D = f32, A = B = tf32, both K-major.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
