@@ -1159,10 +1159,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         lr_build<false>(t, fb, nullptr);
         publish();
 
-        if (!fb && tid == 0) mma0(t, s_bar);
-        // MMA1 (runs under the inverse) is issued by warp 10 in two halves: K
-        // blocks 0, 1 before C1 and 2, 3 after it (warp 10 has little work in
-        // C1 and C2).
+        // MMA0, then MMA1 (which runs under the inverse) in two halves, K
+        // blocks 0, 1 before C1 and 2, 3 after it, all issued by warp 10 (it
+        // has little work in C1 and C2): MMA0 reaches the tensor pipe first,
+        // so C1 does not wait for MMA1 instructions interleaved with it, and
+        // the issuing thread, held at the pipe's rate, is not one C1 needs.
+        if (!fb && tid == (RELAY ? 0 : kIssuer1)) mma0(t, s_bar);
         if (!RELAY && tid == kIssuer1) mma1_part<0>(t, s_bar1);
         if (!fb) wt.wait();   // MMA0
 
