@@ -1135,6 +1135,12 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         // beta logits of the chunk, consumed after the conv phase.
         const float blog = tid < n ? io.beta_logit[(rowbase + t0 + tid) * H + h] : 0.f;
         wtma.wait();
+        // The o tile of the chunk before (K blocks 2, 3 of the L region, which
+        // the q and k conv write) must have left shared memory.
+        if (tid < 256) {
+            if (tid == kOStore) ptx::bulk_wait_read_all();
+            named_barrier_sync(5, 256);
+        }
         // the chunk before ran in the other CTA (relay): its last three inputs from global memory
         const bool big = conv_decay(t, cw, n, (RELAY && ci > 0) ? kWinInputs : kWinShared, ci & 1, true, xg,
                                     rowbase + (size_t)t0 - 3, HD, win);
@@ -1232,8 +1238,6 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         else out_epilogue(t, OFF_OG, p.rms_eps, n, direct, io.o + ((rowbase + t0) * H + h) * D, (size_t)H * D, maps,
                           h, tb0 + t0, bmap);
         wt3.wait();   // MMA3
-        // the next chunk's conv phase overwrites the tile: its reads must be done
-        if (tid == kOStore) ptx::bulk_wait_read_all();
 
         // S_new = e^{G_last - rho_R} M: the scale is carried in a register and
         // applied by the next chunk's state pass (or the final write-back).

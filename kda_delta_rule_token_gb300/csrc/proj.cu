@@ -44,7 +44,8 @@
 namespace kda {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kRingBudget = 192 * 1024;     // shared memory for the ring of stages
 constexpr int kKSlice = 64;                      // bf16 elements in one 128-byte swizzled row
 constexpr uint32_t kATile = 128 * 128;           // 128 weight rows x 128 bytes
 constexpr int kThreads = 192;                    // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
@@ -63,6 +64,7 @@ struct ProjArgs {
     int Nt;                 // token tile: 32, 64, 128 or 256
     int mtiles, ntiles;
     int ksplit;             // K halves per tile: 1, or 2 (fp32 output added into, zero on entry)
+    int stages;             // depth of the ring, ring_stages(Nt)
     int nsegs;              // outputs, each `len` consecutive features of M
     Seg seg[kMaxSegs];
 };
@@ -73,7 +75,17 @@ struct ProjMaps {
 };
 
 __host__ __device__ constexpr uint32_t stage_bytes(int Nt) { return kATile + (uint32_t)Nt * 128; }
-constexpr uint32_t proj_smem_bytes(int Nt) { return kStages * stage_bytes(Nt) + 1024; }
+// Ring depth: as many stages as 192 KiB holds, at most 8 (8 at 32 and 64
+// tokens, 6 at 128, 4 at 256).  A token-light call streams its weights at a
+// rate set by the bytes it keeps in flight per SM, so small tiles get more
+// stages.
+constexpr int ring_stages(int Nt) {
+    return (int)(kRingBudget / stage_bytes(Nt)) < kMaxStages ? (int)(kRingBudget / stage_bytes(Nt)) : kMaxStages;
+}
+constexpr uint32_t proj_smem_bytes(int Nt) { return ring_stages(Nt) * stage_bytes(Nt) + 1024; }
+constexpr uint32_t max_u32(uint32_t a, uint32_t b) { return a > b ? a : b; }
+constexpr uint32_t kMaxSmem = max_u32(max_u32(proj_smem_bytes(32), proj_smem_bytes(64)),
+                                      max_u32(proj_smem_bytes(128), proj_smem_bytes(256)));
 
 __device__ __forceinline__ void red_add(float* p, float v) {
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
@@ -104,9 +116,10 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
     extern __shared__ __align__(1024) uint8_t sm[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t sbytes = stage_bytes(g.Nt);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kStages * sbytes);   // slice landed
-    uint64_t* empty = full + kStages;                                      // slice consumed
-    uint64_t* accf = empty + kStages;                                      // [2] accumulator complete
+    const int S = g.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + S * sbytes);         // slice landed
+    uint64_t* empty = full + kMaxStages;                                   // slice consumed
+    uint64_t* accf = empty + kMaxStages;                                   // [2] accumulator complete
     uint64_t* acce = accf + 2;                                             // [2] accumulator read back
     uint64_t* drain = acce + 2;                                            // give-up path
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
@@ -124,7 +137,7 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
     const uint32_t ncols = 2u * (uint32_t)g.Nt;   // two accumulators
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
@@ -147,20 +160,22 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
     ptx::griddep_wait();
 
     if (tid == 0) {
-        // TMA producer: slices of every tile of this CTA, in order.
-        int it = 0;
+        // TMA producer: slices of every tile of this CTA, in order; slice it
+        // goes to stage s = it % S, rp = parity of it / S.
+        int it = 0, s = 0;
+        uint32_t rp = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
             int mt, nt, k0, k1;
             raster(g, u / g.ksplit, mt, nt);
             krange(u, k0, k1);
             for (int i = k0; i < k1; ++i, ++it) {
-                const int s = it % kStages;
-                if (it >= kStages && !pwait(&empty[s], (uint32_t)((it / kStages - 1) & 1), s_dead, err)) goto done_p;
+                if (it >= S && !pwait(&empty[s], rp ^ 1u, s_dead, err)) goto done_p;
                 uint8_t* st = sm + s * sbytes;
                 ptx::mbar_arrive_expect_tx(&full[s], sbytes);
                 ptx::tma_load_2d(st, &maps.w, i * kKSlice, mt * 128, &full[s]);
                 ptx::tma_load_2d(st + kATile, &maps.x, i * kKSlice, nt * g.Nt, &full[s]);
                 *s_issued = it + 1;
+                if (++s == S) { s = 0; rp ^= 1u; }
             }
         }
     done_p:;
@@ -168,7 +183,8 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
         // MMA issuer: tile j accumulates into TMEM columns [(j & 1) Nt, + Nt)
         // once the epilogue has read that accumulator's previous tile.
         const uint32_t id = tc::idesc_bf16(128, g.Nt);
-        int it = 0, j = 0;
+        int j = 0, s = 0;
+        uint32_t rp = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
             const int b = j & 1;
             if (j >= 2 && !pwait(&acce[b], (uint32_t)(((j >> 1) - 1) & 1), s_dead, err)) break;
@@ -177,16 +193,17 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
             int k0, k1;
             krange(u, k0, k1);
             bool ok = true;
-            for (int i = k0; i < k1; ++i, ++it) {
-                const int s = it % kStages;
-                if (!pwait(&full[s], (uint32_t)((it / kStages) & 1), s_dead, err)) { ok = false; break; }
+            for (int i = k0; i < k1; ++i) {
+                if (!pwait(&full[s], rp, s_dead, err)) { ok = false; break; }
                 tc::fence_after();
-                const uint32_t a = ptx::smem_u32(sm + s * sbytes), bb = a + kATile;
+                const uint64_t da = tc::desc_sw128(ptx::smem_u32(sm + s * sbytes));
+                const uint64_t db = tc::desc_add(da, kATile);
 #pragma unroll
                 for (int kin = 0; kin < 4; ++kin)
-                    tc::mma_ss_bf16(d, tc::desc_sw128(a + kin * 32), tc::desc_sw128(bb + kin * 32), id,
+                    tc::mma_ss_bf16(d, tc::desc_add(da, kin * 32), tc::desc_add(db, kin * 32), id,
                                     (i > k0 || kin > 0) ? 1u : 0u);
                 tc::commit(&empty[s]);
+                if (++s == S) { s = 0; rp ^= 1u; }
             }
             tc::commit(&accf[b]);
             if (!ok) break;
@@ -264,8 +281,8 @@ kda_proj_gemm_kernel(const ProjArgs g, int* err, const __grid_constant__ ProjMap
         if (tid == 32) ptx::mbar_wait_timed(drain, 0);
         if (tid == 0) {
             const int issued = *s_issued;
-            for (int s = 0; s < kStages && s < issued; ++s) {
-                const int uses = (issued - s + kStages - 1) / kStages;
+            for (int s = 0; s < S && s < issued; ++s) {
+                const int uses = (issued - s + S - 1) / S;
                 ptx::mbar_wait_timed(&full[s], (uint32_t)((uses - 1) & 1));
             }
         }
@@ -337,7 +354,7 @@ cudaError_t run_proj(const CUtensorMap& wmap, int M, const void* x, int N, int K
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (!g_attr_done[dev.device].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kda_proj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)proj_smem_bytes(256));
+                                             (int)kMaxSmem);
         if (e != cudaSuccess) return e;
         g_attr_done[dev.device].store(true, std::memory_order_release);
     }
@@ -349,6 +366,7 @@ cudaError_t run_proj(const CUtensorMap& wmap, int M, const void* x, int N, int K
     g.mtiles = M / 128;
     g.ntiles = (N + g.Nt - 1) / g.Nt;
     g.ksplit = ksplit;
+    g.stages = ring_stages(g.Nt);
     g.nsegs = nsegs;
     for (int i = 0; i < nsegs; ++i) g.seg[i] = segs[i];
     ProjMaps maps{};
