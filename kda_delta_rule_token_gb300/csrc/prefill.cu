@@ -1156,29 +1156,34 @@ kda_prefill_kernel(const LayerParams p, const PrefillIO io, int* err, const __gr
         }
 
         norms(t, n, blog, p.l2_eps);
-
-        // ---- D: state pass (relay launches: later, once the state has arrived).
-        if (!RELAY) state_pass(t, esc_prev, false, fb, t.s_gh0[qrow] + t.s_gh1[qrow], s_rxesc);
-        publish();   // norms, beta; S^T operand and rescaled master
+        publish();   // norms, beta
 
         if (fb) exact_fallback(t);
         lr_build<false>(t, fb, nullptr);
         publish();
 
-        // MMA0, then MMA1 (which runs under the inverse) in two halves, K
-        // blocks 0, 1 before C1 and 2, 3 after it, all issued by warp 10 (it
-        // has little work in C1 and C2): MMA0 reaches the tensor pipe first,
-        // so C1 does not wait for MMA1 instructions interleaved with it, and
-        // the issuing thread, held at the pipe's rate, is not one C1 needs.
+        // MMA0 is issued by warp 10 (it has little work in C1 and C2) as soon
+        // as L and R are complete; every warp then runs the state pass under
+        // it (the pass reads and writes only the TMEM master and the S^T
+        // region, neither of which MMA0 touches), and warp 10 issues MMA1
+        // behind MMA0 (it runs under C1 and the inverse).  The tensor pipe
+        // takes MMA0 first, and the issuing thread, held at the pipe's rate,
+        // is not one C1 needs.
         if (!fb && tid == (RELAY ? 0 : kIssuer1)) mma0(t, s_bar);
-        if (!RELAY && tid == kIssuer1) mma1_part<0>(t, s_bar1);
+        if constexpr (!RELAY) {
+            // ---- D: state pass (relay launches: later, once the state has arrived)
+            state_pass(t, esc_prev, false, fb, t.s_gh0[qrow] + t.s_gh1[qrow], s_rxesc);
+            publish();   // S^T operand and rescaled master
+            if (tid == kIssuer1) {
+                mma1_part<0>(t, s_bar1);
+                mma1_part<1>(t, s_bar1);
+            }
+        }
         if (!fb) wt.wait();   // MMA0
 
         c1_pass(t);
         tc::wait_st();
         sync_tc();
-
-        if (!RELAY && tid == kIssuer1) mma1_part<1>(t, s_bar1);
 
         inverse_mma_t(t, s_tbarT);
         if constexpr (RELAY) {
