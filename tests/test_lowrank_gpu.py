@@ -5,7 +5,9 @@ per output tensor.  Each product runs as three tf32 products (hi*hi + hi*lo
 + lo*hi of the split a = hi + lo), whose error is below 2^-19 of |a b|, and
 the fp32 accumulation adds about K * 2^-24 of the sum of |a b| at worst; for
 N(0, 1) inputs with the 1/sqrt(K) weight scale that is a few 1e-6 of
-max|z| at K = 7168, so 2e-5 leaves a margin of several times.
+max|z| at K = 7168, so 2e-5 leaves a margin of several times.  The cases
+span one to 1,000 tokens (token tiles of 32 to 256), ragged hidden, rank and
+H, and the largest rank (512).
 kda_decode_step_lowrank: the decode tolerance, max relative error 1e-4 on o
 at every call and on S after the last call, per (sequence, head), against
 the oracle's front-end followed by the oracle's token step.
@@ -51,7 +53,8 @@ def run_lowrank(ctx, H, x2d):
 
 
 @pytest.mark.parametrize("N,hidden,rank,H", [(5, 96, 32, 3), (64, 7168, 128, 32), (256, 7168, 128, 64),
-                                             (1000, 512, 64, 4), (300, 100, 36, 2)])
+                                             (1000, 512, 64, 4), (300, 100, 36, 2), (64, 100, 36, 3),
+                                             (65, 7168, 128, 32), (1, 7168, 512, 5), (33, 2052, 508, 7)])
 def test_lowrank_matches_oracle(N, hidden, rank, H):
     wl = synth.shrink(synth.WORKLOADS["decode_b64_h32_x256"], B=N, H=H, T=1)
     params = synth.make_params(wl, DEV)
