@@ -68,15 +68,19 @@ def source_sha(*names):
     return h.hexdigest()[:16]
 
 
-def profile_traffic(md_name, sha):
-    """DRAM bytes per launch recorded by an ncu capture in profiles/<md_name>,
-    or None when missing or taken on another version of the kernel source."""
+PROJ_MD = "proj_decode_b64_h32_prefill_b8_h64_traffic.md"
+
+
+def profile_traffic(md_name, sha, label="per launch (full workload)"):
+    """DRAM bytes per launch (or per call, by `label`) recorded by an ncu
+    capture in profiles/<md_name>, or None when missing or taken on another
+    version of the kernel source."""
     p = os.path.join(ROOT, "profiles", md_name)
     if not os.path.exists(p):
         return None
     text = open(p).read()
     m_sha = re.search(r"kernel source sha256\[:16\]:\s*([0-9a-f]{16})", text)
-    m_tr = re.search(r"dram bytes per launch \(full workload\):\s*([0-9.eE+]+)", text)
+    m_tr = re.search(r"dram bytes " + re.escape(label) + r":\s*([0-9.eE+]+)", text)
     if not m_sha or not m_tr or m_sha.group(1) != sha:
         return None
     return float(m_tr.group(1))
@@ -962,6 +966,8 @@ def main():
 
     dsha = source_sha("decode.cu")
     psha = source_sha("prefill.cu", "ptx.cuh", "tc.cuh")
+    lsha = source_sha("lowrank.cu", "ptx.cuh", "tc.cuh")
+    prsha = source_sha("proj.cu", "ptx.cuh", "tc.cuh")
     line = {"metric": METRIC}
     if head is not None:
         wl = head["wl"]
@@ -1011,7 +1017,8 @@ def main():
                 "ms_per_call": round(dlr["ms_frontend"], 5), "gpu_launches": dlr["launches_frontend"],
                 "tflops_algorithmic": round(dlr["fe_flop"] / (dlr["ms_frontend"] * 1e-3) / 1e12, 3),
                 "roofline": {"bound": "hbm", "achieved": round(fe_gbs, 1), "peak": peaks["hbm_gbs"],
-                             "unit": "GB/s", "frac": round(fe_gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                             "unit": "GB/s", "frac": round(fe_gbs / peaks["hbm_gbs"], 4),
+                             "traffic": profile_traffic("lowrank_b64_h32_kda_lowrank_gemm_kernel.md", lsha),
                              "kernel": "kda_lowrank_gemm_kernel + kda_lowrank_reduce_kernel",
                              "alg_bytes_per_call": dlr["fe_bytes"]},
             },
@@ -1043,27 +1050,29 @@ def main():
         gin = r["bytes_in"] / (r["ms_in"] * 1e-3) / 1e9
         gout = r["bytes_out"] / (r["ms_out"] * 1e-3) / 1e9
         big = r["N"] > 4096
+        tr_in = profile_traffic(PROJ_MD, prsha, f"per call (qkvg, {w.name})")
+        tr_out = profile_traffic(PROJ_MD, prsha, f"per call (o, {w.name})")
         blk = {
             "workload": f"{w.name}: {r['N']} tokens, hidden {r['hidden']}, H={r['H']}, bf16 operands, fp32 accumulation",
             "qkvg": {"ms_per_call": round(r["ms_in"], 4), "tflops": round(tin, 1), "gbs": round(gin, 1),
                      "gpu_launches": r["launches_in"],
                      "roofline": ({"bound": "tensor", "achieved": round(tin, 1), "peak": peaks["bf16_tflops"],
                                    "unit": "TFLOP/s", "frac": round(tin / peaks["bf16_tflops"], 4),
-                                   "peak_src": peaks["src"] + " bf16_tflops (burst)", "traffic": None}
+                                   "peak_src": peaks["src"] + " bf16_tflops (burst)", "traffic": tr_in}
                                   if big else
                                   {"bound": "hbm", "achieved": round(gin, 1), "peak": peaks["hbm_gbs"],
                                    "unit": "GB/s", "frac": round(gin / peaks["hbm_gbs"], 4),
-                                   "peak_src": peaks["src"] + " hbm_gbs", "traffic": None}),
+                                   "peak_src": peaks["src"] + " hbm_gbs", "traffic": tr_in}),
                      "kernel": "kda_proj_gemm_kernel"},
             "o": {"ms_per_call": round(r["ms_out"], 4), "tflops": round(tout, 1), "gbs": round(gout, 1),
                   "gpu_launches": r["launches_out"],
                   "roofline": ({"bound": "tensor", "achieved": round(tout, 1), "peak": peaks["bf16_tflops"],
                                 "unit": "TFLOP/s", "frac": round(tout / peaks["bf16_tflops"], 4),
-                                "peak_src": peaks["src"] + " bf16_tflops (burst)", "traffic": None}
+                                "peak_src": peaks["src"] + " bf16_tflops (burst)", "traffic": tr_out}
                                if big else
                                {"bound": "hbm", "achieved": round(gout, 1), "peak": peaks["hbm_gbs"],
                                 "unit": "GB/s", "frac": round(gout / peaks["hbm_gbs"], 4),
-                                "peak_src": peaks["src"] + " hbm_gbs", "traffic": None}),
+                                "peak_src": peaks["src"] + " hbm_gbs", "traffic": tr_out}),
                   "kernel": "kda_to_bf16_kernel + kda_proj_gemm_kernel"},
         }
         if "ms_cublas_in" in r:
