@@ -44,3 +44,17 @@ def test_profile_traffic_only_for_the_captured_source(tmp_path, monkeypatch):
     assert bench.profile_traffic("k.md", "fedcba9876543210") is None
     assert bench.profile_traffic("missing.md", "0123456789abcdef") is None
 
+
+
+def test_profile_traffic_per_call_labels(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "p.md").write_text("kernel source sha256[:16]: 0123456789abcdef\n"
+                               "dram bytes per call (qkvg, decode_b64_h32_x256): 238811392\n"
+                               "dram bytes per call (o, decode_b64_h32_x256): 62164992\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = "0123456789abcdef"
+    assert bench.profile_traffic("p.md", sha, "per call (qkvg, decode_b64_h32_x256)") == 238811392.0
+    assert bench.profile_traffic("p.md", sha, "per call (o, decode_b64_h32_x256)") == 62164992.0
+    assert bench.profile_traffic("p.md", sha, "per call (o, prefill_b8_h64_t8192)") is None
+    assert bench.profile_traffic("p.md", sha) is None   # no per-launch line in this file
