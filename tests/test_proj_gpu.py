@@ -17,6 +17,8 @@ Tolerances, from that arithmetic:
   the unrounded o, the bf16 rounding itself, RMS relative error 2^-8 /
   sqrt(12) times the mean of 1/mantissa (about 1.6e-3 for normal inputs),
   must stay within rel-L2 2.5e-3.
+The cases span the token tiles 32, 64, 128 and 256 (rings of 8, 8, 6 and 4
+stages) and K ranges shorter than the ring.
 """
 import numpy as np
 import pytest
@@ -49,7 +51,7 @@ def _wl(N, H):
     return synth.shrink(synth.WORKLOADS["decode_b64_h32_x256"], B=N, H=H, T=1)
 
 
-@pytest.mark.parametrize("N,hidden,H", [(5, 128, 2), (300, 256, 3), (64, 7168, 32), (1000, 384, 1)])
+@pytest.mark.parametrize("N,hidden,H", [(5, 128, 2), (300, 256, 3), (64, 7168, 32), (1000, 384, 1), (100, 512, 2)])
 @pytest.mark.parametrize("qkv_f32", [False, True])
 def test_project_qkvg_matches_oracle(N, hidden, H, qkv_f32):
     wl = _wl(N, H)
@@ -84,7 +86,8 @@ def test_project_qkvg_matches_oracle(N, hidden, H, qkv_f32):
     print(f"\n  N={N} hidden={hidden} H={H} qkv_f32={qkv_f32}: gate {eg:.2e}")
 
 
-@pytest.mark.parametrize("N,hidden,H", [(5, 128, 2), (64, 7168, 32), (700, 256, 4), (1, 7168, 32), (64, 1024, 64)])
+@pytest.mark.parametrize("N,hidden,H", [(5, 128, 2), (64, 7168, 32), (700, 256, 4), (1, 7168, 32), (64, 1024, 64),
+                                        (120, 768, 3)])
 def test_project_o_matches_oracle(N, hidden, H):
     """Includes calls that split K in two halves across CTAs (64 and 1 tokens
     at hidden 7168: 56 output tiles; hidden 1024 at H = 64: 8 tiles)."""
