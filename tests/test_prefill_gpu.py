@@ -255,8 +255,8 @@ def test_tail_wave_matches_oracle(schedule):
 
 
 @pytest.mark.parametrize("shape", [dict(B=1, H=32, T=4096), dict(B=2, H=100, T=333), dict(B=1, H=1, T=333),
-                                   dict(B=1, H=76, T=1000), dict(B=4, H=16, T=700)],
-                         ids=["single_seq", "tail", "one_head", "h76", "b4_h16"])
+                                   dict(B=1, H=76, T=1000), dict(B=4, H=16, T=700), dict(B=1, H=2, T=8192)],
+                         ids=["single_seq", "tail", "one_head", "h76", "b4_h16", "long_ring"])
 def test_schedules_agree_bit_for_bit(shape):
     """The split schedule, the relay pairs and single CTAs (the packed entry
     point runs one CTA per sequence-head) compute the same arithmetic in the
@@ -264,7 +264,8 @@ def test_schedules_agree_bit_for_bit(shape):
     single-sequence workload's full size; a tail wave with a ragged last
     chunk; one head (one consumer, as many producers as it has chunks); 76
     heads (as many producers as consumers: the producers set the pace); four
-    sequences of 16 heads."""
+    sequences of 16 heads; two heads of 128 chunks each (every head's ring of
+    four slots is refilled 32 times)."""
     wl = synth.shrink(synth.WORKLOADS["prefill_b1_h32_t4096"], **shape)
     params, tokens, S, conv = _setup(wl)
     S0, c0 = S.clone(), conv.clone()
